@@ -1,0 +1,471 @@
+"""Benchmark of the paged-KV attention hot path on GB300.
+
+Headline: a serving decode step on the Qwen2.5-7B-shaped workload (batch 32,
+8,192-token contexts, Hq=28, Hkv=4, D=128, 16-token pages in a 16,384-page
+pool): the eager writeback of each sequence's newest K/V row
+(``kv_write_paged``) followed by split-K decode (``attn_decode_paged``).
+``value`` is decode KV bytes read per second (sum of seq_len * Hkv * D * 2 * 2
+bytes per step / step time).  Extra measurements on the same line: the
+varlen causal prefill (TFLOP/s over visible pairs) and the mixed
+prefill+decode step, each against its roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU: every rank runs an independent replica on its own batch (the path
+has no exchange step), so scaling is weak and ``value`` sums all ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+from paged_kv_decode_17_gb300 import roofline  # noqa: E402
+
+METRIC = "paged decode KV-read GB/s (% of HBM peak); varlen prefill TFLOPS (% peak)"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ----------------------------------------------------------------------------- peaks
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def profile_traffic(name: str, source_files):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current kernel source (sha256 of the listed files); else None."""
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for f in source_files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    want = h.hexdigest()
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_sha256")):
+                k, v = line.strip().split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != want:
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (ctypes) every
+    few ms while running; read-only."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, interval_s=0.002):
+        self.interval = interval_s
+        self.samples = []
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            got = False
+            try:
+                props = torch.cuda.get_device_properties(torch.cuda.current_device())
+                bus = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+                got = nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+            except Exception:
+                got = False
+            if not got and nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
+                return
+            self.nv, self.h = nv, h
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = int(mx.value)
+            self.ok = True
+        except OSError:
+            pass
+
+    def _run(self):
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        getr = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0:
+                rs = int(r.value) if getr(self.h, ctypes.byref(r)) == 0 else 0
+                self.samples.append((int(c.value), rs))
+            time.sleep(self.interval)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "note": "NVML unavailable" if not self.ok else "no samples"}
+        mhz = [s[0] for s in self.samples]
+        reasons = set()
+        for _, rs in self.samples:
+            for bit, name in self.REASONS.items():
+                if rs & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        if torch.cuda.is_available():
+            pg.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            pg.barrier()
+
+
+def max_over_ranks(pg, x: float) -> float:
+    if pg is None:
+        return x
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(pg, x: float) -> float:
+    if pg is None:
+        return x
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle baseline
+def _compact_numpy(case, seqs):
+    """Pages of `seqs` copied to host numpy, table renumbered (input movement only)."""
+    import numpy as np
+    ps = case.page_size
+    idx, tables, lens, cu, rows = [], [], [], [0], []
+    cu_full = case.cu_seqlens_q.cpu().tolist()
+    nxt = 0
+    maxp = 1
+    for b in seqs:
+        L = case.seq_lens_host[b]
+        n = -(-L // ps)
+        idx.append(case.block_table[b, :n].long())
+        tables.append(list(range(nxt, nxt + n)))
+        nxt += n
+        maxp = max(maxp, n)
+        lens.append(L)
+        rows.extend(range(cu_full[b], cu_full[b + 1]))
+        cu.append(cu[-1] + cu_full[b + 1] - cu_full[b])
+    ii = torch.cat(idx)
+
+    def bits(t):
+        return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    bt = np.full((len(seqs), maxp), -1, dtype=np.int64)
+    for i, t in enumerate(tables):
+        bt[i, :len(t)] = t
+    rr = torch.tensor(rows, dtype=torch.long, device=case.q.device)
+    return dict(q_bits=bits(case.q[rr]), k_pool_bits=bits(case.k_pool[ii]), v_pool_bits=bits(case.v_pool[ii]),
+                block_table=bt, seq_lens=lens, cu_seqlens_q=np.array(cu), num_q_heads=case.num_q_heads,
+                num_kv_heads=case.num_kv_heads, page_size=ps, scale=case.softmax_scale)
+
+
+def oracle_decode_rate(case, budget_s=12.0, max_seqs=None):
+    """Time the fp64 CPU oracle on whole sequences of `case` until `budget_s`
+    of CPU work; returns (GB/s of KV, seconds, sequences done)."""
+    import oracle  # test infrastructure: only the CPU-baseline legs use it
+    done, t_total, nbytes = 0, 0.0, 0
+    B = case.batch
+    for b in range(B if max_seqs is None else min(B, max_seqs)):
+        args = _compact_numpy(case, [b])
+        t0 = time.perf_counter()
+        oracle.paged_attention(**args)
+        t_total += time.perf_counter() - t0
+        nbytes += roofline.decode_kv_bytes([case.seq_lens_host[b]], case.num_kv_heads, case.head_dim)
+        done += 1
+        if t_total >= budget_s:
+            break
+    return nbytes / t_total / 1e9, t_total, done
+
+
+def cpu_baseline_subprocess(budget_s=12.0):
+    """Run the oracle in a fresh single-threaded process (BLAS pinned to one
+    thread, so `cores` is exact)."""
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    code = ("import sys, json; sys.path.insert(0, %r); import bench, workloads; "
+            "c = workloads.qwen7b_decode(device='cpu'); "
+            "r = bench.oracle_decode_rate(c, %r); print('CPU_BASELINE', json.dumps(r))" % (ROOT, budget_s))
+    try:
+        out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+        for line in out.stdout.splitlines():
+            if line.startswith("CPU_BASELINE"):
+                gbs, secs, n = json.loads(line.split(" ", 1)[1])
+                return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                        "sample": "%d of 32 sequences (x 28 heads x 8192 tokens) of the qwen7b_decode batch, "
+                                  "fp64 numpy oracle, %.1f s" % (n, secs)}
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": "failed: %s" % (out.stderr.strip().splitlines()[-1:] or ["?"])[0]}
+    except Exception as e:  # pragma: no cover
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: %s" % e}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, rank, world, pg):
+    """The oracle as it stands, on the host cores, on the same workload and
+    metric; each step decodes a bounded sample (one sequence of the batch)."""
+    if rank != 0:
+        return
+    case = workloads.qwen7b_decode(device="cpu")
+    import oracle
+    times = []
+    nbytes = 0
+    for i in range(args.warmup + args.steps):
+        b = i % case.batch
+        a = _compact_numpy(case, [b])
+        t0 = time.perf_counter()
+        oracle.paged_attention(**a)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            nbytes += roofline.decode_kv_bytes([case.seq_lens_host[b]], case.num_kv_heads, case.head_dim)
+    tot = sum(times)
+    val = nbytes / tot / 1e9
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "qwen7b_decode (one sequence per step: 28 heads x 8192 tokens)",
+                       "batch": 32, "ctx": 8192, "Hq": 28, "Hkv": 4, "head_dim": 128, "page_size": 16},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": "one whole sequence of the batch per step"},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def _events(stream, n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def measure_decode(pa, case, steps, warmup, pg):
+    """Decode step = writeback of the newest K/V row + split-K decode."""
+    dev = case.q.device
+    stream = torch.cuda.current_stream()
+    B, Hq, D = case.q.shape
+    ws = pa.Workspace(pa.decode_workspace_bytes(B, Hq, case.num_kv_heads, D), dev)
+    out = torch.empty_like(case.q)
+    ones = torch.arange(B + 1, dtype=torch.int32, device=dev)  # one new row per sequence
+
+    def step():
+        pa.kv_write_paged(case.k_pool, case.v_pool, case.k_new, case.v_new, ones, case.seq_lens, case.block_table)
+        pa.attn_decode_paged(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
+                             case.softmax_scale, max_seq_len=case.max_seq_len, out=out, workspace=ws)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(pg)
+    torch.cuda.synchronize()
+    ev = _events(stream, 4 * steps)
+    sampler = ClockSampler()
+    with sampler:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(steps):
+            ev[4 * i].record(stream)
+            pa.kv_write_paged(case.k_pool, case.v_pool, case.k_new, case.v_new, ones, case.seq_lens,
+                              case.block_table)
+            ev[4 * i + 1].record(stream)
+            pa.attn_decode_paged(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
+                                 case.softmax_scale, max_seq_len=case.max_seq_len, out=out, workspace=ws)
+            ev[4 * i + 2].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(pg)
+    torch.cuda.synchronize()
+    total_ms = t_start.elapsed_time(t_end)
+    dec_ms = [ev[4 * i + 1].elapsed_time(ev[4 * i + 2]) for i in range(steps)]
+    kvw_ms = [ev[4 * i].elapsed_time(ev[4 * i + 1]) for i in range(steps)]
+    return total_ms, dec_ms, kvw_ms, sampler.summary(), 2 * steps
+
+
+def measure_decode_e2e(pa, case, steps, warmup):
+    """Same step through the public API with host buffers: per step the
+    queries and the new K/V rows (and seq_lens) are copied from pinned host
+    memory, the attention output is copied back."""
+    dev = case.q.device
+    stream = torch.cuda.current_stream()
+    B, Hq, D = case.q.shape
+    ws = pa.Workspace(pa.decode_workspace_bytes(B, Hq, case.num_kv_heads, D), dev)
+    h_q = case.q.cpu().pin_memory()
+    h_k = case.k_new.cpu().pin_memory()
+    h_v = case.v_new.cpu().pin_memory()
+    h_len = case.seq_lens.cpu().pin_memory()
+    h_out = torch.empty_like(h_q).pin_memory()
+    d_q, d_k, d_v, d_len = torch.empty_like(case.q), torch.empty_like(case.k_new), torch.empty_like(case.v_new), \
+        torch.empty_like(case.seq_lens)
+    d_out = torch.empty_like(case.q)
+    ones = torch.arange(B + 1, dtype=torch.int32, device=dev)
+
+    def step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        d_len.copy_(h_len, non_blocking=True)
+        pa.kv_write_paged(case.k_pool, case.v_pool, d_k, d_v, ones, d_len, case.block_table)
+        pa.attn_decode_paged(d_q, case.k_pool, case.v_pool, case.block_table, d_len, case.softmax_scale,
+                             max_seq_len=case.max_seq_len, out=d_out, workspace=ws)
+        h_out.copy_(d_out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_len))
+    d2h = h_out.numel() * h_out.element_size()
+    return ms, h2d, d2h
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+
+    rank, world, pg = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world, pg)
+        return 0
+
+    import paged_kv_decode_17_gb300 as pa
+    pa.load_library(build_if_missing=True)
+    peaks = load_peaks()
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    case = workloads.qwen7b_decode(device=dev, seed=1 + rank)
+    kv_bytes = roofline.decode_kv_bytes(case.seq_lens_host, case.num_kv_heads, case.head_dim)
+    total_ms, dec_ms, kvw_ms, clocks, launches = measure_decode(pa, case, args.steps, args.warmup, pg)
+    total_ms = max_over_ranks(pg, total_ms)
+    ms_per_step = total_ms / args.steps
+    all_bytes = sum_over_ranks(pg, kv_bytes * args.steps)
+    value = all_bytes / (total_ms * 1e-3) / 1e9
+
+    dec_avg = statistics.mean(dec_ms)
+    achieved = kv_bytes / (dec_avg * 1e-3) / 1e9
+    traffic = profile_traffic("attn_decode_qwen7b_ncu.md", ["paged_kv_decode_17_gb300/csrc/decode.cu",
+                                                            "paged_kv_decode_17_gb300/csrc/pa_common.cuh"])
+    e2e_ms, h2d, d2h = measure_decode_e2e(pa, case, args.steps, args.warmup)
+    e2e_ms = max_over_ranks(pg, e2e_ms)
+    e2e_val = sum_over_ranks(pg, kv_bytes) / (e2e_ms * 1e-3) / 1e9
+    del case
+    torch.cuda.empty_cache()
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "qwen7b_decode: batch 32 x 8192-token contexts, Hq=28, Hkv=4, head_dim 128, "
+                               "16-token pages, 16384-page pool (seeded permutation); step = KV writeback of the "
+                               "newest row + split-K decode",
+                   "batch": 32, "ctx": 8192, "Hq": 28, "Hkv": 4, "head_dim": 128, "page_size": 16,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2: 512 MiB of KV read per step vs 129 MB L2, no flush"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "attn_decode_paged (decode_kernel<128>)",
+                     "algorithmic_bytes_per_launch": kv_bytes, "launch_ms": dec_avg,
+                     "peak_source": peaks["source"]},
+        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches * world,
+        "clocks": clocks,
+        "kv_write_ms": statistics.mean(kvw_ms),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_subprocess()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier(pg)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

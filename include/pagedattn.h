@@ -1,0 +1,165 @@
+/*
+ * pagedattn.h -- C ABI of the GB300 (sm_103a) paged-KV attention library
+ * (libpagedattn.so).
+ *
+ * Three operations make up the hot path of LLM serving attention over a
+ * paged KV cache:
+ *
+ *   kv_write_paged               eager writeback of new K/V rows into their
+ *                                pages ("Inside Ion", section "IonAttention
+ *                                in One Paragraph": KV pages are written back
+ *                                eagerly as they are produced).
+ *   attn_decode_paged            one query row per sequence against its whole
+ *                                paged history, split along the KV sequence
+ *                                and merged with the log-sum-exp identity
+ *                                ("The Stack Below the Stack, Part 2",
+ *                                section 2.2 Flash-Decoding, steps 1-3).
+ *   attn_prefill_varlen_causal   causal attention of variable-length query
+ *                                blocks against their paged K/V, tiled with
+ *                                the online softmax ("The Stack Below the
+ *                                Stack, Part 2", section 2.1; "8. Kernels and
+ *                                Attention Backends", section "Attention is an
+ *                                I/O problem").  Decode rows may be mixed in as
+ *                                entries with one query row.
+ *
+ * Common conventions
+ * ------------------
+ * Pointers named *_pool, q, out, k_new, v_new, block_table, seq_lens,
+ * cu_seqlens_*, lse, workspace and status are DEVICE pointers; the caller
+ * owns every buffer (nothing is allocated by the library).  All calls are
+ * asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream),
+ * perform no host synchronisation and allocate nothing, so they may be
+ * captured in a CUDA graph.
+ *
+ * Element types: K/V pools, q, out, k_new, v_new are bf16 (IEEE binary16
+ * "brain float", 2 bytes); lse is float32; integer arrays are int32.
+ *
+ * Layouts (row-major, contiguous):
+ *   k_pool, v_pool : [num_pages][num_kv_heads][page_size][head_dim]
+ *   block_table    : [batch][max_pages_per_seq]; entry p of row b is the
+ *                    physical page holding tokens p*page_size ..
+ *                    (p+1)*page_size-1 of sequence b.  Entries past the
+ *                    sequence's last page are never read.
+ *   seq_lens       : [batch]; total keys of each sequence, including the rows
+ *                    being attended from / written in this call.
+ *   q, out         : [rows][num_q_heads][head_dim]
+ *   lse            : [rows][num_q_heads], natural-log log-sum-exp of the
+ *                    scaled scores of each row (-inf for a row with no key).
+ * Query head h attends KV head h / (num_q_heads / num_kv_heads).
+ *
+ * Supported shapes: head_dim 64 or 128; page_size a multiple of 16 up to
+ * 256; num_q_heads a multiple of num_kv_heads; num_q_heads / num_kv_heads
+ * up to 128.
+ *
+ * Errors: a negative return value is a pa_status detected on the host
+ * before anything is launched (nothing was enqueued).  Errors found on the
+ * device (a block_table entry outside [0, num_pages), an inconsistent
+ * length, a wait that timed out) are written, first one wins, to the
+ * optional device word `status` (int32, caller-zeroed); the kernels skip
+ * the offending access instead of faulting, and the affected outputs are
+ * unspecified.  Read `status` after synchronising the stream.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_NULL = -1,       /* a required pointer is NULL                          */
+    PA_ERR_SHAPE = -2,      /* unsupported or inconsistent sizes                   */
+    PA_ERR_WORKSPACE = -3,  /* workspace missing or smaller than required          */
+    PA_ERR_CUDA = -4,       /* a CUDA runtime/driver call or the launch failed     */
+    PA_ERR_TIMEOUT = -5,    /* device: a wait on an asynchronous copy timed out    */
+    PA_ERR_BAD_PAGE = -6,   /* device: block_table entry outside [0, num_pages)    */
+    PA_ERR_BAD_LEN = -7,    /* device: seq_len / row count inconsistent            */
+    PA_ERR_ARCH = -8        /* the current device is not an sm_103 GPU             */
+} pa_status;
+
+/* Version of this ABI (bumped on any signature change). */
+int pa_abi_version(void);
+
+/* Static, NUL-terminated description of a pa_status value. */
+const char* pa_status_string(int status);
+
+/*
+ * Workspace bytes attn_decode_paged needs for these sizes on the current
+ * device.  The workspace holds the split partials (normalised partial
+ * outputs and their log-sum-exps) and one arrival counter per
+ * (sequence, KV head, head block).  The caller must ZERO it once after
+ * allocating it; every successful call leaves the counters zero again.  If
+ * a call reports a device error, zero it again before reuse.  Two calls that
+ * may run concurrently need separate workspaces.
+ */
+size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim);
+
+/*
+ * Decode: out[b][h][:] = softmax(scale * q[b][h] . K_b^T) V_b over the
+ * seq_lens[b] keys of sequence b, with K_b/V_b gathered through
+ * block_table[b] from KV head h / (Hq/Hkv).
+ *   out        bf16 [batch][num_q_heads][head_dim]           (written)
+ *   lse        float [batch][num_q_heads] or NULL             (written)
+ *   q          bf16 [batch][num_q_heads][head_dim]
+ *   max_seq_len  host upper bound of seq_lens (sizes the launch only)
+ * A sequence with seq_lens[b] == 0 gets out = 0 and lse = -inf.
+ */
+int attn_decode_paged(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool,
+                      int num_pages, const int32_t* block_table, int max_pages_per_seq,
+                      const int32_t* seq_lens, int batch, int max_seq_len, int page_size,
+                      int num_q_heads, int num_kv_heads, int head_dim, float softmax_scale,
+                      void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * Workspace bytes attn_prefill_varlen_causal needs (same zeroing rules as
+ * the decode workspace; it also holds the split partials of q_len = 1
+ * entries).
+ */
+size_t pa_prefill_workspace_bytes(int batch, int total_q, int num_q_heads, int num_kv_heads, int head_dim);
+
+/*
+ * Varlen causal prefill over paged K/V.  Rows cu_seqlens_q[b] ..
+ * cu_seqlens_q[b+1]-1 of q belong to sequence b; with
+ * q_len = cu_seqlens_q[b+1] - cu_seqlens_q[b], row i sits at absolute
+ * position seq_lens[b] - q_len + i and attends keys 0 .. that position
+ * (bottom-right causal alignment: earlier cached tokens are all visible).
+ * The K/V of the query rows themselves must already be in the pool (call
+ * kv_write_paged first, on the same stream).  Entries with q_len = 1 are
+ * ordinary decode rows, so one call serves a mixed prefill + decode step.
+ *   out        bf16 [total_q][num_q_heads][head_dim]          (written)
+ *   lse        float [total_q][num_q_heads] or NULL            (written)
+ *   q          bf16 [total_q][num_q_heads][head_dim]
+ *   cu_seqlens_q  int32 [batch+1], cu_seqlens_q[0] = 0, non-decreasing
+ *   max_q_len, max_seq_len  host upper bounds (size the launch only)
+ */
+int attn_prefill_varlen_causal(void* out, float* lse, const void* q, const void* k_pool,
+                               const void* v_pool, int num_pages, const int32_t* block_table,
+                               int max_pages_per_seq, const int32_t* cu_seqlens_q,
+                               const int32_t* seq_lens, int batch, int total_q, int max_q_len,
+                               int max_seq_len, int page_size, int num_q_heads, int num_kv_heads,
+                               int head_dim, float softmax_scale, void* workspace,
+                               size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * Eager KV writeback.  Rows cu_seqlens_new[b] .. cu_seqlens_new[b+1]-1 of
+ * k_new/v_new are the newest n_b = cu_seqlens_new[b+1] - cu_seqlens_new[b]
+ * tokens of sequence b, whose length AFTER the write is seq_lens[b]; row i
+ * goes to position pos = seq_lens[b] - n_b + i, i.e. page
+ * block_table[b][pos / page_size], slot pos % page_size, for every KV head.
+ * A bit-exact copy; no other byte of the pools is touched.
+ *   k_new, v_new  bf16 [total_new][num_kv_heads][head_dim]
+ */
+int kv_write_paged(void* k_pool, void* v_pool, int num_pages, const void* k_new, const void* v_new,
+                   const int32_t* cu_seqlens_new, const int32_t* seq_lens,
+                   const int32_t* block_table, int max_pages_per_seq, int batch, int total_new,
+                   int page_size, int num_kv_heads, int head_dim, int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

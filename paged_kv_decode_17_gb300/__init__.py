@@ -1,1 +1,25 @@
-"""GB300-native exact softmax attention over a paged bf16 KV cache."""
+"""GB300-native exact softmax attention over a paged bf16 KV cache.
+
+Public calls (same names as the C ABI in include/pagedattn.h):
+
+* ``kv_write_paged``              eager writeback of new K/V rows into pages
+* ``attn_decode_paged``           split-K Flash-Decoding over pages
+* ``attn_prefill_varlen_causal``  varlen causal prefill (and mixed
+                                  prefill + decode steps) over pages
+
+All compute runs in hand-written CUDA kernels for sm_103a inside
+``libpagedattn.so``; this package only marshals arguments.  Build the library
+with ``paged_kv_decode_17_gb300.build.build()``.
+"""
+
+from .ops import (  # noqa: F401
+    Workspace,
+    attn_decode_paged,
+    attn_prefill_varlen_causal,
+    check_status,
+    decode_workspace_bytes,
+    kv_write_paged,
+    new_status,
+    prefill_workspace_bytes,
+)
+from ._lib import PagedAttnError, load as load_library  # noqa: F401

@@ -1,0 +1,670 @@
+// Split-K paged decode: Flash-Decoding over a paged KV cache.
+//
+// What it computes ("The Stack Below the Stack, Part 2", section 2.2
+// Flash-Decoding): the KV sequence of every (sequence, KV head) is split into
+// chunks; each chunk yields a normalised partial output and its local
+// log-sum-exp; the chunks are merged with
+//     lse = log sum_c exp(lse_c),   o = sum_c exp(lse_c - lse) o_c.
+// Inside a chunk, keys are streamed 16 at a time with the online softmax of
+// section 2.1 (running max and running sum, rescaled when the max grows).
+//
+// GB300 design
+// * Work is measured in "units": 16 consecutive tokens of one
+//   (sequence b, KV head g, head block hb) segment.  A unit is one 16 x D bf16
+//   block of K plus one of V, contiguous in the [page][Hkv][page_size][D]
+//   pools.  All units of all segments are laid end to end and every CTA of a
+//   persistent grid (a multiple of the SM count) takes one equal contiguous
+//   range of them, so a 1-token sequence and a 131k-token one balance the
+//   same way.  The ranges are derived on the device from seq_lens (no host
+//   synchronisation; the call can be captured in a CUDA graph).
+// * Inside a CTA each warp takes every W-th unit of the CTA's part of a
+//   segment and runs its own TMA pipeline: DEPTH stages, each a 16-row K box
+//   and V box loaded by cp.async.bulk.tensor with 128-byte swizzle, so the
+//   ldmatrix reads below are bank-conflict free.  There is no cross-warp
+//   producer/consumer handshake in the loop.
+// * Q.K^T and P.V run on bf16 mma.sync (m16n8k16) with the GQA head block as
+//   the M dimension (up to 16 query heads share one KV head's K/V tiles);
+//   scores, running max/sum and O stay in fp32 registers.
+// * At the end of the CTA's part of a segment the warps' states are merged
+//   in shared memory in a fixed order.  A segment covered by one CTA is
+//   normalised and stored directly; otherwise the partial (o_c, lse_c) goes
+//   to the workspace and the last CTA to arrive (atomic ticket, no waiting)
+//   merges all partials of that segment in a fixed order, so results are
+//   bit-identical run to run.
+#include "pa_common.cuh"
+#include "pa_host.h"
+
+namespace pa {
+namespace dec {
+
+constexpr int W = 4;           // warps per CTA
+constexpr int UNIT = 16;       // tokens per unit
+constexpr int MAXR = 16;       // query heads per head block (mma M)
+constexpr int MIN_CHUNK = 16;  // minimum units per CTA
+constexpr int CTAS_PER_SM = 1;
+
+template <int D>
+struct Cfg {
+    static constexpr int DEPTH = (D == 128) ? 5 : 8;
+    static constexpr int BOXES = D / 64;             // 128-byte-wide TMA boxes per row
+    static constexpr int BOX_BYTES = UNIT * 128;     // 16 rows x 128 bytes
+    static constexpr int UNIT_BYTES = UNIT * D * 2;  // one K or V unit
+    static constexpr int STAGE_BYTES = 2 * UNIT_BYTES;
+    static constexpr int STAGES_BYTES = W * DEPTH * STAGE_BYTES;
+    static constexpr int MSTRIDE = D + 4;  // fp32 row stride of the merge buffer
+    static constexpr int MERGE_BYTES = W * MAXR * MSTRIDE * 4;
+    static constexpr int SMEM_BYTES = 1024 + STAGES_BYTES + MERGE_BYTES;
+};
+
+struct Params {
+    __nv_bfloat16* out;
+    float* lse;
+    const __nv_bfloat16* q;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    int32_t* counters;
+    float* ws_lse;  // [slots][MAXR], log2 domain
+    float* ws_o;    // [slots][MAXR][D], normalised
+    int32_t* status;
+    int num_pages, max_pages, batch, page_size;
+    int Hq, Hkv, group, HB, R;
+    float scale_log2;
+};
+
+// One (b, g, hb) segment: its units are [start, end) in the global order
+// b-major, then g, then hb.
+struct Seg {
+    int b, g, hb, len, n, start, end;
+};
+
+__device__ __forceinline__ int load_len(const Params& p, int b) {
+    int len = __ldg(p.seq_lens + b);
+    const int cap = p.max_pages * p.page_size;
+    if (len < 0 || len > cap) {
+        report(p.status, PA_ERR_BAD_LEN);
+        len = len < 0 ? 0 : cap;
+    }
+    return len;
+}
+
+// Advance to the next segment with at least one unit.  The caller makes sure
+// one exists (the CTA's range ends before the last unit).
+__device__ __forceinline__ void seg_next(Seg& s, const Params& p) {
+    do {
+        s.start = s.end;
+        if (++s.hb == p.HB) {
+            s.hb = 0;
+            if (++s.g == p.Hkv) {
+                s.g = 0;
+                ++s.b;
+                s.len = (s.b < p.batch) ? load_len(p, s.b) : 0;
+                s.n = (s.len + UNIT - 1) / UNIT;
+            }
+        }
+        s.end = s.start + s.n;
+    } while (s.n == 0 && s.b < p.batch);
+}
+
+// The sequence of units one warp loads: within each segment piece
+// [pa, pe) of the CTA range, units pa + w, pa + w + W, ...
+struct UnitIter {
+    Seg seg;
+    int pe, u, U1;
+    bool done;
+    __device__ __forceinline__ void norm(const Params& p, int w) {
+        while (!done && u >= pe) {
+            if (pe >= U1) {
+                done = true;
+                break;
+            }
+            seg_next(seg, p);
+            pe = min(U1, seg.end);
+            u = seg.start + w;
+        }
+    }
+};
+
+template <int D>
+__device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, uint8_t* stage, uint64_t* bar,
+                                           int* phys_slot, const CUtensorMap* kmap, const CUtensorMap* vmap,
+                                           int lane, uint64_t policy) {
+    using C = Cfg<D>;
+    const int j = it.u - it.seg.start;  // unit index within the sequence
+    const int tok0 = j * UNIT;
+    const int page = tok0 / p.page_size;
+    const int sub = (tok0 - page * p.page_size) / UNIT;
+    if (lane == 0) {
+        const int phys = __ldg(p.block_table + (size_t)it.seg.b * p.max_pages + page);
+        if (phys < 0 || phys >= p.num_pages) {
+            report(p.status, PA_ERR_BAD_PAGE);
+            *phys_slot = -1;
+            mbar_arrive(bar);
+        } else {
+            *phys_slot = phys;
+            const int row = (phys * p.Hkv + it.seg.g) * p.page_size + sub * UNIT;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+#pragma unroll
+            for (int bx = 0; bx < C::BOXES; ++bx) {
+                tma_load_2d_hint(stage + bx * C::BOX_BYTES, kmap, bar, bx * 64, row, policy);
+                tma_load_2d_hint(stage + C::UNIT_BYTES + bx * C::BOX_BYTES, vmap, bar, bx * 64, row, policy);
+            }
+        }
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(W * 32, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                  const Params p) {
+    using C = Cfg<D>;
+    constexpr int DEPTH = C::DEPTH;
+    constexpr int KSTEPS = D / 16;
+    constexpr int NT = D / 8;  // n-tiles of O
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stages = smem;
+    float* merge_o = reinterpret_cast<float*>(smem + C::STAGES_BYTES);
+    __shared__ __align__(8) uint64_t bars[W][DEPTH];
+    __shared__ int s_phys[W][DEPTH];
+    __shared__ float s_m[W][MAXR], s_l[W][MAXR], s_M[MAXR], s_L[MAXR];
+    __shared__ int s_plan[8];
+    __shared__ int s_last;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+
+    // ---- plan: total units T, this CTA's range, and the segment holding U0
+    if (warp == 0) {
+        int T = 0;
+        for (int b0 = 0; b0 < p.batch; b0 += 32) {
+            const int b = b0 + lane;
+            int n = 0;
+            if (b < p.batch) {
+                const int len = load_len(p, b);
+                n = (len + UNIT - 1) / UNIT * p.Hkv * p.HB;
+                if (len == 0 && (b % gridDim.x) == blockIdx.x) {
+                    // empty sequence: defined result, out = 0, lse = -inf
+                    for (int h = 0; h < p.Hq; ++h) {
+                        uint4* o = reinterpret_cast<uint4*>(p.out + ((size_t)b * p.Hq + h) * D);
+                        for (int c = 0; c < D / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
+                        if (p.lse) p.lse[(size_t)b * p.Hq + h] = -INFINITY;
+                    }
+                }
+            }
+            T += warp_sum_int(n);
+        }
+        int chunk = (T + gridDim.x - 1) / gridDim.x;
+        chunk = max(chunk, MIN_CHUNK);
+        const int U0 = blockIdx.x * chunk;  // grid * chunk < 2^31 is checked on the host
+        const int U1 = min(T, U0 + chunk);
+        int sb = -1, sP = 0;
+        if (U0 < U1) {
+            int P = 0;
+            for (int b0 = 0; b0 < p.batch && sb < 0; b0 += 32) {
+                const int b = b0 + lane;
+                const int n = (b < p.batch) ? (load_len(p, b) + UNIT - 1) / UNIT * p.Hkv * p.HB : 0;
+                const int incl = warp_incl_scan(n);
+                const int tot = __shfl_sync(0xffffffffu, incl, 31);
+                if (U0 < P + tot) {
+                    const unsigned hit = __ballot_sync(0xffffffffu, P + incl > U0);
+                    const int l = __ffs(hit) - 1;
+                    sb = b0 + l;
+                    sP = P + __shfl_sync(0xffffffffu, incl - n, l);
+                }
+                P += tot;
+            }
+        }
+        if (lane == 0) {
+            s_plan[0] = T;
+            s_plan[1] = chunk;
+            s_plan[2] = U0;
+            s_plan[3] = U1;
+            s_plan[4] = sb;
+            s_plan[5] = sP;
+        }
+    }
+    if (lane == 0) {
+        for (int i = 0; i < DEPTH; ++i) mbar_init(&bars[warp][i], 1);
+        fence_mbar_init();
+    }
+    if (tid == 0) {
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
+    __syncthreads();
+    const int chunk = s_plan[1];
+    const int U0 = s_plan[2], U1 = s_plan[3];
+    if (U0 >= U1) return;
+
+    // segment holding U0
+    Seg seg0;
+    {
+        const int b = s_plan[4];
+        const int len = load_len(p, b);
+        const int n = (len + UNIT - 1) / UNIT;
+        const int idx = (U0 - s_plan[5]) / n;  // (g, hb) index within sequence b
+        seg0.b = b;
+        seg0.g = idx / p.HB;
+        seg0.hb = idx - seg0.g * p.HB;
+        seg0.len = len;
+        seg0.n = n;
+        seg0.start = s_plan[5] + idx * n;
+        seg0.end = seg0.start + n;
+    }
+
+    const uint64_t policy = policy_evict_first();
+    uint8_t* my_stages = stages + warp * DEPTH * C::STAGE_BYTES;
+
+    // ---- prologue: fill this warp's pipeline
+    UnitIter it;
+    it.seg = seg0;
+    it.U1 = U1;
+    it.pe = min(U1, seg0.end);
+    it.u = U0 + warp;
+    it.done = false;
+    it.norm(p, warp);
+    uint32_t issued = 0, consumed = 0;
+    for (int i = 0; i < DEPTH && !it.done; ++i) {
+        issue_unit<D>(p, it, my_stages + i * C::STAGE_BYTES, &bars[warp][i], &s_phys[warp][i], &kmap, &vmap, lane,
+                      policy);
+        ++issued;
+        it.u += W;
+        it.norm(p, warp);
+    }
+    __syncwarp();
+
+    // per-lane ldmatrix geometry (see the fragment layouts of mma.m16n8k16)
+    const int mi = lane >> 3, ri = lane & 7;
+    const int k_key = ((mi >> 1) << 3) + ri;  // K: matrices (keys 0-7|8-15) x (d lo|hi)
+    const int k_dsel = mi & 1;
+    const int v_key = ((mi & 1) << 3) + ri;   // V (trans): matrices (keys lo|hi) x (d lo|hi)
+    const int v_dsel = mi >> 1;
+    const int qr = lane >> 2;       // row group of this lane in mma fragments
+    const int qc = (lane & 3) * 2;  // column pair of this lane
+
+    bool aborted = false;
+    uint32_t waited = 0;  // units whose copy is known to have landed
+    Seg cs = seg0;
+    int pa_ = U0;
+    while (true) {
+        const int pe = min(U1, cs.end);
+        const int rows = min(p.R, p.group - cs.hb * p.R);
+        const int h0 = cs.g * p.group + cs.hb * p.R;
+
+        // Q fragments of the head block (rows >= `rows` are zero)
+        uint32_t qa[KSTEPS][4];
+        {
+            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(p.q + ((size_t)cs.b * p.Hq + h0 + qr) * D);
+            const uint32_t* q8 = reinterpret_cast<const uint32_t*>(p.q + ((size_t)cs.b * p.Hq + h0 + qr + 8) * D);
+            const bool r0ok = qr < rows, r8ok = qr + 8 < rows;
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                const int c = (kk * 16 + qc) >> 1;
+                qa[kk][0] = r0ok ? __ldg(q0 + c) : 0u;
+                qa[kk][1] = r8ok ? __ldg(q8 + c) : 0u;
+                qa[kk][2] = r0ok ? __ldg(q0 + c + 4) : 0u;
+                qa[kk][3] = r8ok ? __ldg(q8 + c + 4) : 0u;
+            }
+        }
+        float o[NT][4];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+        for (int u = pa_ + warp; u < pe; u += W) {
+            const int st = consumed % DEPTH;
+            const uint32_t par = (consumed / DEPTH) & 1u;
+            if (!aborted) {
+                if (mbar_wait(&bars[warp][st], par)) {
+                    waited = consumed + 1;
+                } else {
+                    aborted = true;
+                    if (lane == 0) report(p.status, PA_ERR_TIMEOUT);
+                }
+            }
+            const int phys = s_phys[warp][st];
+            uint8_t* sk = my_stages + st * C::STAGE_BYTES;
+            uint8_t* sv = sk + C::UNIT_BYTES;
+            if (!aborted && phys >= 0) {
+                const int valid = min(UNIT, cs.len - (u - cs.start) * UNIT);
+                if (valid < UNIT) {
+                    // zero V rows past the end of the sequence (their slots may hold anything)
+                    const int nvec = (UNIT - valid) * (D / 8);
+                    for (int i = lane; i < nvec; i += 32) {
+                        const int r = valid + i / (D / 8);
+                        const int c = i % (D / 8);
+                        *reinterpret_cast<uint4*>(sv + (c >> 3) * C::BOX_BYTES + r * 128 + (c & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();  // before a later TMA overwrites this stage
+                    __syncwarp();
+                }
+                const uint32_t kb = smem_u32(sk), vb = smem_u32(sv);
+                // S = Q K^T  (16 heads x 16 keys)
+                float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    const int dch = kk * 2 + k_dsel;
+                    const uint32_t addr =
+                        kb + (dch >> 3) * C::BOX_BYTES + k_key * 128 + (((dch & 7) ^ (k_key & 7)) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(addr, b0, b1, b2, b3);
+                    mma_16816(s[0], qa[kk], b0, b1);
+                    mma_16816(s[1], qa[kk], b2, b3);
+                }
+                // scale to log2 domain, mask keys >= valid
+                float x[2][4];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int key = j * 8 + qc + (e & 1);
+                        x[j][e] = key < valid ? s[j][e] * p.scale_log2 : -INFINITY;
+                    }
+                }
+                float rm0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+                float rm1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+                rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, 1));
+                rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, 2));
+                rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 1));
+                rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 2));
+                const float mn0 = fmaxf(m0, rm0), mn1 = fmaxf(m1, rm1);
+                const float a0 = ex2(m0 - mn0), a1 = ex2(m1 - mn1);  // 0 when m was -inf
+                m0 = mn0;
+                m1 = mn1;
+                float pr[2][4];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    pr[j][0] = ex2(x[j][0] - mn0);
+                    pr[j][1] = ex2(x[j][1] - mn0);
+                    pr[j][2] = ex2(x[j][2] - mn1);
+                    pr[j][3] = ex2(x[j][3] - mn1);
+                }
+                l0 = l0 * a0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+                l1 = l1 * a1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+                if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        o[n][0] *= a0;
+                        o[n][1] *= a0;
+                        o[n][2] *= a1;
+                        o[n][3] *= a1;
+                    }
+                }
+                uint32_t pa[4];
+                pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+                pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+                pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+                pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+                // O += P V
+#pragma unroll
+                for (int jj = 0; jj < D / 16; ++jj) {
+                    const int dch = jj * 2 + v_dsel;
+                    const uint32_t addr =
+                        vb + (dch >> 3) * C::BOX_BYTES + v_key * 128 + (((dch & 7) ^ (v_key & 7)) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_trans(addr, b0, b1, b2, b3);
+                    mma_16816(o[2 * jj], pa, b0, b1);
+                    mma_16816(o[2 * jj + 1], pa, b2, b3);
+                }
+            }
+            __syncwarp();
+            ++consumed;
+            if (!it.done && !aborted) {
+                const int sti = issued % DEPTH;
+                issue_unit<D>(p, it, my_stages + sti * C::STAGE_BYTES, &bars[warp][sti], &s_phys[warp][sti], &kmap,
+                              &vmap, lane, policy);
+                ++issued;
+                it.u += W;
+                it.norm(p, warp);
+                __syncwarp();
+            }
+        }
+
+        // ---- merge the W warp states of this segment piece (fixed order)
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        if ((lane & 3) == 0) {
+            s_m[warp][qr] = m0;
+            s_l[warp][qr] = l0;
+            s_m[warp][qr + 8] = m1;
+            s_l[warp][qr + 8] = l1;
+        }
+        __syncthreads();
+        {
+            float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                M0 = fmaxf(M0, s_m[w][qr]);
+                M1 = fmaxf(M1, s_m[w][qr + 8]);
+            }
+            float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                const float mw0 = s_m[w][qr], mw1 = s_m[w][qr + 8];
+                L0 += (mw0 == -INFINITY) ? 0.f : s_l[w][qr] * ex2(mw0 - M0);
+                L1 += (mw1 == -INFINITY) ? 0.f : s_l[w][qr + 8] * ex2(mw1 - M1);
+            }
+            const float sc0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - M0);
+            const float sc1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - M1);
+            float* mo = merge_o + warp * MAXR * C::MSTRIDE;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const int col = n * 8 + qc;
+                *reinterpret_cast<float2*>(mo + qr * C::MSTRIDE + col) = make_float2(o[n][0] * sc0, o[n][1] * sc0);
+                *reinterpret_cast<float2*>(mo + (qr + 8) * C::MSTRIDE + col) =
+                    make_float2(o[n][2] * sc1, o[n][3] * sc1);
+            }
+            if (warp == 0 && (lane & 3) == 0) {
+                s_M[qr] = M0;
+                s_L[qr] = L0;
+                s_M[qr + 8] = M1;
+                s_L[qr + 8] = L1;
+            }
+        }
+        __syncthreads();
+        const int c0 = cs.start / chunk, c1 = (cs.end - 1) / chunk;
+        const int sid = (cs.b * p.Hkv + cs.g) * p.HB + cs.hb;
+        const bool single = (c0 == c1);
+        for (int idx = tid; idx < rows * (D / 4); idx += W * 32) {
+            const int r = idx / (D / 4);
+            const int d4 = idx - r * (D / 4);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                const float4 v = *reinterpret_cast<const float4*>(merge_o + (w * MAXR + r) * C::MSTRIDE + d4 * 4);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            const float L = s_L[r];
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            if (single) {
+                uint2 ob;
+                ob.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+                ob.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+                *reinterpret_cast<uint2*>(p.out + ((size_t)cs.b * p.Hq + h0 + r) * D + d4 * 4) = ob;
+                if (p.lse != nullptr && d4 == 0)
+                    p.lse[(size_t)cs.b * p.Hq + h0 + r] = L > 0.f ? (s_M[r] + lg2(L)) * kLn2 : -INFINITY;
+            } else {
+                const size_t slot = (size_t)blockIdx.x + sid;
+                *reinterpret_cast<float4*>(p.ws_o + (slot * MAXR + r) * D + d4 * 4) =
+                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                if (d4 == 0) p.ws_lse[slot * MAXR + r] = L > 0.f ? s_M[r] + lg2(L) : -INFINITY;
+            }
+        }
+        if (!single) {
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) {
+                const int prev = atomicAdd(p.counters + sid, 1);
+                s_last = (prev == c1 - c0);
+            }
+            __syncthreads();
+            if (s_last) {
+                // last CTA of this segment: merge all partials in slot order
+                __threadfence();
+                for (int idx = tid; idx < rows * (D / 4); idx += W * 32) {
+                    const int r = idx / (D / 4);
+                    const int d4 = idx - r * (D / 4);
+                    float M = -INFINITY;
+                    for (int c = c0; c <= c1; ++c) M = fmaxf(M, __ldcg(p.ws_lse + ((size_t)c + sid) * MAXR + r));
+                    float L = 0.f;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (M != -INFINITY) {
+                        for (int c = c0; c <= c1; ++c) {
+                            const size_t slot = (size_t)c + sid;
+                            const float lc = __ldcg(p.ws_lse + slot * MAXR + r);
+                            if (lc == -INFINITY) continue;
+                            const float wgt = ex2(lc - M);
+                            const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (slot * MAXR + r) * D) + d4);
+                            L += wgt;
+                            acc.x += wgt * v.x;
+                            acc.y += wgt * v.y;
+                            acc.z += wgt * v.z;
+                            acc.w += wgt * v.w;
+                        }
+                    }
+                    const float inv = L > 0.f ? 1.f / L : 0.f;
+                    uint2 ob;
+                    ob.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+                    ob.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+                    *reinterpret_cast<uint2*>(p.out + ((size_t)cs.b * p.Hq + h0 + r) * D + d4 * 4) = ob;
+                    if (p.lse != nullptr && d4 == 0)
+                        p.lse[(size_t)cs.b * p.Hq + h0 + r] = L > 0.f ? (M + lg2(L)) * kLn2 : -INFINITY;
+                }
+                if (tid == 0) p.counters[sid] = 0;  // leave the workspace ready for the next call
+            }
+        }
+        __syncthreads();  // merge buffers are reused by the next piece
+        if (pe >= U1) break;
+        pa_ = pe;
+        seg_next(cs, p);
+    }
+
+    // drain: never leave the CTA with a bulk copy still writing its shared memory
+    for (uint32_t i = waited; i < issued; ++i) {
+        if (!mbar_wait(&bars[warp][i % DEPTH], (i / DEPTH) & 1u)) {
+            if (lane == 0) report(p.status, PA_ERR_TIMEOUT);
+            break;
+        }
+    }
+}
+
+// Workspace layout: [counters: S int32][ws_lse: slots x MAXR f32][ws_o: slots x MAXR x D f32]
+struct WsLayout {
+    size_t counters, lse, o, total;
+};
+
+inline WsLayout ws_layout(int slots, int segs, int D) {
+    WsLayout w;
+    w.counters = 0;
+    w.lse = align_up((size_t)segs * 4, 256);
+    w.o = w.lse + align_up((size_t)slots * MAXR * 4, 256);
+    w.total = w.o + (size_t)slots * MAXR * D * 4;
+    return w;
+}
+
+inline int head_blocks(int group) { return (group + MAXR - 1) / MAXR; }
+
+}  // namespace dec
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim) {
+    if (batch <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads) return 0;
+    DeviceInfo dev;
+    if (current_device(&dev) != PA_OK) return 0;
+    const int group = num_q_heads / num_kv_heads;
+    const int segs = batch * num_kv_heads * dec::head_blocks(group);
+    const int slots = dev.sm_count * dec::CTAS_PER_SM + segs;
+    return dec::ws_layout(slots, segs, head_dim).total;
+}
+
+extern "C" int attn_decode_paged(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool,
+                                 int num_pages, const int32_t* block_table, int max_pages_per_seq,
+                                 const int32_t* seq_lens, int batch, int max_seq_len, int page_size, int num_q_heads,
+                                 int num_kv_heads, int head_dim, float softmax_scale, void* workspace,
+                                 size_t workspace_bytes, int32_t* status, void* stream) {
+    if (batch < 0 || max_seq_len < 0) return PA_ERR_SHAPE;
+    int rc = check_common_shapes(page_size, num_q_heads, num_kv_heads, head_dim);
+    if (rc != PA_OK) return rc;
+    if (batch == 0) return PA_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_table || !seq_lens) return PA_ERR_NULL;
+    if (num_pages < 1 || max_pages_per_seq < 1) return PA_ERR_SHAPE;
+    if ((long long)max_seq_len > (long long)max_pages_per_seq * page_size) return PA_ERR_SHAPE;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(q) || !aligned16(out)) return PA_ERR_SHAPE;
+    const long long pool_rows = (long long)num_pages * num_kv_heads * page_size;
+    if (pool_rows >= (1ll << 31)) return PA_ERR_SHAPE;
+
+    DeviceInfo dev;
+    rc = current_device(&dev);
+    if (rc != PA_OK) return rc;
+
+    const int group = num_q_heads / num_kv_heads;
+    const int HB = dec::head_blocks(group);
+    const int R = (group + HB - 1) / HB;
+    const int segs = batch * num_kv_heads * HB;
+    const long long units_upper = (long long)segs * ((max_seq_len + dec::UNIT - 1) / dec::UNIT);
+    // every unit index and grid * chunk must fit in int32
+    if ((long long)segs * ((max_pages_per_seq * (long long)page_size + dec::UNIT - 1) / dec::UNIT) +
+            (long long)dev.sm_count * dec::CTAS_PER_SM * dec::MIN_CHUNK >=
+        (1ll << 31))
+        return PA_ERR_SHAPE;
+    const int gmax = dev.sm_count * dec::CTAS_PER_SM;
+    long long g = (units_upper + dec::MIN_CHUNK - 1) / dec::MIN_CHUNK;
+    if (g < 1) g = 1;
+    const int grid = (int)(g < gmax ? g : gmax);
+
+    const int slots = gmax + segs;
+    const dec::WsLayout wl = dec::ws_layout(slots, segs, head_dim);
+    if (workspace == nullptr) return PA_ERR_WORKSPACE;
+    if (workspace_bytes < wl.total) return PA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_WORKSPACE;
+
+    CUtensorMap kmap, vmap;
+    if (encode_rows_map(&kmap, k_pool, (uint64_t)pool_rows, head_dim, 64, dec::UNIT) != PA_OK) return PA_ERR_CUDA;
+    if (encode_rows_map(&vmap, v_pool, (uint64_t)pool_rows, head_dim, 64, dec::UNIT) != PA_OK) return PA_ERR_CUDA;
+
+    dec::Params prm;
+    prm.out = static_cast<__nv_bfloat16*>(out);
+    prm.lse = lse;
+    prm.q = static_cast<const __nv_bfloat16*>(q);
+    prm.block_table = block_table;
+    prm.seq_lens = seq_lens;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    prm.counters = reinterpret_cast<int32_t*>(ws + wl.counters);
+    prm.ws_lse = reinterpret_cast<float*>(ws + wl.lse);
+    prm.ws_o = reinterpret_cast<float*>(ws + wl.o);
+    prm.status = status;
+    prm.num_pages = num_pages;
+    prm.max_pages = max_pages_per_seq;
+    prm.batch = batch;
+    prm.page_size = page_size;
+    prm.Hq = num_q_heads;
+    prm.Hkv = num_kv_heads;
+    prm.group = group;
+    prm.HB = HB;
+    prm.R = R;
+    prm.scale_log2 = softmax_scale * kLog2e;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (head_dim == 128) {
+        constexpr int smem = dec::Cfg<128>::SMEM_BYTES;
+        if (set_smem_limit_once((const void*)dec::decode_kernel<128>, smem, dev.device, 0) != PA_OK)
+            return PA_ERR_CUDA;
+        dec::decode_kernel<128><<<grid, dec::W * 32, smem, st>>>(kmap, vmap, prm);
+    } else {
+        constexpr int smem = dec::Cfg<64>::SMEM_BYTES;
+        if (set_smem_limit_once((const void*)dec::decode_kernel<64>, smem, dev.device, 1) != PA_OK)
+            return PA_ERR_CUDA;
+        dec::decode_kernel<64><<<grid, dec::W * 32, smem, st>>>(kmap, vmap, prm);
+    }
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}

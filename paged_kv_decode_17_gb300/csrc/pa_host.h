@@ -1,0 +1,51 @@
+// Host-side helpers shared by the launchers (argument checks, device
+// properties, tensor-map encoding).  Internal to libpagedattn.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pagedattn.h"
+
+namespace pa {
+
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int major, minor;
+    size_t max_smem_optin;
+};
+
+// Properties of the current device (cached per device).  Returns PA_OK,
+// PA_ERR_CUDA or PA_ERR_ARCH (not an sm_103 GPU).
+int current_device(DeviceInfo* info);
+
+// Encode a 2-D bf16 tensor map over `rows` rows of `row_elems` elements
+// (row stride = row_elems * 2 bytes), box = box_cols x box_rows, 128-byte
+// swizzle.  Returns PA_OK or PA_ERR_CUDA.
+int encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t row_elems, uint32_t box_cols,
+                    uint32_t box_rows);
+
+// Same, without swizzle (plain row-major box).
+int encode_rows_map_noswizzle(CUtensorMap* map, const void* base, uint64_t rows, uint32_t row_elems,
+                              uint32_t box_cols, uint32_t box_rows);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Checks shared by every entry point.
+inline int check_common_shapes(int page_size, int num_q_heads, int num_kv_heads, int head_dim) {
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_SHAPE;
+    if (page_size < 16 || page_size > 256 || page_size % 16 != 0) return PA_ERR_SHAPE;
+    if (num_kv_heads < 1 || num_q_heads < num_kv_heads || num_q_heads % num_kv_heads != 0) return PA_ERR_SHAPE;
+    if (num_q_heads / num_kv_heads > 128) return PA_ERR_SHAPE;
+    return PA_OK;
+}
+
+// Set the dynamic shared-memory limit of a kernel once per device.
+int set_smem_limit_once(const void* kernel, int bytes, int device, int slot);
+
+}  // namespace pa

@@ -1,0 +1,162 @@
+"""attn_decode_paged on the GPU against the fp64 oracle, plus the invariants
+that must hold bit for bit (page permutation, run-to-run determinism)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.conftest import assert_attention_close, bits, compact_for_oracle, oracle_args
+
+pytestmark = pytest.mark.gpu
+
+
+def _pa():
+    return pytest.importorskip("paged_kv_decode_17_gb300")
+
+
+def _decode(case, dev, **kw):
+    pa = _pa()
+    g = case.to(dev) if case.q.device != dev else case
+    status = pa.new_status(dev)
+    out, lse = pa.attn_decode_paged(g.q, g.k_pool, g.v_pool, g.block_table, g.seq_lens, g.softmax_scale,
+                                    max_seq_len=max(1, case.max_seq_len), return_lse=True, status=status, **kw)
+    pa.check_status(status, "attn_decode_paged")
+    return out, lse
+
+
+def _check(case, dev):
+    ref_out, ref_lse = oracle.paged_attention(**oracle_args(case))
+    out, lse = _decode(case, dev)
+    return assert_attention_close(out, ref_out, lse, ref_lse, what=case.name)
+
+
+@pytest.mark.parametrize("sharp", [False, True])
+def test_tiny_decode(cuda_device, sharp):
+    _check(workloads.tiny_decode(seed=0, sharp=sharp), cuda_device)
+
+
+@pytest.mark.parametrize("name", sorted(workloads.awkward_cases().keys()))
+def test_awkward_decode(cuda_device, name):
+    _check(workloads.awkward_cases()[name], cuda_device)
+
+
+@pytest.mark.parametrize("seed", [40, 41, 42])
+def test_random_ragged_decode(cuda_device, seed):
+    gen = torch.Generator().manual_seed(seed)
+    B = int(torch.randint(1, 40, (1,), generator=gen))
+    lens = torch.randint(1, 3000, (B,), generator=gen).tolist()
+    Hkv = int(torch.randint(1, 5, (1,), generator=gen))
+    group = int(torch.randint(1, 9, (1,), generator=gen))
+    D = 64 if seed % 2 else 128
+    case = workloads.make_paged_case("rand%d" % seed, lens, [1] * B, Hkv * group, Hkv, D, seed=seed)
+    _check(case, cuda_device)
+
+
+def test_page_permutation_bit_exact(cuda_device):
+    case = workloads.make_paged_case("perm", [700, 33, 1500], [1, 1, 1], 8, 2, 128, num_pages=160, seed=43)
+    out1, lse1 = _decode(case, cuda_device)
+    P = case.num_pages
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(9))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(P)
+    case2 = workloads.PagedCase(**{**case.__dict__})
+    case2.k_pool = case.k_pool[perm].contiguous()
+    case2.v_pool = case.v_pool[perm].contiguous()
+    bt = case.block_table.clone()
+    m = bt >= 0
+    bt[m] = inv[bt[m].long()].to(torch.int32)
+    case2.block_table = bt
+    out2, lse2 = _decode(case2, cuda_device)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+
+
+def test_run_twice_bit_exact(cuda_device):
+    case = workloads.make_paged_case("twice", [5000, 12000, 77], [1, 1, 1], 32, 8, 128, seed=44)
+    g = case.to(cuda_device)
+    o1, l1 = _decode(g, cuda_device)
+    o2, l2 = _decode(g, cuda_device)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+
+
+def test_tail_slots_never_read(cuda_device):
+    # overwrite every slot past each sequence's end with +inf; outputs must not move
+    case = workloads.make_paged_case("tail", [17, 33, 250], [1, 1, 1], 8, 4, 64, num_pages=40, seed=45)
+    o1, l1 = _decode(case, cuda_device)
+    k = case.k_pool.clone()
+    v = case.v_pool.clone()
+    for b, L in enumerate(case.seq_lens_host):
+        last = int(case.block_table[b, (L - 1) // 16])
+        k[last, :, L % 16 or 16:, :] = float("inf")
+        v[last, :, L % 16 or 16:, :] = float("inf")
+    case.k_pool, case.v_pool = k, v
+    o2, l2 = _decode(case, cuda_device)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+def test_bad_page_reports_status(cuda_device):
+    pa = _pa()
+    case = workloads.make_paged_case("bad", [100, 60], [1, 1], 4, 2, 64, seed=46, num_pages=12)
+    g = case.to(cuda_device)
+    g.block_table[1, 2] = -5
+    status = pa.new_status(cuda_device)
+    pa.attn_decode_paged(g.q, g.k_pool, g.v_pool, g.block_table, g.seq_lens, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -6
+    # the workspace counters may be left dirty after a device error: reset and run clean
+    for ws in list(pa.ops._ws_cache.values()):
+        ws.reset()
+    _check(case, cuda_device)
+
+
+def test_seq_len_beyond_table_reports_status(cuda_device):
+    pa = _pa()
+    case = workloads.make_paged_case("badlen", [30, 20], [1, 1], 4, 2, 64, seed=47)
+    g = case.to(cuda_device)
+    g.seq_lens[0] = 10 ** 6
+    status = pa.new_status(cuda_device)
+    pa.attn_decode_paged(g.q, g.k_pool, g.v_pool, g.block_table, g.seq_lens, max_seq_len=32, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -7
+    for ws in list(pa.ops._ws_cache.values()):
+        ws.reset()
+
+
+def test_host_validation_errors(cuda_device):
+    pa = _pa()
+    case = workloads.tiny_decode().to(cuda_device)
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.attn_decode_paged(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
+                             workspace=pa.Workspace(256, cuda_device))
+    assert e.value.code == -3  # workspace too small
+    q3 = case.q[:, :3].contiguous()  # 3 query heads over 2 KV heads
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.attn_decode_paged(q3, case.k_pool, case.v_pool, case.block_table, case.seq_lens)
+    assert e.value.code == -2
+
+
+def _sampled_full_size(case, seqs, dev):
+    out, lse = _decode(case, dev)
+    args, rows = compact_for_oracle(case, seqs)
+    ref_out, ref_lse = oracle.paged_attention(**args)
+    assert_attention_close(out[rows], ref_out, lse[rows], ref_lse, what=case.name + " sampled")
+    # no NaN anywhere in the full output
+    assert torch.isfinite(out.float()).all()
+    return out
+
+
+@pytest.mark.slow
+def test_qwen7b_decode_full_size_sampled(cuda_device):
+    case = workloads.qwen7b_decode(device=cuda_device)
+    _sampled_full_size(case, [0, 13, 31], cuda_device)
+
+
+@pytest.mark.slow
+def test_llama8b_ragged_decode_full_size_sampled(cuda_device):
+    case = workloads.llama8b_ragged_decode(device=cuda_device)
+    lens = case.seq_lens_host
+    order = sorted(range(len(lens)), key=lambda b: lens[b])
+    seqs = [order[0], order[len(order) // 2], order[-1]]  # shortest, median, longest
+    _sampled_full_size(case, seqs, cuda_device)
