@@ -78,7 +78,8 @@ typedef enum {
     PA_ERR_TIMEOUT = -5,    /* device: a wait on an asynchronous copy timed out    */
     PA_ERR_BAD_PAGE = -6,   /* device: block_table entry outside [0, num_pages)    */
     PA_ERR_BAD_LEN = -7,    /* device: seq_len / row count inconsistent            */
-    PA_ERR_ARCH = -8        /* the current device is not an sm_103 GPU             */
+    PA_ERR_ARCH = -8,       /* the current device is not an sm_103 GPU             */
+    PA_ERR_SCRATCH_LIMIT = -9 /* needs more scratch than attn_decode_paged_noalloc holds */
 } pa_status;
 
 /* Version of this ABI (bumped on any signature change). */
@@ -157,6 +158,37 @@ int kv_write_paged(void* k_pool, void* v_pool, int num_pages, const void* k_new,
                    const int32_t* cu_seqlens_new, const int32_t* seq_lens,
                    const int32_t* block_table, int max_pages_per_seq, int batch, int total_new,
                    int page_size, int num_kv_heads, int head_dim, int32_t* status, void* stream);
+
+/*
+ * Allocation-free variant of attn_decode_paged.  This entry point has no
+ * counterpart in the paper; it exists for callers that cannot allocate
+ * device memory -- code running inside an allocator or memory-pool
+ * callback, plugins whose host framework owns every device allocation, or
+ * paths that must never enter the driver's allocator -- and therefore
+ * cannot provide the decode workspace.
+ *
+ * Same arguments and results as attn_decode_paged, minus the workspace: the
+ * split-K scratch lives in a fixed 8 MiB device array inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ * Problems whose workspace (pa_decode_workspace_bytes) exceeds 8 MiB are
+ * rejected with PA_ERR_SCRATCH_LIMIT before anything is enqueued; roughly,
+ * batch * num_kv_heads * ceil((num_q_heads/num_kv_heads)/16) + SM count
+ * must stay below about 1000 at head_dim 128 (about 2000 at head_dim 64).
+ *
+ * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call clears the arrival counters in the
+ * array (an asynchronous memset on `stream`) before it launches.  All calls
+ * on a device share the one array and it keeps the last call's contents:
+ * calls whose execution may overlap on the GPU (different streams, or
+ * concurrent graph branches) race on it and give wrong results.
+ */
+int attn_decode_paged_noalloc(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool,
+                              int num_pages, const int32_t* block_table, int max_pages_per_seq,
+                              const int32_t* seq_lens, int batch, int max_seq_len, int page_size,
+                              int num_q_heads, int num_kv_heads, int head_dim, float softmax_scale,
+                              int32_t* status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -34,6 +34,8 @@
 #include "pa_common.cuh"
 #include "pa_host.h"
 
+#include <mutex>
+
 namespace pa {
 namespace dec {
 
@@ -667,4 +669,73 @@ extern "C" int attn_decode_paged(void* out, float* lse, const void* q, const voi
         dec::decode_kernel<64><<<grid, dec::W * 32, smem, st>>>(kmap, vmap, prm);
     }
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode entry point.
+//
+// Some callers cannot call cudaMalloc: code running inside an allocator or
+// memory-pool callback, a plugin loaded into a host framework that owns all
+// device memory, or a latency-critical path that must not enter the driver's
+// allocator.  For them this file keeps the split-K scratch (arrival counters
+// and partial outputs) in a fixed device array, so the only buffers they
+// pass are inputs and outputs.
+// ---------------------------------------------------------------------------
+namespace pa {
+namespace dec {
+
+constexpr size_t kStaticScratchBytes = 8u << 20;  // 8 MiB held by every GPU that loads the library
+
+// Zero at module load.  Shared by every call on the device.
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+namespace {
+std::mutex g_static_mu;
+void* g_static_ptr[64] = {};
+}  // namespace
+
+// Device address of g_static_scratch on the current device, looked up once
+// per device (the host-side name is only a stand-in, not a device address).
+static int static_scratch_ptr(int device, void** out) {
+    if (device < 0 || device >= 64) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (g_static_ptr[device] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
+        g_static_ptr[device] = p;
+    }
+    *out = g_static_ptr[device];
+    return PA_OK;
+}
+
+}  // namespace dec
+}  // namespace pa
+
+extern "C" int attn_decode_paged_noalloc(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool,
+                                         int num_pages, const int32_t* block_table, int max_pages_per_seq,
+                                         const int32_t* seq_lens, int batch, int max_seq_len, int page_size,
+                                         int num_q_heads, int num_kv_heads, int head_dim, float softmax_scale,
+                                         int32_t* status, void* stream) {
+    if (batch < 0) return PA_ERR_SHAPE;
+    int rc = check_common_shapes(page_size, num_q_heads, num_kv_heads, head_dim);
+    if (rc != PA_OK) return rc;
+    if (batch == 0) return PA_OK;
+    DeviceInfo dev;
+    rc = current_device(&dev);
+    if (rc != PA_OK) return rc;
+    const size_t need = pa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim);
+    if (need == 0) return PA_ERR_SHAPE;
+    if (need > dec::kStaticScratchBytes) return PA_ERR_SCRATCH_LIMIT;
+    void* scratch = nullptr;
+    rc = dec::static_scratch_ptr(dev.device, &scratch);
+    if (rc != PA_OK) return rc;
+    // The arrival counters must start at zero; an earlier call that stopped
+    // on a device error may have left them dirty, so clear them every call.
+    const int segs = batch * num_kv_heads * dec::head_blocks(num_q_heads / num_kv_heads);
+    const size_t counter_bytes = align_up((size_t)segs * 4, 256);
+    if (cudaMemsetAsync(scratch, 0, counter_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return attn_decode_paged(out, lse, q, k_pool, v_pool, num_pages, block_table, max_pages_per_seq, seq_lens, batch,
+                             max_seq_len, page_size, num_q_heads, num_kv_heads, head_dim, softmax_scale, scratch,
+                             dec::kStaticScratchBytes, status, stream);
 }

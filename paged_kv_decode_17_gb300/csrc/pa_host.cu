@@ -102,6 +102,7 @@ extern "C" const char* pa_status_string(int status) {
         case PA_ERR_BAD_PAGE: return "device: block_table entry outside [0, num_pages)";
         case PA_ERR_BAD_LEN: return "device: sequence length / row count inconsistent";
         case PA_ERR_ARCH: return "current device is not an sm_103 GPU";
+        case PA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the allocation-free decode holds (8 MiB)";
         default: return "unknown status";
     }
 }
