@@ -398,6 +398,114 @@ def measure_decode_e2e(pa, case, steps, warmup):
     return ms, h2d, d2h
 
 
+def _flush_l2(buf):
+    buf.zero_()
+
+
+def measure_prefill(pa, steps, warmup, peaks):
+    """Varlen causal prefill step: writeback of every new row, then prefill.
+    16 sequences of 512..4096 tokens, Hq=28, Hkv=4, D=128.  L2 is flushed
+    (256 MiB write) between iterations, outside the timed events."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = workloads.varlen_prefill(device=dev)
+    stream = torch.cuda.current_stream()
+    B = case.batch
+    ws = pa.Workspace(pa.prefill_workspace_bytes(B, case.total_q, case.num_q_heads, case.num_kv_heads,
+                                                 case.head_dim), dev)
+    out = torch.empty_like(case.q)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def write():
+        pa.kv_write_paged(case.k_pool, case.v_pool, case.k_new, case.v_new, case.cu_seqlens_q, case.seq_lens,
+                          case.block_table)
+
+    def attn():
+        pa.attn_prefill_varlen_causal(case.q, case.k_pool, case.v_pool, case.block_table, case.cu_seqlens_q,
+                                      case.seq_lens, case.softmax_scale, max_q_len=case.max_q_len,
+                                      max_seq_len=case.max_seq_len, out=out, workspace=ws)
+
+    for _ in range(warmup):
+        write()
+        attn()
+    torch.cuda.synchronize()
+    w_ms, a_ms = [], []
+    for _ in range(steps):
+        _flush_l2(flush)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        write()
+        e[1].record(stream)
+        attn()
+        e[2].record(stream)
+        torch.cuda.synchronize()
+        w_ms.append(e[0].elapsed_time(e[1]))
+        a_ms.append(e[1].elapsed_time(e[2]))
+    flops = roofline.prefill_flops(case.q_lens_host, case.seq_lens_host, case.num_q_heads, case.head_dim)
+    wbytes = roofline.kv_write_bytes(case.total_q, case.num_kv_heads, case.head_dim)
+    a = statistics.median(a_ms)
+    w = statistics.median(w_ms)
+    tflops = flops / (a * 1e-3) / 1e12
+    res = {"workload": "varlen_prefill: 16 sequences, lengths uniform 512..4096 (seeded), no prior tokens, "
+                       "Hq=28, Hkv=4, head_dim 128, 16-token pages; step = writeback of all new rows + prefill",
+           "tokens": case.total_q, "flops_visible_pairs": flops, "prefill_ms": a, "tflops": tflops,
+           "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                        "frac": tflops / peaks["bf16_tflops"], "peak_source": peaks["source"] + " (burst)"},
+           "tokens_per_s": case.total_q / ((a + w) * 1e-3),
+           "kv_write": {"ms": w, "bytes": wbytes, "gbs": wbytes / (w * 1e-3) / 1e9,
+                        "frac_hbm": wbytes / (w * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+           "l2": "flushed (256 MiB write) between iterations", "steps": steps, "launches_per_step": 3}
+    del case, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_mixed(pa, steps, warmup, peaks):
+    """Mixed serving step in one call: 4 prefill chunks of 2048 tokens after
+    0..8192 cached tokens + 60 decodes (1k..64k context) + one 131,072-token
+    decode; Hq=32, Hkv=8, D=128.  Inputs (about 9 GB of KV) exceed L2."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = workloads.mixed_step(device=dev)
+    stream = torch.cuda.current_stream()
+    ws = pa.Workspace(pa.prefill_workspace_bytes(case.batch, case.total_q, case.num_q_heads, case.num_kv_heads,
+                                                 case.head_dim), dev)
+    out = torch.empty_like(case.q)
+
+    def attn():
+        pa.attn_prefill_varlen_causal(case.q, case.k_pool, case.v_pool, case.block_table, case.cu_seqlens_q,
+                                      case.seq_lens, case.softmax_scale, max_q_len=case.max_q_len,
+                                      max_seq_len=case.max_seq_len, out=out, workspace=ws)
+
+    for _ in range(warmup):
+        attn()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        attn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    t = statistics.median(ms)
+    dec = [(L, q) for L, q in zip(case.seq_lens_host, case.q_lens_host) if q == 1]
+    pre_q = [q for q in case.q_lens_host if q > 1]
+    pre_L = [L for L, q in zip(case.seq_lens_host, case.q_lens_host) if q > 1]
+    dbytes = roofline.decode_kv_bytes([L for L, _ in dec], case.num_kv_heads, case.head_dim)
+    flops = roofline.prefill_flops(pre_q, pre_L, case.num_q_heads, case.head_dim)
+    t_bytes = dbytes / (peaks["hbm_gbs"] * 1e9)
+    t_flops = flops / (peaks["bf16_tflops"] * 1e12)
+    res = {"workload": "mixed_step: 4 prefill chunks x 2048 tokens (0..8192 prior) + 60 decodes (1k..64k) + "
+                       "1 decode at 131072; Hq=32, Hkv=8, head_dim 128, 16-token pages",
+           "step_ms": t, "decode_kv_bytes": dbytes, "prefill_flops": flops,
+           "t_roofline_ms": 1e3 * max(t_bytes, t_flops), "t_serial_roofline_ms": 1e3 * (t_bytes + t_flops),
+           "frac_of_roofline": max(t_bytes, t_flops) / (t * 1e-3),
+           "tokens_per_s": case.total_q / (t * 1e-3), "launches_per_step": 2, "steps": steps,
+           "l2": "inputs larger than L2 (about 9 GB of KV)"}
+    del case
+    torch.cuda.empty_cache()
+    return res
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -405,6 +513,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-only", action="store_true", help="skip the prefill and mixed-step measurements")
+    ap.add_argument("--only", choices=["prefill", "mixed"], default=None,
+                    help="run just this extra measurement (for profiling); prints its object only")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
 
@@ -417,6 +528,12 @@ def main(argv=None):
     pa.load_library(build_if_missing=True)
     peaks = load_peaks()
     dev = torch.device("cuda", torch.cuda.current_device())
+    if args.only is not None:
+        fn = measure_prefill if args.only == "prefill" else measure_mixed
+        res = fn(pa, args.steps, args.warmup, peaks)
+        if rank == 0:
+            print(json.dumps({"only": args.only, args.only: res}), flush=True)
+        return 0
 
     case = workloads.qwen7b_decode(device=dev, seed=1 + rank)
     kv_bytes = roofline.decode_kv_bytes(case.seq_lens_host, case.num_kv_heads, case.head_dim)
@@ -457,6 +574,11 @@ def main(argv=None):
         "clocks": clocks,
         "kv_write_ms": statistics.mean(kvw_ms),
     }
+    if not args.decode_only:
+        psteps = max(3, min(args.steps, 20))
+        line["prefill"] = measure_prefill(pa, psteps, 3, peaks)
+        line["mixed"] = measure_mixed(pa, psteps, 3, peaks)
+        line["gpu_launches"] += world * psteps * (3 + 2)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_subprocess()
     if rank == 0:

@@ -47,7 +47,7 @@
  *                    scaled scores of each row (-inf for a row with no key).
  * Query head h attends KV head h / (num_q_heads / num_kv_heads).
  *
- * Supported shapes: head_dim 64 or 128; page_size a multiple of 16 up to
+ * Supported shapes: head_dim 64 or 128; page_size a power of two from 16 to
  * 256; num_q_heads a multiple of num_kv_heads; num_q_heads / num_kv_heads
  * up to 128.
  *
@@ -172,8 +172,9 @@ int kv_write_paged(void* k_pool, void* v_pool, int num_pages, const void* k_new,
  * which every GPU that loads the library holds until the process exits.
  * Problems whose workspace (pa_decode_workspace_bytes) exceeds 8 MiB are
  * rejected with PA_ERR_SCRATCH_LIMIT before anything is enqueued; roughly,
- * batch * num_kv_heads * ceil((num_q_heads/num_kv_heads)/16) + SM count
- * must stay below about 1000 at head_dim 128 (about 2000 at head_dim 64).
+ * batch * num_kv_heads * ceil((num_q_heads/num_kv_heads)/16) plus twice the
+ * SM count must stay below about 1000 at head_dim 128 (about 2000 at
+ * head_dim 64).
  *
  * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
  * The first call on each device looks up the array's device address

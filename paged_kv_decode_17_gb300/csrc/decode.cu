@@ -43,18 +43,18 @@ constexpr int W = 4;           // warps per CTA
 constexpr int UNIT = 16;       // tokens per unit
 constexpr int MAXR = 16;       // query heads per head block (mma M)
 constexpr int MIN_CHUNK = 16;  // minimum units per CTA
-constexpr int CTAS_PER_SM = 1;
+constexpr int CTAS_PER_SM = 2;  // two CTAs (8 warps) per SM hide each other's latency
 
 template <int D>
 struct Cfg {
-    static constexpr int DEPTH = (D == 128) ? 5 : 8;
+    static constexpr int DEPTH = (D == 128) ? 3 : 6;
     static constexpr int BOXES = D / 64;             // 128-byte-wide TMA boxes per row
     static constexpr int BOX_BYTES = UNIT * 128;     // 16 rows x 128 bytes
     static constexpr int UNIT_BYTES = UNIT * D * 2;  // one K or V unit
     static constexpr int STAGE_BYTES = 2 * UNIT_BYTES;
     static constexpr int STAGES_BYTES = W * DEPTH * STAGE_BYTES;
     static constexpr int MSTRIDE = D + 4;  // fp32 row stride of the merge buffer
-    static constexpr int MERGE_BYTES = W * MAXR * MSTRIDE * 4;
+    static constexpr int MERGE_BYTES = MAXR * MSTRIDE * 4;  // warps add into it one after another
     static constexpr int SMEM_BYTES = 1024 + STAGES_BYTES + MERGE_BYTES;
 };
 
@@ -64,11 +64,12 @@ struct Params {
     const __nv_bfloat16* q;
     const int32_t* block_table;
     const int32_t* seq_lens;
+    const int32_t* cu_q;  // non-null in a mixed call: only entries with one query row are decoded here
     int32_t* counters;
     float* ws_lse;  // [slots][MAXR], log2 domain
     float* ws_o;    // [slots][MAXR][D], normalised
     int32_t* status;
-    int num_pages, max_pages, batch, page_size;
+    int num_pages, max_pages, batch, page_size, ps_shift;  // page_size = 1 << ps_shift
     int Hq, Hkv, group, HB, R;
     float scale_log2;
 };
@@ -79,7 +80,20 @@ struct Seg {
     int b, g, hb, len, n, start, end;
 };
 
+// Is sequence b served by this kernel?  Always in a decode call; in a mixed
+// call only when it contributes exactly one query row.
+__device__ __forceinline__ bool is_decode_entry(const Params& p, int b) {
+    return p.cu_q == nullptr || __ldg(p.cu_q + b + 1) - __ldg(p.cu_q + b) == 1;
+}
+
+// Row of q / out holding sequence b's query.
+__device__ __forceinline__ size_t q_row(const Params& p, int b) {
+    return p.cu_q == nullptr ? (size_t)b : (size_t)__ldg(p.cu_q + b);
+}
+
+// Keys of sequence b this kernel attends over (0 for entries it does not serve).
 __device__ __forceinline__ int load_len(const Params& p, int b) {
+    if (!is_decode_entry(p, b)) return 0;
     int len = __ldg(p.seq_lens + b);
     const int cap = p.max_pages * p.page_size;
     if (len < 0 || len > cap) {
@@ -133,8 +147,8 @@ __device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, 
     using C = Cfg<D>;
     const int j = it.u - it.seg.start;  // unit index within the sequence
     const int tok0 = j * UNIT;
-    const int page = tok0 / p.page_size;
-    const int sub = (tok0 - page * p.page_size) / UNIT;
+    const int page = tok0 >> p.ps_shift;
+    const int sub = (tok0 - (page << p.ps_shift)) / UNIT;
     if (lane == 0) {
         const int phys = __ldg(p.block_table + (size_t)it.seg.b * p.max_pages + page);
         if (phys < 0 || phys >= p.num_pages) {
@@ -156,7 +170,7 @@ __device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, 
 }
 
 template <int D>
-__global__ void __launch_bounds__(W * 32, 1)
+__global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const Params p) {
     using C = Cfg<D>;
@@ -186,12 +200,13 @@ __global__ void __launch_bounds__(W * 32, 1)
             if (b < p.batch) {
                 const int len = load_len(p, b);
                 n = (len + UNIT - 1) / UNIT * p.Hkv * p.HB;
-                if (len == 0 && (b % gridDim.x) == blockIdx.x) {
+                if (len == 0 && (b % gridDim.x) == blockIdx.x && is_decode_entry(p, b)) {
                     // empty sequence: defined result, out = 0, lse = -inf
+                    const size_t row = q_row(p, b);
                     for (int h = 0; h < p.Hq; ++h) {
-                        uint4* o = reinterpret_cast<uint4*>(p.out + ((size_t)b * p.Hq + h) * D);
+                        uint4* o = reinterpret_cast<uint4*>(p.out + (row * p.Hq + h) * D);
                         for (int c = 0; c < D / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
-                        if (p.lse) p.lse[(size_t)b * p.Hq + h] = -INFINITY;
+                        if (p.lse) p.lse[row * p.Hq + h] = -INFINITY;
                     }
                 }
             }
@@ -298,8 +313,9 @@ __global__ void __launch_bounds__(W * 32, 1)
         // Q fragments of the head block (rows >= `rows` are zero)
         uint32_t qa[KSTEPS][4];
         {
-            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(p.q + ((size_t)cs.b * p.Hq + h0 + qr) * D);
-            const uint32_t* q8 = reinterpret_cast<const uint32_t*>(p.q + ((size_t)cs.b * p.Hq + h0 + qr + 8) * D);
+            const size_t qrow = q_row(p, cs.b);
+            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(p.q + (qrow * p.Hq + h0 + qr) * D);
+            const uint32_t* q8 = reinterpret_cast<const uint32_t*>(p.q + (qrow * p.Hq + h0 + qr + 8) * D);
             const bool r0ok = qr < rows, r8ok = qr + 8 < rows;
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
@@ -345,7 +361,10 @@ __global__ void __launch_bounds__(W * 32, 1)
                 }
                 const uint32_t kb = smem_u32(sk), vb = smem_u32(sv);
                 // S = Q K^T  (16 heads x 16 keys)
+                // two independent accumulator chains (even / odd k-steps) halve the
+                // dependent mma latency; summed below
                 float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; ++kk) {
                     const int dch = kk * 2 + k_dsel;
@@ -353,9 +372,18 @@ __global__ void __launch_bounds__(W * 32, 1)
                         kb + (dch >> 3) * C::BOX_BYTES + k_key * 128 + (((dch & 7) ^ (k_key & 7)) << 4);
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4(addr, b0, b1, b2, b3);
-                    mma_16816(s[0], qa[kk], b0, b1);
-                    mma_16816(s[1], qa[kk], b2, b3);
+                    if (kk & 1) {
+                        mma_16816(s2[0], qa[kk], b0, b1);
+                        mma_16816(s2[1], qa[kk], b2, b3);
+                    } else {
+                        mma_16816(s[0], qa[kk], b0, b1);
+                        mma_16816(s[1], qa[kk], b2, b3);
+                    }
                 }
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s[j][e] += s2[j][e];
                 // scale to log2 domain, mask keys >= valid
                 float x[2][4];
 #pragma unroll
@@ -453,46 +481,54 @@ __global__ void __launch_bounds__(W * 32, 1)
             }
             const float sc0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - M0);
             const float sc1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - M1);
-            float* mo = merge_o + warp * MAXR * C::MSTRIDE;
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                const int col = n * 8 + qc;
-                *reinterpret_cast<float2*>(mo + qr * C::MSTRIDE + col) = make_float2(o[n][0] * sc0, o[n][1] * sc0);
-                *reinterpret_cast<float2*>(mo + (qr + 8) * C::MSTRIDE + col) =
-                    make_float2(o[n][2] * sc1, o[n][3] * sc1);
-            }
             if (warp == 0 && (lane & 3) == 0) {
                 s_M[qr] = M0;
                 s_L[qr] = L0;
                 s_M[qr + 8] = M1;
                 s_L[qr + 8] = L1;
             }
+            // warps add their rescaled O into one buffer in a fixed order
+#pragma unroll 1
+            for (int w = 0; w < W; ++w) {
+                if (warp == w) {
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        const int col = n * 8 + qc;
+                        float2* a0 = reinterpret_cast<float2*>(merge_o + qr * C::MSTRIDE + col);
+                        float2* a1 = reinterpret_cast<float2*>(merge_o + (qr + 8) * C::MSTRIDE + col);
+                        float2 v0 = make_float2(o[n][0] * sc0, o[n][1] * sc0);
+                        float2 v1 = make_float2(o[n][2] * sc1, o[n][3] * sc1);
+                        if (w > 0) {
+                            const float2 p0 = *a0, p1 = *a1;
+                            v0.x += p0.x;
+                            v0.y += p0.y;
+                            v1.x += p1.x;
+                            v1.y += p1.y;
+                        }
+                        *a0 = v0;
+                        *a1 = v1;
+                    }
+                }
+                __syncthreads();
+            }
         }
-        __syncthreads();
         const int c0 = cs.start / chunk, c1 = (cs.end - 1) / chunk;
         const int sid = (cs.b * p.Hkv + cs.g) * p.HB + cs.hb;
         const bool single = (c0 == c1);
+        const size_t orow = q_row(p, cs.b);
         for (int idx = tid; idx < rows * (D / 4); idx += W * 32) {
             const int r = idx / (D / 4);
             const int d4 = idx - r * (D / 4);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int w = 0; w < W; ++w) {
-                const float4 v = *reinterpret_cast<const float4*>(merge_o + (w * MAXR + r) * C::MSTRIDE + d4 * 4);
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
-            }
+            const float4 acc = *reinterpret_cast<const float4*>(merge_o + r * C::MSTRIDE + d4 * 4);
             const float L = s_L[r];
             const float inv = L > 0.f ? 1.f / L : 0.f;
             if (single) {
                 uint2 ob;
                 ob.x = pack_bf16x2(acc.x * inv, acc.y * inv);
                 ob.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-                *reinterpret_cast<uint2*>(p.out + ((size_t)cs.b * p.Hq + h0 + r) * D + d4 * 4) = ob;
+                *reinterpret_cast<uint2*>(p.out + (orow * p.Hq + h0 + r) * D + d4 * 4) = ob;
                 if (p.lse != nullptr && d4 == 0)
-                    p.lse[(size_t)cs.b * p.Hq + h0 + r] = L > 0.f ? (s_M[r] + lg2(L)) * kLn2 : -INFINITY;
+                    p.lse[orow * p.Hq + h0 + r] = L > 0.f ? (s_M[r] + lg2(L)) * kLn2 : -INFINITY;
             } else {
                 const size_t slot = (size_t)blockIdx.x + sid;
                 *reinterpret_cast<float4*>(p.ws_o + (slot * MAXR + r) * D + d4 * 4) =
@@ -536,9 +572,9 @@ __global__ void __launch_bounds__(W * 32, 1)
                     uint2 ob;
                     ob.x = pack_bf16x2(acc.x * inv, acc.y * inv);
                     ob.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-                    *reinterpret_cast<uint2*>(p.out + ((size_t)cs.b * p.Hq + h0 + r) * D + d4 * 4) = ob;
+                    *reinterpret_cast<uint2*>(p.out + (orow * p.Hq + h0 + r) * D + d4 * 4) = ob;
                     if (p.lse != nullptr && d4 == 0)
-                        p.lse[(size_t)cs.b * p.Hq + h0 + r] = L > 0.f ? (M + lg2(L)) * kLn2 : -INFINITY;
+                        p.lse[orow * p.Hq + h0 + r] = L > 0.f ? (M + lg2(L)) * kLn2 : -INFINITY;
                 }
                 if (tid == 0) p.counters[sid] = 0;  // leave the workspace ready for the next call
             }
@@ -589,11 +625,17 @@ extern "C" size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_
     return dec::ws_layout(slots, segs, head_dim).total;
 }
 
-extern "C" int attn_decode_paged(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool,
-                                 int num_pages, const int32_t* block_table, int max_pages_per_seq,
-                                 const int32_t* seq_lens, int batch, int max_seq_len, int page_size, int num_q_heads,
-                                 int num_kv_heads, int head_dim, float softmax_scale, void* workspace,
-                                 size_t workspace_bytes, int32_t* status, void* stream) {
+namespace pa {
+namespace dec {
+
+// Launch the split-K decode.  cu_q == nullptr: one query row per sequence
+// (row b).  Otherwise (a mixed prefill + decode call): only sequences with
+// exactly one query row are served, reading/writing row cu_q[b].
+int launch_decode(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool, int num_pages,
+                  const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
+                  const int32_t* cu_q, int batch, int max_seq_len, int page_size, int num_q_heads,
+                  int num_kv_heads, int head_dim, float softmax_scale, void* workspace, size_t workspace_bytes,
+                  int32_t* status, void* stream) {
     if (batch < 0 || max_seq_len < 0) return PA_ERR_SHAPE;
     int rc = check_common_shapes(page_size, num_q_heads, num_kv_heads, head_dim);
     if (rc != PA_OK) return rc;
@@ -640,6 +682,7 @@ extern "C" int attn_decode_paged(void* out, float* lse, const void* q, const voi
     prm.q = static_cast<const __nv_bfloat16*>(q);
     prm.block_table = block_table;
     prm.seq_lens = seq_lens;
+    prm.cu_q = cu_q;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     prm.counters = reinterpret_cast<int32_t*>(ws + wl.counters);
     prm.ws_lse = reinterpret_cast<float*>(ws + wl.lse);
@@ -649,6 +692,7 @@ extern "C" int attn_decode_paged(void* out, float* lse, const void* q, const voi
     prm.max_pages = max_pages_per_seq;
     prm.batch = batch;
     prm.page_size = page_size;
+    prm.ps_shift = __builtin_ctz((unsigned)page_size);
     prm.Hq = num_q_heads;
     prm.Hkv = num_kv_heads;
     prm.group = group;
@@ -669,6 +713,19 @@ extern "C" int attn_decode_paged(void* out, float* lse, const void* q, const voi
         dec::decode_kernel<64><<<grid, dec::W * 32, smem, st>>>(kmap, vmap, prm);
     }
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace dec
+}  // namespace pa
+
+extern "C" int attn_decode_paged(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool,
+                                 int num_pages, const int32_t* block_table, int max_pages_per_seq,
+                                 const int32_t* seq_lens, int batch, int max_seq_len, int page_size, int num_q_heads,
+                                 int num_kv_heads, int head_dim, float softmax_scale, void* workspace,
+                                 size_t workspace_bytes, int32_t* status, void* stream) {
+    return dec::launch_decode(out, lse, q, k_pool, v_pool, num_pages, block_table, max_pages_per_seq, seq_lens,
+                              nullptr, batch, max_seq_len, page_size, num_q_heads, num_kv_heads, head_dim,
+                              softmax_scale, workspace, workspace_bytes, status, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -77,6 +77,19 @@ int encode_rows_map_noswizzle(CUtensorMap* map, const void* base, uint64_t rows,
     return encode_impl(map, base, rows, row_elems, box_cols, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+int encode_q_map(CUtensorMap* map, const void* q, int total_q, int Hq, int D) {
+    std::call_once(g_encode_once, load_encode);
+    if (g_encode == nullptr) return PA_ERR_CUDA;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)total_q};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2u, (cuuint64_t)Hq * D * 2u};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 int set_smem_limit_once(const void* kernel, int bytes, int device, int slot) {
     if (device < 0 || device >= kMaxDevices || slot < 0 || slot >= kMaxKernelSlots) return PA_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);

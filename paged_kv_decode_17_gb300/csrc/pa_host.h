@@ -32,6 +32,10 @@ int encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t 
 int encode_rows_map_noswizzle(CUtensorMap* map, const void* base, uint64_t rows, uint32_t row_elems,
                               uint32_t box_cols, uint32_t box_rows);
 
+// 3-D bf16 tensor map over q [total_q][Hq][D] with box {64, 1, 128} and
+// 128-byte swizzle: one head's 128-row tile, 64 columns at a time.
+int encode_q_map(CUtensorMap* map, const void* q, int total_q, int Hq, int D);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -39,11 +43,21 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Checks shared by every entry point.
 inline int check_common_shapes(int page_size, int num_q_heads, int num_kv_heads, int head_dim) {
     if (head_dim != 64 && head_dim != 128) return PA_ERR_SHAPE;
-    if (page_size < 16 || page_size > 256 || page_size % 16 != 0) return PA_ERR_SHAPE;
+    if (page_size < 16 || page_size > 256 || (page_size & (page_size - 1)) != 0) return PA_ERR_SHAPE;
     if (num_kv_heads < 1 || num_q_heads < num_kv_heads || num_q_heads % num_kv_heads != 0) return PA_ERR_SHAPE;
     if (num_q_heads / num_kv_heads > 128) return PA_ERR_SHAPE;
     return PA_OK;
 }
+
+namespace dec {
+// Split-K decode launcher (decode.cu); cu_q != nullptr serves the q_len == 1
+// entries of a mixed prefill + decode call.
+int launch_decode(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool, int num_pages,
+                  const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
+                  const int32_t* cu_q, int batch, int max_seq_len, int page_size, int num_q_heads,
+                  int num_kv_heads, int head_dim, float softmax_scale, void* workspace, size_t workspace_bytes,
+                  int32_t* status, void* stream);
+}  // namespace dec
 
 // Set the dynamic shared-memory limit of a kernel once per device.
 int set_smem_limit_once(const void* kernel, int bytes, int device, int slot);

@@ -1,0 +1,554 @@
+// Varlen causal prefill over a paged KV cache on tcgen05 tensor cores.
+//
+// What it computes ("The Stack Below the Stack, Part 2", section 2.1; "8.
+// Kernels and Attention Backends", section "Attention is an I/O problem"):
+// exact softmax attention, tiled.  Query tiles of 128 rows and key tiles of 64
+// keys stream through on-chip memory; each row carries a running maximum and
+// a running sum of exponentials, and the output accumulated so far is
+// rescaled when the maximum grows, so the result equals the untiled softmax.
+// Row i of a sequence with q_len rows and seq_len keys sits at position
+// seq_len - q_len + i and sees keys 0 .. that position.
+//
+// GB300 design (one CTA = one 128-row query tile of one sequence, for two
+// query heads that share a KV head, so each K/V tile is loaded once for both):
+// * warp 8 (TMA): loads the two Q tiles once, then K and V tiles through a
+//   5-stage ring; a 64-key tile is four 16-row page blocks gathered through
+//   the block table, each a 128-byte-swizzled TMA box.
+// * warp 9 (MMA): one thread issues tcgen05.mma: S_h = Q_h K^T into TMEM
+//   (fp32, 64 columns per head) and O_h += P_h V into TMEM (fp32, D columns
+//   per head).  The issue order S(j+1), PV(j) lets the tensor core compute the
+//   next scores while the softmax of the current tile runs.
+// * warps 0-3 / 4-7: softmax for head 0 / head 1, one thread per query row
+//   (its TMEM lane).  They read S with tcgen05.ld, mask, update the running
+//   max/sum, write P (bf16) to shared memory in the MMA operand layout, and at
+//   the end normalise O and store it.  O lives in TMEM; it is rescaled only
+//   when a row's maximum grows by more than TAU = 8 (log2 units): until then
+//   the exponentials are taken against the older, smaller maximum, which
+//   keeps them <= 2^8 and the result exact, because the final division uses
+//   the same reference maximum for numerator and denominator.
+// Every wait is bounded; a timeout sets a CTA-wide abort flag, records
+// PA_ERR_TIMEOUT and all roles fall through to a clean exit.
+#include "pa_common.cuh"
+#include "pa_host.h"
+
+namespace pa {
+namespace pf {
+
+constexpr int BM = 128;      // query rows per tile (= TMEM lanes)
+constexpr int BN = 64;       // keys per KV tile
+constexpr int NSTAGE = 5;    // K/V ring depth (K and V tiles alternate)
+constexpr float TAU = 8.f;   // rescale threshold, log2 units
+constexpr int NTHREADS = 320;
+constexpr int WARP_TMA = 8, WARP_MMA = 9;
+
+template <int D>
+struct Cfg {
+    static constexpr int KB = D / 64;               // 128-byte column blocks per row
+    static constexpr int Q_BYTES = BM * D * 2;      // one head's Q tile
+    static constexpr int KV_BYTES = BN * D * 2;     // one K or V tile
+    static constexpr int P_BYTES = BM * BN * 2;     // one P tile
+    static constexpr int Q_KB = BM * 128;           // bytes per column block of a Q tile
+    static constexpr int KV_KB = BN * 128;          // bytes per column block of a K/V tile
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_P = 2 * Q_BYTES;       // P[head][buffer]
+    static constexpr int OFF_KV = OFF_P + 4 * P_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + OFF_KV + NSTAGE * KV_BYTES;
+    static constexpr int TM_S0 = 0;
+    static constexpr int TM_O0 = 2 * BN;
+    static constexpr int TM_COLS = (2 * BN + 2 * D) <= 256 ? 256 : 512;
+    static constexpr uint32_t IDESC_S = tc::idesc_bf16(BM, BN, 0, 0);   // Q K-major, K K-major
+    static constexpr uint32_t IDESC_PV = tc::idesc_bf16(BM, D, 0, 1);   // P K-major, V MN-major
+};
+
+struct Params {
+    __nv_bfloat16* out;
+    float* lse;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    const int32_t* cu_q;
+    int32_t* status;
+    int num_pages, max_pages, batch, page_size;
+    int Hq, Hkv, group, NP;
+    int skip_single;  // sequences with q_len == 1 are served by the decode kernel
+    float scale_log2;
+};
+
+struct Shared {
+    uint64_t bar_q;
+    uint64_t kv_full[NSTAGE];
+    uint64_t kv_empty[NSTAGE];
+    uint64_t s_full[2], s_free[2], p_ready[2], pv_done[2];
+    uint32_t tmem_base;
+    int abort_flag;
+    int item[8];
+};
+
+__device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, Shared& sh, int32_t* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*reinterpret_cast<volatile int*>(&sh.abort_flag)) return false;
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            *reinterpret_cast<volatile int*>(&sh.abort_flag) = 1;
+            report(status, PA_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                            int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+// number of 128-row tiles of sequence b served by this kernel (0 if none)
+__device__ __forceinline__ int seq_tiles(const Params& p, int b, int& q_len, int& seq_len) {
+    q_len = __ldg(p.cu_q + b + 1) - __ldg(p.cu_q + b);
+    seq_len = __ldg(p.seq_lens + b);
+    if (q_len < 0 || seq_len < q_len || seq_len > p.max_pages * p.page_size) {
+        report(p.status, PA_ERR_BAD_LEN);
+        return 0;
+    }
+    if (q_len == 0 || (p.skip_single && q_len == 1)) return 0;
+    return (q_len + BM - 1) / BM;
+}
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, const Params p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ Shared sh;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+
+    // ---- which (sequence, tile, KV head, head pair) this CTA computes
+    if (warp == 0) {
+        const int per = p.Hkv * p.NP;
+        const int T = blockIdx.x / per;
+        const int rem = blockIdx.x - T * per;
+        int found_b = -1, found_P = 0, found_n = 0, P = 0;
+        for (int b0 = 0; b0 < p.batch && found_b < 0; b0 += 32) {
+            const int b = b0 + lane;
+            int ql = 0, sl = 0, n = 0;
+            if (b < p.batch) n = seq_tiles(p, b, ql, sl);
+            const int incl = warp_incl_scan(n);
+            const int tot = __shfl_sync(0xffffffffu, incl, 31);
+            if (T < P + tot) {
+                const unsigned hit = __ballot_sync(0xffffffffu, P + incl > T);
+                const int l = __ffs(hit) - 1;
+                found_b = b0 + l;
+                found_P = P + __shfl_sync(0xffffffffu, incl - n, l);
+                found_n = __shfl_sync(0xffffffffu, n, l);
+            }
+            P += tot;
+        }
+        if (lane == 0) {
+            sh.item[0] = found_b;
+            if (found_b >= 0) {
+                const int g = rem / p.NP;
+                const int pair = rem - g * p.NP;
+                const int ql = __ldg(p.cu_q + found_b + 1) - __ldg(p.cu_q + found_b);
+                const int sl = __ldg(p.seq_lens + found_b);
+                const int t = found_n - 1 - (T - found_P);  // heaviest tile of the sequence first
+                sh.item[1] = t;
+                sh.item[2] = ql;
+                sh.item[3] = sl;
+                sh.item[4] = __ldg(p.cu_q + found_b) + t * BM;    // first q row of the tile
+                sh.item[5] = g;
+                sh.item[6] = g * p.group + 2 * pair;               // first query head
+                sh.item[7] = min(2, p.group - 2 * pair);           // heads in this CTA
+            }
+            sh.abort_flag = 0;
+        }
+    }
+    if (tid == 0) {
+        mbar_init(&sh.bar_q, 1);
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(&sh.kv_full[s], 1);
+            mbar_init(&sh.kv_empty[s], 1);
+        }
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&sh.s_full[h], 1);
+            mbar_init(&sh.s_free[h], 4 * 32);
+            mbar_init(&sh.p_ready[h], 4 * 32);
+            mbar_init(&sh.pv_done[h], 1);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (sh.item[0] < 0) return;  // uniform: no tile for this CTA
+
+    const int b = sh.item[0];
+    const int t = sh.item[1];
+    const int q_len = sh.item[2];
+    const int seq_len = sh.item[3];
+    const int row0 = sh.item[4];
+    const int g = sh.item[5];
+    const int h0 = sh.item[6];
+    const int nheads = sh.item[7];
+    const int prior = seq_len - q_len;
+    const int rows_valid = min(BM, q_len - t * BM);
+    const int qmin = prior + t * BM;                 // position of the tile's first row
+    const int qlast = qmin + rows_valid - 1;         // position of its last valid row
+    const int n_kv = qlast / BN + 1;                 // key tiles 0 .. n_kv-1
+
+    if (warp == WARP_TMA) {
+        tc::tmem_alloc(&sh.tmem_base, C::TM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = sh.tmem_base;
+
+    uint8_t* sQ = smem + C::OFF_Q;
+    uint8_t* sP = smem + C::OFF_P;
+    uint8_t* sKV = smem + C::OFF_KV;
+
+    if (warp == WARP_TMA) {
+        // ===================================================== producer
+        if (lane == 0) {
+            prefetch_tensormap(&qmap);
+            prefetch_tensormap(&kmap);
+            prefetch_tensormap(&vmap);
+            mbar_arrive_expect_tx(&sh.bar_q, nheads * C::Q_BYTES);
+            for (int hh = 0; hh < nheads; ++hh)
+                for (int kb = 0; kb < C::KB; ++kb)
+                    tma_load_3d(sQ + hh * C::Q_BYTES + kb * C::Q_KB, &qmap, &sh.bar_q, kb * 64, h0 + hh, row0);
+            const int32_t* bt = p.block_table + (size_t)b * p.max_pages;
+            int issued = 0;
+            for (int j = 0; j < n_kv; ++j) {
+                // the four 16-key blocks of this tile: physical rows in the pool
+                int rowsel[4];
+                int good = 0;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int key0 = j * BN + u * 16;
+                    rowsel[u] = -1;
+                    if (key0 < seq_len) {
+                        const int page = key0 / p.page_size;
+                        const int phys = __ldg(bt + page);
+                        if (phys < 0 || phys >= p.num_pages) {
+                            report(p.status, PA_ERR_BAD_PAGE);
+                        } else {
+                            rowsel[u] = (phys * p.Hkv + g) * p.page_size + (key0 - page * p.page_size);
+                            ++good;
+                        }
+                    }
+                }
+                for (int x = 0; x < 2; ++x) {
+                    const int i = 2 * j + x;
+                    const int s = i % NSTAGE;
+                    if (!wait_ab(&sh.kv_empty[s], ((i / NSTAGE) & 1) ^ 1, sh, p.status)) break;
+                    uint8_t* dst = sKV + s * C::KV_BYTES;
+                    if (good == 0) {
+                        mbar_arrive(&sh.kv_full[s]);
+                    } else {
+                        mbar_arrive_expect_tx(&sh.kv_full[s], good * 16 * D * 2);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            if (rowsel[u] < 0) continue;
+#pragma unroll
+                            for (int kb = 0; kb < C::KB; ++kb)
+                                tma_load_2d(dst + kb * C::KV_KB + u * 2048, x == 0 ? &kmap : &vmap,
+                                            &sh.kv_full[s], kb * 64, rowsel[u]);
+                        }
+                    }
+                    ++issued;
+                }
+                if (*reinterpret_cast<volatile int*>(&sh.abort_flag)) break;
+            }
+            // never exit with a copy still landing in shared memory
+            mbar_wait(&sh.bar_q, 0);
+            for (int i = max(0, issued - NSTAGE); i < issued; ++i) mbar_wait(&sh.kv_full[i % NSTAGE], (i / NSTAGE) & 1);
+        }
+        __syncwarp();
+    } else if (warp == WARP_MMA) {
+        // ===================================================== MMA issuer
+        if (lane == 0) {
+            const uint32_t q_base = smem_u32(sQ);
+            const uint32_t p_base = smem_u32(sP);
+            const uint32_t kv_base = smem_u32(sKV);
+            bool ok = wait_ab(&sh.bar_q, 0, sh, p.status);
+            tc::fence_after_sync();
+            auto issue_s = [&](int hh, int j) {
+                const int s = (2 * j) % NSTAGE;
+                const uint32_t kaddr = kv_base + s * C::KV_BYTES;
+                const uint32_t qaddr = q_base + hh * C::Q_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t ad = tc::smem_desc_sw128(qaddr + (kk >> 2) * C::Q_KB + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = tc::smem_desc_sw128(kaddr + (kk >> 2) * C::KV_KB + (kk & 3) * 32, 16, 1024);
+                    tc::mma_ss(tmem + C::TM_S0 + hh * BN, ad, bd, C::IDESC_S, kk > 0);
+                }
+                tc::commit(&sh.s_full[hh]);
+            };
+            auto issue_pv = [&](int hh, int j) {
+                const int s = (2 * j + 1) % NSTAGE;
+                const uint32_t vaddr = kv_base + s * C::KV_BYTES;
+                const uint32_t paddr = p_base + (hh * 2 + (j & 1)) * C::P_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint64_t ad = tc::smem_desc_sw128(paddr + kk * 32, 16, 1024);
+                    const uint64_t bd = tc::smem_desc_sw128(vaddr + kk * 2048, C::KV_KB, 1024);
+                    tc::mma_ss(tmem + C::TM_O0 + hh * D, ad, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::commit(&sh.pv_done[hh]);
+            };
+            // prologue: scores of key tile 0
+            if (ok) ok = wait_ab(&sh.kv_full[0], 0, sh, p.status);
+            if (ok) {
+                tc::fence_after_sync();
+                for (int hh = 0; hh < nheads; ++hh) issue_s(hh, 0);
+                tc::commit(&sh.kv_empty[0]);
+            }
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int ik = 2 * (j + 1), iv = 2 * j + 1;
+                const bool more = j + 1 < n_kv;
+                if (more) {
+                    ok = wait_ab(&sh.kv_full[ik % NSTAGE], (ik / NSTAGE) & 1, sh, p.status);
+                    if (!ok) break;
+                }
+                ok = wait_ab(&sh.kv_full[iv % NSTAGE], (iv / NSTAGE) & 1, sh, p.status);
+                if (!ok) break;
+                for (int hh = 0; hh < nheads && ok; ++hh) {
+                    if (more) {
+                        ok = wait_ab(&sh.s_free[hh], j & 1, sh, p.status);
+                        if (!ok) break;
+                        tc::fence_after_sync();
+                        issue_s(hh, j + 1);
+                    }
+                    ok = wait_ab(&sh.p_ready[hh], j & 1, sh, p.status);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    issue_pv(hh, j);
+                }
+                if (!ok) break;
+                if (more) tc::commit(&sh.kv_empty[ik % NSTAGE]);
+                tc::commit(&sh.kv_empty[iv % NSTAGE]);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ===================================================== softmax (one thread per row)
+        const int hh = warp >> 2;
+        if (hh < nheads) {
+            const int quarter = warp & 3;
+            const int r = quarter * 32 + lane;  // tile row = TMEM lane
+            const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            const uint32_t t_s = tmem + lane_off + C::TM_S0 + hh * BN;
+            const uint32_t t_o = tmem + lane_off + C::TM_O0 + hh * D;
+            const int qpos = qmin + r;
+            float m_ref = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int j = 0; j < n_kv; ++j) {
+                ok = __all_sync(0xffffffffu, wait_ab(&sh.s_full[hh], j & 1, sh, p.status));
+                if (!ok) break;
+                tc::fence_after_sync();
+                uint32_t sr[2][32];
+                tc::ld_32x32b_x32(t_s, sr[0]);
+                tc::ld_32x32b_x32(t_s + 32, sr[1]);
+                tc::wait_ld();
+                tc::fence_before_sync();
+                mbar_arrive(&sh.s_free[hh]);
+
+                const bool diag = (j + 1) * BN - 1 > qmin;
+                float x[BN];
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < BN; ++c) {
+                    const float v = __uint_as_float(sr[c >> 5][c & 31]) * p.scale_log2;
+                    x[c] = (diag && j * BN + c > qpos) ? -INFINITY : v;
+                    mx = fmaxf(mx, x[c]);
+                }
+                if (j == 0) {
+                    m_ref = mx;
+                } else {
+                    const bool need = mx > m_ref + TAU;
+                    if (__any_sync(0xffffffffu, need)) {
+                        const float m_new = fmaxf(m_ref, mx);
+                        const float alpha = ex2(m_ref - m_new);
+                        ok = __all_sync(0xffffffffu, wait_ab(&sh.pv_done[hh], (j - 1) & 1, sh, p.status));
+                        if (!ok) break;
+                        tc::fence_after_sync();
+#pragma unroll 1
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t o[32];
+                            tc::ld_32x32b_x32(t_o + c0, o);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                            tc::st_32x32b_x32(t_o + c0, o);
+                        }
+                        tc::wait_st();
+                        l *= alpha;
+                        m_ref = m_new;
+                    }
+                }
+                float rs = 0.f;
+                uint32_t pk[BN / 2];
+#pragma unroll
+                for (int c = 0; c < BN; c += 2) {
+                    const float p0 = ex2(x[c] - m_ref), p1 = ex2(x[c + 1] - m_ref);
+                    rs += p0 + p1;
+                    pk[c >> 1] = pack_bf16x2(p0, p1);
+                }
+                l += rs;
+                // PV(j-1) must be done: it read the other P buffer's predecessor, and
+                // waiting for it keeps p_ready from running two phases ahead of the
+                // MMA issuer (mbarrier parity only tells adjacent phases apart)
+                if (j >= 1) {
+                    ok = __all_sync(0xffffffffu, wait_ab(&sh.pv_done[hh], (j - 1) & 1, sh, p.status));
+                    if (!ok) break;
+                }
+                uint8_t* prow = sP + (hh * 2 + (j & 1)) * C::P_BYTES + r * 128;
+#pragma unroll
+                for (int c8 = 0; c8 < BN / 8; ++c8)
+                    *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) =
+                        make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+                if (hh == 0 && j == n_kv - 1 && (j + 1) * BN > seq_len) {
+                    // keys past the sequence end: their V rows may hold anything (0 * NaN = NaN)
+                    const int iv = 2 * j + 1;
+                    ok = __all_sync(0xffffffffu, wait_ab(&sh.kv_full[iv % NSTAGE], (iv / NSTAGE) & 1, sh, p.status));
+                    if (!ok) break;
+                    if (r < BN && j * BN + r >= seq_len) {
+                        uint8_t* vrow = sKV + (iv % NSTAGE) * C::KV_BYTES + r * 128;
+#pragma unroll
+                        for (int kb = 0; kb < C::KB; ++kb)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                *reinterpret_cast<uint4*>(vrow + kb * C::KV_KB + c * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc::fence_before_sync();
+                mbar_arrive(&sh.p_ready[hh]);
+            }
+            // ---- epilogue: O / l -> bf16
+            if (ok) ok = __all_sync(0xffffffffu, wait_ab(&sh.pv_done[hh], (n_kv - 1) & 1, sh, p.status));
+            if (ok) {
+                tc::fence_after_sync();
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const bool store = r < rows_valid;
+                const int h = h0 + hh;
+                __nv_bfloat16* orow = p.out + ((size_t)(row0 + r) * p.Hq + h) * D;
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tc::ld_32x32b_x32(t_o + c0, o);
+                    tc::wait_ld();
+                    if (store) {
+                        uint32_t pkd[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pkd[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+                        uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+                    }
+                }
+                if (store && p.lse != nullptr)
+                    p.lse[(size_t)(row0 + r) * p.Hq + h] = l > 0.f ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == WARP_TMA) tc::tmem_dealloc(tmem, C::TM_COLS);
+}
+
+}  // namespace pf
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" size_t pa_prefill_workspace_bytes(int batch, int total_q, int num_q_heads, int num_kv_heads,
+                                             int head_dim) {
+    (void)total_q;
+    return pa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim);
+}
+
+extern "C" int attn_prefill_varlen_causal(void* out, float* lse, const void* q, const void* k_pool,
+                                          const void* v_pool, int num_pages, const int32_t* block_table,
+                                          int max_pages_per_seq, const int32_t* cu_seqlens_q,
+                                          const int32_t* seq_lens, int batch, int total_q, int max_q_len,
+                                          int max_seq_len, int page_size, int num_q_heads, int num_kv_heads,
+                                          int head_dim, float softmax_scale, void* workspace,
+                                          size_t workspace_bytes, int32_t* status, void* stream) {
+    if (batch < 0 || total_q < 0 || max_q_len < 0 || max_seq_len < 0) return PA_ERR_SHAPE;
+    int rc = check_common_shapes(page_size, num_q_heads, num_kv_heads, head_dim);
+    if (rc != PA_OK) return rc;
+    if (batch == 0 || total_q == 0) return PA_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_table || !cu_seqlens_q || !seq_lens) return PA_ERR_NULL;
+    if (num_pages < 1 || max_pages_per_seq < 1) return PA_ERR_SHAPE;
+    if ((long long)max_seq_len > (long long)max_pages_per_seq * page_size) return PA_ERR_SHAPE;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(q) || !aligned16(out)) return PA_ERR_SHAPE;
+    const long long pool_rows = (long long)num_pages * num_kv_heads * page_size;
+    if (pool_rows >= (1ll << 31)) return PA_ERR_SHAPE;
+
+    DeviceInfo dev;
+    rc = current_device(&dev);
+    if (rc != PA_OK) return rc;
+
+    const int group = num_q_heads / num_kv_heads;
+    const int NP = (group + 1) / 2;
+    const long long tiles_upper = (long long)(total_q + pf::BM - 1) / pf::BM + batch;
+    const long long grid = tiles_upper * num_kv_heads * NP;
+    if (grid >= (1ll << 31)) return PA_ERR_SHAPE;
+
+    CUtensorMap qmap, kmap, vmap;
+    if (encode_q_map(&qmap, q, total_q, num_q_heads, head_dim) != PA_OK) return PA_ERR_CUDA;
+    if (encode_rows_map(&kmap, k_pool, (uint64_t)pool_rows, head_dim, 64, 16) != PA_OK) return PA_ERR_CUDA;
+    if (encode_rows_map(&vmap, v_pool, (uint64_t)pool_rows, head_dim, 64, 16) != PA_OK) return PA_ERR_CUDA;
+
+    pf::Params prm;
+    prm.out = static_cast<__nv_bfloat16*>(out);
+    prm.lse = lse;
+    prm.block_table = block_table;
+    prm.seq_lens = seq_lens;
+    prm.cu_q = cu_seqlens_q;
+    prm.status = status;
+    prm.num_pages = num_pages;
+    prm.max_pages = max_pages_per_seq;
+    prm.batch = batch;
+    prm.page_size = page_size;
+    prm.Hq = num_q_heads;
+    prm.Hkv = num_kv_heads;
+    prm.group = group;
+    prm.NP = NP;
+    prm.skip_single = 1;  // q_len == 1 entries go to the split-K decode kernel below
+    prm.scale_log2 = softmax_scale * kLog2e;
+
+    // decode rows (q_len == 1) of a mixed step: split-K over their KV
+    rc = dec::launch_decode(out, lse, q, k_pool, v_pool, num_pages, block_table, max_pages_per_seq, seq_lens,
+                            cu_seqlens_q, batch, max_seq_len, page_size, num_q_heads, num_kv_heads, head_dim,
+                            softmax_scale, workspace, workspace_bytes, status, stream);
+    if (rc != PA_OK) return rc;
+    if (max_q_len < 2) return PA_OK;  // no entry needs the prefill kernel
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (head_dim == 128) {
+        constexpr int smem = pf::Cfg<128>::SMEM_BYTES;
+        if (set_smem_limit_once((const void*)pf::prefill_kernel<128>, smem, dev.device, 2) != PA_OK)
+            return PA_ERR_CUDA;
+        pf::prefill_kernel<128><<<(unsigned)grid, pf::NTHREADS, smem, st>>>(qmap, kmap, vmap, prm);
+    } else {
+        constexpr int smem = pf::Cfg<64>::SMEM_BYTES;
+        if (set_smem_limit_once((const void*)pf::prefill_kernel<64>, smem, dev.device, 3) != PA_OK)
+            return PA_ERR_CUDA;
+        pf::prefill_kernel<64><<<(unsigned)grid, pf::NTHREADS, smem, st>>>(qmap, kmap, vmap, prm);
+    }
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}

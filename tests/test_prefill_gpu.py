@@ -1,0 +1,162 @@
+"""attn_prefill_varlen_causal (and writeback + prefill) on the GPU against the
+fp64 oracle, including mixed prefill + decode entries and the bit-exact
+invariants."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.conftest import assert_attention_close, bits, compact_for_oracle, np_i32, oracle_args
+
+pytestmark = pytest.mark.gpu
+
+
+def _pa():
+    return pytest.importorskip("paged_kv_decode_17_gb300")
+
+
+def _prefill(g, dev, **kw):
+    pa = _pa()
+    status = pa.new_status(dev)
+    out, lse = pa.attn_prefill_varlen_causal(g.q, g.k_pool, g.v_pool, g.block_table, g.cu_seqlens_q, g.seq_lens,
+                                             g.softmax_scale, max_q_len=max(1, g.max_q_len),
+                                             max_seq_len=max(1, g.max_seq_len), return_lse=True, status=status, **kw)
+    pa.check_status(status, "attn_prefill_varlen_causal")
+    return out, lse
+
+
+def _check(case, dev):
+    ref_out, ref_lse = oracle.paged_attention(**oracle_args(case))
+    out, lse = _prefill(case.to(dev), dev)
+    return assert_attention_close(out, ref_out, lse, ref_lse, what=case.name)
+
+
+CASES = [
+    # name, seq_lens, q_lens, Hq, Hkv, D, page_size
+    ("single_37", [37], [37], 2, 1, 128, 16),
+    ("tile_exact", [128, 64], [128, 64], 4, 2, 128, 16),
+    ("tile_plus1", [129, 65, 200], [129, 65, 200], 8, 2, 128, 16),
+    ("ragged_many", [300, 17, 513, 2], [300, 17, 513, 2], 28, 4, 128, 16),
+    ("prior_chunk", [1000, 700], [200, 129], 8, 2, 128, 16),
+    ("prior_small_q", [333, 90], [5, 3], 8, 4, 128, 16),
+    ("odd_group", [150, 260], [150, 100], 6, 2, 128, 16),
+    ("mha", [190], [190], 4, 4, 128, 16),
+    ("d64", [400, 129], [400, 60], 8, 2, 64, 16),
+    ("page32", [500, 77], [300, 77], 8, 2, 128, 32),
+    ("page64", [260, 1000], [260, 500], 4, 1, 128, 64),
+    ("mixed_decode_rows", [900, 1, 77, 3000, 256], [256, 1, 1, 1, 256], 32, 8, 128, 16),
+]
+
+
+@pytest.mark.parametrize("name,seq_lens,q_lens,hq,hkv,d,ps", CASES, ids=[c[0] for c in CASES])
+def test_prefill_matches_oracle(cuda_device, name, seq_lens, q_lens, hq, hkv, d, ps):
+    case = workloads.make_paged_case(name, seq_lens, q_lens, hq, hkv, d, page_size=ps, seed=len(name) * 7 + d)
+    _check(case, cuda_device)
+
+
+def test_prefill_sharp_logits(cuda_device):
+    case = workloads.make_paged_case("sharp", [700, 300], [700, 150], 8, 2, 128, k_scale=8.0, seed=60)
+    _check(case, cuda_device)
+
+
+def test_writeback_then_prefill(cuda_device):
+    """The serving order: write the new rows into their pages, then attend."""
+    pa = _pa()
+    case = workloads.make_paged_case("wb_prefill", [600, 333, 90], [200, 333, 90], 8, 2, 128, prewritten=False,
+                                     seed=61)
+    kp, vp = oracle.kv_write_paged(bits(case.k_pool), bits(case.v_pool), bits(case.k_new), bits(case.v_new),
+                                   np_i32(case.cu_seqlens_q), case.seq_lens_host, np_i32(case.block_table),
+                                   case.page_size)
+    args = oracle_args(case)
+    args["k_pool_bits"], args["v_pool_bits"] = kp, vp
+    ref_out, ref_lse = oracle.paged_attention(**args)
+    g = case.to(cuda_device)
+    pa.kv_write_paged(g.k_pool, g.v_pool, g.k_new, g.v_new, g.cu_seqlens_q, g.seq_lens, g.block_table)
+    out, lse = _prefill(g, cuda_device)
+    assert_attention_close(out, ref_out, lse, ref_lse, what="writeback+prefill")
+
+
+def test_decode_rows_equal_decode_entry_point(cuda_device):
+    """q_len = 1 entries of the prefill call give the same rows as attn_decode_paged."""
+    pa = _pa()
+    case = workloads.make_paged_case("dec_eq", [5000, 1, 333, 70], [1, 1, 1, 1], 16, 2, 128, seed=62).to(cuda_device)
+    out_p, lse_p = _prefill(case, cuda_device)
+    out_d, lse_d = pa.attn_decode_paged(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
+                                        case.softmax_scale, return_lse=True)
+    d = (out_p.float() - out_d.float()).abs()
+    assert bool((d <= 2e-2 + 2e-2 * out_d.float().abs()).all())
+    assert float((lse_p - lse_d).abs().max()) < 1e-3
+
+
+def test_causal_future_keys_do_not_matter(cuda_device):
+    """Rows at positions < t are bit-identical when K/V at positions >= t change."""
+    case = workloads.make_paged_case("causal", [400], [400], 4, 2, 128, seed=63)
+    out1, _ = _prefill(case.to(cuda_device), cuda_device)
+    t = 250
+    k, v = case.k_pool.clone(), case.v_pool.clone()
+    for pos in range(t, 400):
+        phys = int(case.block_table[0, pos // 16])
+        k[phys, :, pos % 16] = 3.0
+        v[phys, :, pos % 16] = -5.0
+    case.k_pool, case.v_pool = k, v
+    out2, _ = _prefill(case.to(cuda_device), cuda_device)
+    assert torch.equal(out1[:t].view(torch.int16), out2[:t].view(torch.int16))
+    assert not torch.equal(out1[t:].view(torch.int16), out2[t:].view(torch.int16))
+
+
+def test_prefill_page_permutation_and_determinism(cuda_device):
+    case = workloads.make_paged_case("perm", [520, 130], [520, 60], 8, 2, 128, num_pages=60, seed=64)
+    g = case.to(cuda_device)
+    o1, l1 = _prefill(g, cuda_device)
+    o1b, l1b = _prefill(g, cuda_device)
+    assert torch.equal(o1.view(torch.int16), o1b.view(torch.int16)) and torch.equal(l1, l1b)
+    P = case.num_pages
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(3))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(P)
+    c2 = workloads.PagedCase(**{**case.__dict__})
+    c2.k_pool = case.k_pool[perm].contiguous()
+    c2.v_pool = case.v_pool[perm].contiguous()
+    bt = case.block_table.clone()
+    m = bt >= 0
+    bt[m] = inv[bt[m].long()].to(torch.int32)
+    c2.block_table = bt
+    o2, l2 = _prefill(c2.to(cuda_device), cuda_device)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+
+
+def test_prefill_bad_page_reports_status(cuda_device):
+    pa = _pa()
+    case = workloads.make_paged_case("bad", [300], [300], 4, 2, 128, seed=65).to(cuda_device)
+    case.block_table[0, 3] = 10 ** 6
+    status = pa.new_status(cuda_device)
+    pa.attn_prefill_varlen_causal(case.q, case.k_pool, case.v_pool, case.block_table, case.cu_seqlens_q,
+                                  case.seq_lens, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -6
+
+
+@pytest.mark.slow
+def test_varlen_prefill_full_size_sampled(cuda_device):
+    """16 sequences of 512..4096 tokens, Hq=28, Hkv=4: writeback then prefill;
+    the shortest and the longest sequence checked against the oracle on 3 heads."""
+    pa = _pa()
+    case = workloads.varlen_prefill(device=cuda_device)
+    lens = case.seq_lens_host
+    seqs = [int(np.argmin(lens)), int(np.argmax(lens))]
+    # oracle inputs: the generator's pre-write pages of those sequences, written by the oracle's scatter
+    args, rows = compact_for_oracle(case, seqs)
+    ri = torch.tensor(rows, device=cuda_device)
+    args["k_pool_bits"], args["v_pool_bits"] = oracle.kv_write_paged(
+        args["k_pool_bits"], args["v_pool_bits"], bits(case.k_new[ri]), bits(case.v_new[ri]),
+        args["cu_seqlens_q"], args["seq_lens"], args["block_table"], case.page_size)
+    pa.kv_write_paged(case.k_pool, case.v_pool, case.k_new, case.v_new, case.cu_seqlens_q, case.seq_lens,
+                      case.block_table)
+    out, lse = _prefill(case, cuda_device)
+    assert torch.isfinite(out.float()).all()
+    heads = [0, 13, 27]
+    ref_out, ref_lse = oracle.paged_attention(**args, heads=heads)
+    assert_attention_close(out[rows][:, heads], ref_out[:, heads], lse[rows][:, heads], ref_lse[:, heads],
+                           what="varlen_prefill sampled")
