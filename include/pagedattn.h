@@ -136,6 +136,7 @@ size_t pa_prefill_workspace_bytes(int batch, int total_q, int num_q_heads, int n
  *   q          bf16 [total_q][num_q_heads][head_dim]
  *   cu_seqlens_q  int32 [batch+1], cu_seqlens_q[0] = 0, non-decreasing
  *   max_q_len, max_seq_len  host upper bounds (size the launch only)
+ *   softmax_scale  must be finite and > 0 (PA_ERR_SHAPE otherwise)
  */
 int attn_prefill_varlen_causal(void* out, float* lse, const void* q, const void* k_pool,
                                const void* v_pool, int num_pages, const int32_t* block_table,

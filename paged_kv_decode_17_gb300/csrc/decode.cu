@@ -18,10 +18,13 @@
 //   same way.  The ranges are derived on the device from seq_lens (no host
 //   synchronisation; the call can be captured in a CUDA graph).
 // * Inside a CTA each warp takes every W-th unit of the CTA's part of a
-//   segment and runs its own TMA pipeline: DEPTH stages, each a 16-row K box
-//   and V box loaded by cp.async.bulk.tensor with 128-byte swizzle, so the
-//   ldmatrix reads below are bank-conflict free.  There is no cross-warp
-//   producer/consumer handshake in the loop.
+//   segment and runs its own copy pipeline: DEPTH stages, each unit's K and V
+//   staged by 16-byte cp.async copies (coalesced 512-byte warp requests) into a
+//   128-byte-swizzled layout, so the ldmatrix reads below are bank-conflict
+//   free.  (Per-thread copies, not TMA: with one 16-row page block per request,
+//   the TMA engine's per-request cost capped the read rate near 18 bytes per
+//   cycle per SM.)  There is no cross-warp producer/consumer handshake in the
+//   loop.
 // * Q.K^T and P.V run on bf16 mma.sync (m16n8k16) with the GQA head block as
 //   the M dimension (up to 16 query heads share one KV head's K/V tiles);
 //   scores, running max/sum and O stay in fp32 registers.
@@ -62,6 +65,8 @@ struct Params {
     __nv_bfloat16* out;
     float* lse;
     const __nv_bfloat16* q;
+    const __nv_bfloat16* k_pool;
+    const __nv_bfloat16* v_pool;
     const int32_t* block_table;
     const int32_t* seq_lens;
     const int32_t* cu_q;  // non-null in a mixed call: only entries with one query row are decoded here
@@ -140,39 +145,57 @@ struct UnitIter {
     }
 };
 
+// Stage one unit (16 keys of K and of V) with 16-byte cp.async copies, written
+// in the 128-byte-swizzled layout the ldmatrix reads expect: 16-byte chunk c of
+// row r of a 64-column box sits at r * 128 + ((c ^ (r & 7)) * 16).  Lanes
+// 0-15 / 16-31 copy two consecutive 256-byte rows per instruction (coalesced).
+// Rows past the sequence end are not copied; their V rows are zeroed (their
+// slots may hold anything and 0 * NaN = NaN), their K rows are masked later.
+// Every call commits exactly one cp.async group (possibly empty).
 template <int D>
-__device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, uint8_t* stage, uint64_t* bar,
-                                           int* phys_slot, const CUtensorMap* kmap, const CUtensorMap* vmap,
+__device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, uint8_t* stage, int* phys_slot,
                                            int lane, uint64_t policy) {
     using C = Cfg<D>;
+    constexpr int CH = D / 8;  // 16-byte chunks per row
     const int j = it.u - it.seg.start;  // unit index within the sequence
     const int tok0 = j * UNIT;
     const int page = tok0 >> p.ps_shift;
     const int sub = (tok0 - (page << p.ps_shift)) / UNIT;
-    if (lane == 0) {
-        const int phys = __ldg(p.block_table + (size_t)it.seg.b * p.max_pages + page);
-        if (phys < 0 || phys >= p.num_pages) {
+    const int phys = __ldg(p.block_table + (size_t)it.seg.b * p.max_pages + page);
+    if (phys < 0 || phys >= p.num_pages) {
+        if (lane == 0) {
             report(p.status, PA_ERR_BAD_PAGE);
             *phys_slot = -1;
-            mbar_arrive(bar);
-        } else {
-            *phys_slot = phys;
-            const int row = (phys * p.Hkv + it.seg.g) * p.page_size + sub * UNIT;
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+        }
+    } else {
+        if (lane == 0) *phys_slot = phys;
+        const size_t row = (size_t)(phys * p.Hkv + it.seg.g) * p.page_size + sub * UNIT;
+        const int valid = min(UNIT, it.seg.len - tok0);
+        const char* ksrc = reinterpret_cast<const char*>(p.k_pool + row * D);
+        const char* vsrc = reinterpret_cast<const char*>(p.v_pool + row * D);
+        const uint32_t sbase = smem_u32(stage);
 #pragma unroll
-            for (int bx = 0; bx < C::BOXES; ++bx) {
-                tma_load_2d_hint(stage + bx * C::BOX_BYTES, kmap, bar, bx * 64, row, policy);
-                tma_load_2d_hint(stage + C::UNIT_BYTES + bx * C::BOX_BYTES, vmap, bar, bx * 64, row, policy);
+        for (int i = 0; i < CH; ++i) {
+            const int q = i * 32 + lane;
+            const int t = q / (UNIT * CH);  // 0 = K, 1 = V
+            const int qq = q - t * UNIT * CH;
+            const int r = qq / CH;
+            const int cc = qq - r * CH;
+            const uint32_t dst = sbase + t * C::UNIT_BYTES + (cc >> 3) * C::BOX_BYTES + r * 128 +
+                                 (((cc & 7) ^ (r & 7)) << 4);
+            if (r < valid) {
+                cp_async_16(dst, (t ? vsrc : ksrc) + r * D * 2 + cc * 16, policy);
+            } else if (t == 1) {
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
             }
         }
     }
+    cp_async_commit();
 }
 
 template <int D>
 __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
-    decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                  const Params p) {
+    decode_kernel(const Params p) {
     using C = Cfg<D>;
     constexpr int DEPTH = C::DEPTH;
     constexpr int KSTEPS = D / 16;
@@ -182,7 +205,6 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
     float* merge_o = reinterpret_cast<float*>(smem + C::STAGES_BYTES);
-    __shared__ __align__(8) uint64_t bars[W][DEPTH];
     __shared__ int s_phys[W][DEPTH];
     __shared__ float s_m[W][MAXR], s_l[W][MAXR], s_M[MAXR], s_L[MAXR];
     __shared__ int s_plan[8];
@@ -242,14 +264,6 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
             s_plan[5] = sP;
         }
     }
-    if (lane == 0) {
-        for (int i = 0; i < DEPTH; ++i) mbar_init(&bars[warp][i], 1);
-        fence_mbar_init();
-    }
-    if (tid == 0) {
-        prefetch_tensormap(&kmap);
-        prefetch_tensormap(&vmap);
-    }
     __syncthreads();
     const int chunk = s_plan[1];
     const int U0 = s_plan[2], U1 = s_plan[3];
@@ -282,15 +296,17 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
     it.u = U0 + warp;
     it.done = false;
     it.norm(p, warp);
-    uint32_t issued = 0, consumed = 0;
-    for (int i = 0; i < DEPTH && !it.done; ++i) {
-        issue_unit<D>(p, it, my_stages + i * C::STAGE_BYTES, &bars[warp][i], &s_phys[warp][i], &kmap, &vmap, lane,
-                      policy);
-        ++issued;
-        it.u += W;
-        it.norm(p, warp);
+    uint32_t consumed = 0;
+    // prologue: one cp.async group per stage (empty groups once the warp runs out of units)
+    for (int i = 0; i < DEPTH; ++i) {
+        if (!it.done) {
+            issue_unit<D>(p, it, my_stages + i * C::STAGE_BYTES, &s_phys[warp][i], lane, policy);
+            it.u += W;
+            it.norm(p, warp);
+        } else {
+            cp_async_commit();
+        }
     }
-    __syncwarp();
 
     // per-lane ldmatrix geometry (see the fragment layouts of mma.m16n8k16)
     const int mi = lane >> 3, ri = lane & 7;
@@ -301,8 +317,6 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
     const int qr = lane >> 2;       // row group of this lane in mma fragments
     const int qc = (lane & 3) * 2;  // column pair of this lane
 
-    bool aborted = false;
-    uint32_t waited = 0;  // units whose copy is known to have landed
     Seg cs = seg0;
     int pa_ = U0;
     while (true) {
@@ -333,32 +347,13 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
 
         for (int u = pa_ + warp; u < pe; u += W) {
             const int st = consumed % DEPTH;
-            const uint32_t par = (consumed / DEPTH) & 1u;
-            if (!aborted) {
-                if (mbar_wait(&bars[warp][st], par)) {
-                    waited = consumed + 1;
-                } else {
-                    aborted = true;
-                    if (lane == 0) report(p.status, PA_ERR_TIMEOUT);
-                }
-            }
+            cp_async_wait_group<DEPTH - 1>();  // this unit's group (DEPTH - 1 younger ones may fly)
+            __syncwarp();
             const int phys = s_phys[warp][st];
             uint8_t* sk = my_stages + st * C::STAGE_BYTES;
             uint8_t* sv = sk + C::UNIT_BYTES;
-            if (!aborted && phys >= 0) {
+            if (phys >= 0) {
                 const int valid = min(UNIT, cs.len - (u - cs.start) * UNIT);
-                if (valid < UNIT) {
-                    // zero V rows past the end of the sequence (their slots may hold anything)
-                    const int nvec = (UNIT - valid) * (D / 8);
-                    for (int i = lane; i < nvec; i += 32) {
-                        const int r = valid + i / (D / 8);
-                        const int c = i % (D / 8);
-                        *reinterpret_cast<uint4*>(sv + (c >> 3) * C::BOX_BYTES + r * 128 + (c & 7) * 16) =
-                            make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();  // before a later TMA overwrites this stage
-                    __syncwarp();
-                }
                 const uint32_t kb = smem_u32(sk), vb = smem_u32(sv);
                 // S = Q K^T  (16 heads x 16 keys)
                 // two independent accumulator chains (even / odd k-steps) halve the
@@ -440,16 +435,14 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
                     mma_16816(o[2 * jj + 1], pa, b2, b3);
                 }
             }
-            __syncwarp();
+            __syncwarp();  // every lane is done reading this stage
             ++consumed;
-            if (!it.done && !aborted) {
-                const int sti = issued % DEPTH;
-                issue_unit<D>(p, it, my_stages + sti * C::STAGE_BYTES, &bars[warp][sti], &s_phys[warp][sti], &kmap,
-                              &vmap, lane, policy);
-                ++issued;
+            if (!it.done) {
+                issue_unit<D>(p, it, my_stages + st * C::STAGE_BYTES, &s_phys[warp][st], lane, policy);
                 it.u += W;
                 it.norm(p, warp);
-                __syncwarp();
+            } else {
+                cp_async_commit();
             }
         }
 
@@ -585,13 +578,7 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
         seg_next(cs, p);
     }
 
-    // drain: never leave the CTA with a bulk copy still writing its shared memory
-    for (uint32_t i = waited; i < issued; ++i) {
-        if (!mbar_wait(&bars[warp][i % DEPTH], (i / DEPTH) & 1u)) {
-            if (lane == 0) report(p.status, PA_ERR_TIMEOUT);
-            break;
-        }
-    }
+    cp_async_wait_group<0>();  // never exit with a copy still landing in shared memory
 }
 
 // Workspace layout: [counters: S int32][ws_lse: slots x MAXR f32][ws_o: slots x MAXR x D f32]
@@ -672,14 +659,13 @@ int launch_decode(void* out, float* lse, const void* q, const void* k_pool, cons
     if (workspace_bytes < wl.total) return PA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_WORKSPACE;
 
-    CUtensorMap kmap, vmap;
-    if (encode_rows_map(&kmap, k_pool, (uint64_t)pool_rows, head_dim, 64, dec::UNIT) != PA_OK) return PA_ERR_CUDA;
-    if (encode_rows_map(&vmap, v_pool, (uint64_t)pool_rows, head_dim, 64, dec::UNIT) != PA_OK) return PA_ERR_CUDA;
 
     dec::Params prm;
     prm.out = static_cast<__nv_bfloat16*>(out);
     prm.lse = lse;
     prm.q = static_cast<const __nv_bfloat16*>(q);
+    prm.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
+    prm.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
     prm.block_table = block_table;
     prm.seq_lens = seq_lens;
     prm.cu_q = cu_q;
@@ -705,12 +691,12 @@ int launch_decode(void* out, float* lse, const void* q, const void* k_pool, cons
         constexpr int smem = dec::Cfg<128>::SMEM_BYTES;
         if (set_smem_limit_once((const void*)dec::decode_kernel<128>, smem, dev.device, 0) != PA_OK)
             return PA_ERR_CUDA;
-        dec::decode_kernel<128><<<grid, dec::W * 32, smem, st>>>(kmap, vmap, prm);
+        dec::decode_kernel<128><<<grid, dec::W * 32, smem, st>>>(prm);
     } else {
         constexpr int smem = dec::Cfg<64>::SMEM_BYTES;
         if (set_smem_limit_once((const void*)dec::decode_kernel<64>, smem, dev.device, 1) != PA_OK)
             return PA_ERR_CUDA;
-        dec::decode_kernel<64><<<grid, dec::W * 32, smem, st>>>(kmap, vmap, prm);
+        dec::decode_kernel<64><<<grid, dec::W * 32, smem, st>>>(prm);
     }
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -11,21 +11,23 @@
 //
 // GB300 design (one CTA = one 128-row query tile of one sequence, for two
 // query heads that share a KV head, so each K/V tile is loaded once for both):
-// * warp 8 (TMA): loads the two Q tiles once, then K and V tiles through a
-//   5-stage ring; a 64-key tile is four 16-row page blocks gathered through
-//   the block table, each a 128-byte-swizzled TMA box.
-// * warp 9 (MMA): one thread issues tcgen05.mma: S_h = Q_h K^T into TMEM
-//   (fp32, 64 columns per head) and O_h += P_h V into TMEM (fp32, D columns
-//   per head).  The issue order S(j+1), PV(j) lets the tensor core compute the
-//   next scores while the softmax of the current tile runs.
-// * warps 0-3 / 4-7: softmax for head 0 / head 1, one thread per query row
-//   (its TMEM lane).  They read S with tcgen05.ld, mask, update the running
-//   max/sum, write P (bf16) to shared memory in the MMA operand layout, and at
-//   the end normalise O and store it.  O lives in TMEM; it is rescaled only
-//   when a row's maximum grows by more than TAU = 8 (log2 units): until then
-//   the exponentials are taken against the older, smaller maximum, which
-//   keeps them <= 2^8 and the result exact, because the final division uses
-//   the same reference maximum for numerator and denominator.
+// * warp 16 (producer): loads the two Q tiles once by TMA, then gathers K and
+//   V tiles through a 7-stage ring: a 64-key tile is four 16-row page blocks
+//   found through the block table (one tile ahead), copied with coalesced
+//   16-byte cp.async into the 128-byte-swizzled operand layout.
+// * warps 17 / 18 (MMA, one per head): one thread issues tcgen05.mma:
+//   S_h = Q_h K^T into TMEM (fp32, 64 columns) and O_h += P_h V into TMEM
+//   (fp32, D columns).  The issue order S(j+1), PV(j) lets the tensor core
+//   compute the next scores while the softmax of the current tile runs.
+// * warps 0-15 (softmax): per head two warpgroups, each owning half of the
+//   64 score columns of every row (thread = TMEM lane = row); the two halves
+//   exchange their row maxima through shared memory at a named barrier.  They
+//   write P (bf16) to shared memory in the MMA operand layout and at the end
+//   normalise O and store it.  O is rescaled only when a row's maximum grows by
+//   more than TAU = 8 (log2 units): until then the exponentials are taken
+//   against the older, smaller maximum, which keeps them <= 2^8 and the result
+//   exact, because the final division uses the same reference maximum for
+//   numerator and denominator.
 // Every wait is bounded; a timeout sets a CTA-wide abort flag, records
 // PA_ERR_TIMEOUT and all roles fall through to a clean exit.
 #include "pa_common.cuh"
@@ -36,10 +38,26 @@ namespace pf {
 
 constexpr int BM = 128;      // query rows per tile (= TMEM lanes)
 constexpr int BN = 64;       // keys per KV tile
-constexpr int NSTAGE = 5;    // K/V ring depth (K and V tiles alternate)
+#ifndef PA_PF_NSTAGE
+#define PA_PF_NSTAGE 5
+#endif
+#ifndef PA_PF_NPB
+#define PA_PF_NPB 2
+#endif
+#ifndef PA_PF_MAX_CLUSTER
+#define PA_PF_MAX_CLUSTER 4
+#endif
+constexpr int NSTAGE = PA_PF_NSTAGE;  // K/V ring depth (K and V tiles alternate)
+constexpr int NPB = PA_PF_NPB;        // P buffers per head (tile j uses buffer j % NPB)
+// CTAs of one (sequence, query tile, KV head) -- its head pairs -- form a cluster
+// of up to this many; each K/V tile is fetched once per cluster (TMA multicast)
+constexpr int MAX_CLUSTER = PA_PF_MAX_CLUSTER;
 constexpr float TAU = 8.f;   // rescale threshold, log2 units
-constexpr int NTHREADS = 320;
-constexpr int WARP_TMA = 8, WARP_MMA = 9;
+// warps 0-15: softmax (head = warp / 8, column half = (warp / 4) & 1, row quarter = warp & 3)
+// warp 16: TMA producer; warps 17 and 18: MMA issuers of head 0 and head 1
+constexpr int NTHREADS = 608;
+constexpr int WARP_TMA = 16, WARP_MMA0 = 17;
+constexpr int HALF = BN / 2;  // score columns per softmax thread
 
 template <int D>
 struct Cfg {
@@ -51,7 +69,7 @@ struct Cfg {
     static constexpr int KV_KB = BN * 128;          // bytes per column block of a K/V tile
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_P = 2 * Q_BYTES;       // P[head][buffer]
-    static constexpr int OFF_KV = OFF_P + 4 * P_BYTES;
+    static constexpr int OFF_KV = OFF_P + 2 * NPB * P_BYTES;
     static constexpr int SMEM_BYTES = 1024 + OFF_KV + NSTAGE * KV_BYTES;
     static constexpr int TM_S0 = 0;
     static constexpr int TM_O0 = 2 * BN;
@@ -66,9 +84,12 @@ struct Params {
     const int32_t* block_table;
     const int32_t* seq_lens;
     const int32_t* cu_q;
+    const __nv_bfloat16* k_pool;
+    const __nv_bfloat16* v_pool;
     int32_t* status;
     int num_pages, max_pages, batch, page_size;
-    int Hq, Hkv, group, NP;
+    int Hq, Hkv, group, NP;  // NP = head pairs per KV head, padded to a multiple of CS
+    int CS;                  // cluster size (CTAs sharing each K/V tile)
     int skip_single;  // sequences with q_len == 1 are served by the decode kernel
     float scale_log2;
 };
@@ -77,10 +98,14 @@ struct Shared {
     uint64_t bar_q;
     uint64_t kv_full[NSTAGE];
     uint64_t kv_empty[NSTAGE];
-    uint64_t s_full[2], s_free[2], p_ready[2], pv_done[2];
+    uint64_t s_full[2], s_free[2];
+    uint64_t p_ready[2][NPB], pv_done[2][NPB];  // [head][P buffer]
+    uint64_t v_tail;  // TMA copies of a V tile that runs past the sequence end land here first
+    float xmax[2][2][2][BM];  // [head][tile parity][column half][row]: partial row maxima
+    float xsum[2][2][BM];     // [head][column half][row]: partial row sums at the end
     uint32_t tmem_base;
     int abort_flag;
-    int item[8];
+    int item[9];
 };
 
 __device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, Shared& sh, int32_t* status) {
@@ -104,6 +129,34 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                               uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
+        : "memory");
+}
+
+// Arrive on `bar` at the same offset in every CTA of `mask` once this thread's MMAs are done.
+__device__ __forceinline__ void commit_mc(uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
 }
 
 // number of 128-row tiles of sequence b served by this kernel (0 if none)
@@ -164,28 +217,39 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 sh.item[3] = sl;
                 sh.item[4] = __ldg(p.cu_q + found_b) + t * BM;    // first q row of the tile
                 sh.item[5] = g;
-                sh.item[6] = g * p.group + 2 * pair;               // first query head
-                sh.item[7] = min(2, p.group - 2 * pair);           // heads in this CTA
+                sh.item[6] = g * p.group + 2 * pair;                       // first query head
+                sh.item[7] = max(0, min(2, p.group - 2 * pair));           // heads in this CTA (0: loads only)
+                const int pair0 = pair - pair % p.CS;                       // first pair of the cluster
+                sh.item[8] = max(0, min(2 * p.CS, p.group - 2 * pair0));   // heads in the cluster
             }
             sh.abort_flag = 0;
         }
     }
+    __syncthreads();
     if (tid == 0) {
         mbar_init(&sh.bar_q, 1);
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(&sh.kv_full[s], 1);
-            mbar_init(&sh.kv_empty[s], 1);
+            // released once by every head of the cluster (each MMA thread commits to all CTAs)
+            mbar_init(&sh.kv_empty[s], sh.item[0] >= 0 ? max(1, sh.item[8]) : 1);
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(&sh.s_full[h], 1);
-            mbar_init(&sh.s_free[h], 4 * 32);
-            mbar_init(&sh.p_ready[h], 4 * 32);
-            mbar_init(&sh.pv_done[h], 1);
+            mbar_init(&sh.s_free[h], 8 * 32);
+            mbar_init(&sh.v_tail, 1);
+            for (int bf = 0; bf < NPB; ++bf) {
+                mbar_init(&sh.p_ready[h][bf], 8 * 32);
+                mbar_init(&sh.pv_done[h][bf], 1);
+            }
         }
         fence_mbar_init();
     }
     __syncthreads();
-    if (sh.item[0] < 0) return;  // uniform: no tile for this CTA
+    if (sh.item[0] < 0) return;  // uniform over the cluster: no tile for it
+    const int CS = p.CS;
+    const uint16_t cmask = (uint16_t)((1u << CS) - 1);
+    const int crank = CS > 1 ? (int)cluster_rank() : 0;
+    if (CS > 1) cluster_sync();  // every CTA's barriers exist before anyone multicasts into them
 
     const int b = sh.item[0];
     const int t = sh.item[1];
@@ -215,234 +279,294 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint8_t* sKV = smem + C::OFF_KV;
 
     if (warp == WARP_TMA) {
-        // ===================================================== producer
+        // ===================================================== producer (whole warp)
         if (lane == 0) {
             prefetch_tensormap(&qmap);
             prefetch_tensormap(&kmap);
             prefetch_tensormap(&vmap);
-            mbar_arrive_expect_tx(&sh.bar_q, nheads * C::Q_BYTES);
-            for (int hh = 0; hh < nheads; ++hh)
-                for (int kb = 0; kb < C::KB; ++kb)
-                    tma_load_3d(sQ + hh * C::Q_BYTES + kb * C::Q_KB, &qmap, &sh.bar_q, kb * 64, h0 + hh, row0);
-            const int32_t* bt = p.block_table + (size_t)b * p.max_pages;
-            int issued = 0;
-            for (int j = 0; j < n_kv; ++j) {
-                // the four 16-key blocks of this tile: physical rows in the pool
-                int rowsel[4];
-                int good = 0;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int key0 = j * BN + u * 16;
-                    rowsel[u] = -1;
-                    if (key0 < seq_len) {
-                        const int page = key0 / p.page_size;
-                        const int phys = __ldg(bt + page);
-                        if (phys < 0 || phys >= p.num_pages) {
-                            report(p.status, PA_ERR_BAD_PAGE);
-                        } else {
-                            rowsel[u] = (phys * p.Hkv + g) * p.page_size + (key0 - page * p.page_size);
-                            ++good;
-                        }
-                    }
-                }
-                for (int x = 0; x < 2; ++x) {
-                    const int i = 2 * j + x;
-                    const int s = i % NSTAGE;
-                    if (!wait_ab(&sh.kv_empty[s], ((i / NSTAGE) & 1) ^ 1, sh, p.status)) break;
-                    uint8_t* dst = sKV + s * C::KV_BYTES;
-                    if (good == 0) {
-                        mbar_arrive(&sh.kv_full[s]);
-                    } else {
-                        mbar_arrive_expect_tx(&sh.kv_full[s], good * 16 * D * 2);
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            if (rowsel[u] < 0) continue;
-#pragma unroll
-                            for (int kb = 0; kb < C::KB; ++kb)
-                                tma_load_2d(dst + kb * C::KV_KB + u * 2048, x == 0 ? &kmap : &vmap,
-                                            &sh.kv_full[s], kb * 64, rowsel[u]);
-                        }
-                    }
-                    ++issued;
-                }
-                if (*reinterpret_cast<volatile int*>(&sh.abort_flag)) break;
+            if (nheads > 0) {
+                mbar_arrive_expect_tx(&sh.bar_q, nheads * C::Q_BYTES);
+                for (int hh = 0; hh < nheads; ++hh)
+                    for (int kb = 0; kb < C::KB; ++kb)
+                        tma_load_3d(sQ + hh * C::Q_BYTES + kb * C::Q_KB, &qmap, &sh.bar_q, kb * 64, h0 + hh, row0);
             }
-            // never exit with a copy still landing in shared memory
-            mbar_wait(&sh.bar_q, 0);
-            for (int i = max(0, issued - NSTAGE); i < issued; ++i) mbar_wait(&sh.kv_full[i % NSTAGE], (i / NSTAGE) & 1);
+        }
+        // A K (or V) tile is 4 x KB boxes: 16-key page blocks x 64-column halves.  Box b
+        // is fetched by the cluster CTA of rank b % CS and multicast to all of them, so
+        // every CTA's barrier receives the whole tile.  Lane u < 4 resolves block u of a
+        // tile through the block table one tile ahead.
+        const int32_t* bt = p.block_table + (size_t)b * p.max_pages;
+        auto block_row = [&](int j) -> int {  // pool row of block `lane` of tile j, -1 if none
+            int row = -1;
+            if (lane < 4 && j < n_kv) {
+                const int key0 = j * BN + lane * 16;
+                if (key0 < seq_len) {
+                    const int page = key0 / p.page_size;
+                    const int phys = __ldg(bt + page);
+                    if (phys < 0 || phys >= p.num_pages)
+                        report(p.status, PA_ERR_BAD_PAGE);
+                    else
+                        row = (phys * p.Hkv + g) * p.page_size + (key0 - page * p.page_size);
+                }
+            }
+            return row;
+        };
+        int next_row = block_row(0);
+        bool ok = true;
+        int issued = 0;
+        for (int j = 0; j < n_kv && ok; ++j) {
+            const int my_row = next_row;
+            next_row = block_row(j + 1);
+            const unsigned goodmask = __ballot_sync(0xffffffffu, my_row >= 0) & 0xFu;
+            const int good = __popc(goodmask);
+            const int box_row = __shfl_sync(0xffffffffu, my_row, (lane / C::KB) & 3);  // block of box `lane`
+            const bool mine = lane < 4 * C::KB && (lane % CS) == crank && box_row >= 0;
+            const bool tail = (j + 1) * BN > seq_len;
+            for (int x = 0; x < 2 && ok; ++x) {
+                const int i = 2 * j + x;
+                const int st = i % NSTAGE;
+                ok = __all_sync(0xffffffffu, wait_ab(&sh.kv_empty[st], ((i / NSTAGE) & 1) ^ 1, sh, p.status));
+                if (!ok) break;
+                uint8_t* dst = sKV + st * C::KV_BYTES;
+                const bool via_tail = (x == 1) && tail;
+                uint64_t* land = via_tail ? &sh.v_tail : &sh.kv_full[st];
+                if (lane == 0) {
+                    if (good == 0)
+                        mbar_arrive(land);
+                    else
+                        mbar_arrive_expect_tx(land, good * 16 * D * 2);  // the whole tile, from all CTAs
+                }
+                __syncwarp();
+                if (mine) {
+                    const int u = lane / C::KB, kb = lane - u * C::KB;
+                    uint8_t* bdst = dst + kb * C::KV_KB + u * 2048;
+                    const CUtensorMap* map = x == 0 ? &kmap : &vmap;
+                    if (CS > 1)
+                        tma_load_2d_mc(bdst, map, land, kb * 64, box_row, cmask);
+                    else
+                        tma_load_2d(bdst, map, land, kb * 64, box_row);
+                }
+                ++issued;
+                if (via_tail) {
+                    // keys past the sequence end: their V rows may hold anything and 0 * NaN = NaN,
+                    // so zero them (in this CTA's copy) before any MMA may read this tile
+                    ok = __all_sync(0xffffffffu, wait_ab(&sh.v_tail, 0, sh, p.status));
+                    if (!ok) break;
+                    const int first = seq_len - j * BN;
+                    const int nchunk = (BN - first) * 8 * C::KB;  // 16-byte chunks to clear
+                    for (int c = lane; c < nchunk; c += 32) {
+                        const int kb = c / ((BN - first) * 8);
+                        const int rem = c - kb * (BN - first) * 8;
+                        const int r = first + rem / 8;
+                        *reinterpret_cast<uint4*>(dst + kb * C::KV_KB + r * 128 + (rem & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh.kv_full[st]);
+                }
+            }
+        }
+        // Before leaving: every copy into this CTA has landed and every head of the
+        // cluster has released the last stages (no remote arrival can still target us).
+        if (lane == 0) {
+            if (nheads > 0) mbar_wait(&sh.bar_q, 0);
+            for (int i = max(0, issued - NSTAGE); i < issued; ++i) {
+                mbar_wait(&sh.kv_full[i % NSTAGE], (i / NSTAGE) & 1);
+                mbar_wait(&sh.kv_empty[i % NSTAGE], (i / NSTAGE) & 1);
+            }
         }
         __syncwarp();
-    } else if (warp == WARP_MMA) {
-        // ===================================================== MMA issuer
-        if (lane == 0) {
-            const uint32_t q_base = smem_u32(sQ);
-            const uint32_t p_base = smem_u32(sP);
+    } else if (warp == WARP_MMA0 || warp == WARP_MMA0 + 1) {
+        // ===================================================== MMA issuer of one head
+        const int hh = warp - WARP_MMA0;
+        if (lane == 0 && hh < nheads) {
+            const uint32_t qaddr = smem_u32(sQ) + hh * C::Q_BYTES;
+            const uint32_t p_base = smem_u32(sP) + hh * NPB * C::P_BYTES;
             const uint32_t kv_base = smem_u32(sKV);
+            const uint32_t t_s = tmem + C::TM_S0 + hh * BN;
+            const uint32_t t_o = tmem + C::TM_O0 + hh * D;
             bool ok = wait_ab(&sh.bar_q, 0, sh, p.status);
             tc::fence_after_sync();
-            auto issue_s = [&](int hh, int j) {
-                const int s = (2 * j) % NSTAGE;
-                const uint32_t kaddr = kv_base + s * C::KV_BYTES;
-                const uint32_t qaddr = q_base + hh * C::Q_BYTES;
+            auto issue_s = [&](int j) {
+                const uint32_t kaddr = kv_base + ((2 * j) % NSTAGE) * C::KV_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t ad = tc::smem_desc_sw128(qaddr + (kk >> 2) * C::Q_KB + (kk & 3) * 32, 16, 1024);
                     const uint64_t bd = tc::smem_desc_sw128(kaddr + (kk >> 2) * C::KV_KB + (kk & 3) * 32, 16, 1024);
-                    tc::mma_ss(tmem + C::TM_S0 + hh * BN, ad, bd, C::IDESC_S, kk > 0);
+                    tc::mma_ss(t_s, ad, bd, C::IDESC_S, kk > 0);
                 }
                 tc::commit(&sh.s_full[hh]);
             };
-            auto issue_pv = [&](int hh, int j) {
-                const int s = (2 * j + 1) % NSTAGE;
-                const uint32_t vaddr = kv_base + s * C::KV_BYTES;
-                const uint32_t paddr = p_base + (hh * 2 + (j & 1)) * C::P_BYTES;
+            auto issue_pv = [&](int j) {
+                const uint32_t vaddr = kv_base + ((2 * j + 1) % NSTAGE) * C::KV_BYTES;
+                const uint32_t paddr = p_base + (j % NPB) * C::P_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     const uint64_t ad = tc::smem_desc_sw128(paddr + kk * 32, 16, 1024);
                     const uint64_t bd = tc::smem_desc_sw128(vaddr + kk * 2048, C::KV_KB, 1024);
-                    tc::mma_ss(tmem + C::TM_O0 + hh * D, ad, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_ss(t_o, ad, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc::commit(&sh.pv_done[hh]);
+                tc::commit(&sh.pv_done[hh][j % NPB]);
+            };
+            // a K/V stage is free once every head of the cluster is done with it
+            auto release = [&](uint64_t* bar) {
+                if (CS > 1)
+                    commit_mc(bar, cmask);
+                else
+                    tc::commit(bar);
             };
             // prologue: scores of key tile 0
             if (ok) ok = wait_ab(&sh.kv_full[0], 0, sh, p.status);
             if (ok) {
                 tc::fence_after_sync();
-                for (int hh = 0; hh < nheads; ++hh) issue_s(hh, 0);
-                tc::commit(&sh.kv_empty[0]);
+                issue_s(0);
+                release(&sh.kv_empty[0]);
             }
             for (int j = 0; j < n_kv && ok; ++j) {
                 const int ik = 2 * (j + 1), iv = 2 * j + 1;
-                const bool more = j + 1 < n_kv;
-                if (more) {
-                    ok = wait_ab(&sh.kv_full[ik % NSTAGE], (ik / NSTAGE) & 1, sh, p.status);
-                    if (!ok) break;
-                }
-                ok = wait_ab(&sh.kv_full[iv % NSTAGE], (iv / NSTAGE) & 1, sh, p.status);
-                if (!ok) break;
-                for (int hh = 0; hh < nheads && ok; ++hh) {
-                    if (more) {
-                        ok = wait_ab(&sh.s_free[hh], j & 1, sh, p.status);
-                        if (!ok) break;
-                        tc::fence_after_sync();
-                        issue_s(hh, j + 1);
-                    }
-                    ok = wait_ab(&sh.p_ready[hh], j & 1, sh, p.status);
+                if (j + 1 < n_kv) {
+                    // next scores as soon as the softmax has pulled the current ones out of TMEM
+                    ok = wait_ab(&sh.kv_full[ik % NSTAGE], (ik / NSTAGE) & 1, sh, p.status) &&
+                         wait_ab(&sh.s_free[hh], j & 1, sh, p.status);
                     if (!ok) break;
                     tc::fence_after_sync();
-                    issue_pv(hh, j);
+                    issue_s(j + 1);
+                    release(&sh.kv_empty[ik % NSTAGE]);
                 }
+                ok = wait_ab(&sh.kv_full[iv % NSTAGE], (iv / NSTAGE) & 1, sh, p.status) &&
+                     wait_ab(&sh.p_ready[hh][j % NPB], (j / NPB) & 1, sh, p.status);
                 if (!ok) break;
-                if (more) tc::commit(&sh.kv_empty[ik % NSTAGE]);
-                tc::commit(&sh.kv_empty[iv % NSTAGE]);
+                tc::fence_after_sync();
+                issue_pv(j);
+                release(&sh.kv_empty[iv % NSTAGE]);
             }
         }
         __syncwarp();
     } else {
-        // ===================================================== softmax (one thread per row)
-        const int hh = warp >> 2;
+        // ===================================================== softmax (thread = row, half the columns)
+        const int hh = warp >> 3;
+        const int half = (warp >> 2) & 1;
         if (hh < nheads) {
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;  // tile row = TMEM lane
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-            const uint32_t t_s = tmem + lane_off + C::TM_S0 + hh * BN;
-            const uint32_t t_o = tmem + lane_off + C::TM_O0 + hh * D;
+            const uint32_t t_s = tmem + lane_off + C::TM_S0 + hh * BN + half * HALF;
+            const uint32_t t_o = tmem + lane_off + C::TM_O0 + hh * D + half * (D / 2);
             const int qpos = qmin + r;
+            const int key_off = half * HALF;
             float m_ref = -INFINITY, l = 0.f;
+            // `ok` turns false (for the whole warp) once a wait times out or another role
+            // aborted; the loop still runs to the end so that both column halves of a head
+            // meet at every named barrier, but does no further work
             bool ok = true;
             for (int j = 0; j < n_kv; ++j) {
-                ok = __all_sync(0xffffffffu, wait_ab(&sh.s_full[hh], j & 1, sh, p.status));
-                if (!ok) break;
-                tc::fence_after_sync();
-                uint32_t sr[2][32];
-                tc::ld_32x32b_x32(t_s, sr[0]);
-                tc::ld_32x32b_x32(t_s + 32, sr[1]);
-                tc::wait_ld();
-                tc::fence_before_sync();
-                mbar_arrive(&sh.s_free[hh]);
-
-                const bool diag = (j + 1) * BN - 1 > qmin;
-                float x[BN];
-                float mx = -INFINITY;
+                if (ok) ok = __all_sync(0xffffffffu, wait_ab(&sh.s_full[hh], j & 1, sh, p.status));
+                float x[HALF];
+                float mine = -INFINITY;
+                if (ok) {
+                    tc::fence_after_sync();
+                    uint32_t sr[HALF];
+                    tc::ld_32x32b_x32(t_s, sr);
+                    tc::wait_ld();
+                    tc::fence_before_sync();
+                    mbar_arrive(&sh.s_free[hh]);
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    const float v = __uint_as_float(sr[c >> 5][c & 31]) * p.scale_log2;
-                    x[c] = (diag && j * BN + c > qpos) ? -INFINITY : v;
-                    mx = fmaxf(mx, x[c]);
+                    for (int c = 0; c < HALF; ++c) x[c] = __uint_as_float(sr[c]);
+                    if ((j + 1) * BN - 1 > qmin) {  // diagonal tile: some key is after some row
+                        const int k0 = j * BN + key_off;
+#pragma unroll
+                        for (int c = 0; c < HALF; ++c)
+                            if (k0 + c > qpos) x[c] = -INFINITY;
+                    }
+                    // row max of the raw scores (softmax_scale > 0) over my half, as a tree
+                    float t8[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) t8[i] = x[i];
+#pragma unroll
+                    for (int c = 8; c < HALF; ++c) t8[c & 7] = fmaxf(t8[c & 7], x[c]);
+                    mine = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
+                                 fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
                 }
+                // exchange with the warp holding the other half of the row
+                sh.xmax[hh][j & 1][half][r] = mine;
+                asm volatile("bar.sync %0, %1;" ::"r"(1 + hh), "r"(8 * 32) : "memory");
+                if (ok) ok = !*reinterpret_cast<volatile int*>(&sh.abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) continue;
+                const float other = sh.xmax[hh][j & 1][half ^ 1][r];
+                const float mx = (half == 0 ? fmaxf(mine, other) : fmaxf(other, mine)) * p.scale_log2;
                 if (j == 0) {
                     m_ref = mx;
-                } else {
-                    const bool need = mx > m_ref + TAU;
-                    if (__any_sync(0xffffffffu, need)) {
-                        const float m_new = fmaxf(m_ref, mx);
-                        const float alpha = ex2(m_ref - m_new);
-                        ok = __all_sync(0xffffffffu, wait_ab(&sh.pv_done[hh], (j - 1) & 1, sh, p.status));
-                        if (!ok) break;
-                        tc::fence_after_sync();
+                } else if (__any_sync(0xffffffffu, mx > m_ref + TAU)) {
+                    // rescale O (this half's columns) to a new reference maximum
+                    const float m_new = fmaxf(m_ref, mx);
+                    const float alpha = ex2(m_ref - m_new);
+                    // all earlier PVs are done once PV(j-1) is (one issuing thread, in order)
+                    ok = __all_sync(0xffffffffu,
+                                    wait_ab(&sh.pv_done[hh][(j - 1) % NPB], ((j - 1) / NPB) & 1, sh, p.status));
+                    if (!ok) continue;
+                    tc::fence_after_sync();
 #pragma unroll 1
-                        for (int c0 = 0; c0 < D; c0 += 32) {
-                            uint32_t o[32];
-                            tc::ld_32x32b_x32(t_o + c0, o);
-                            tc::wait_ld();
+                    for (int c0 = 0; c0 < D / 2; c0 += 32) {
+                        uint32_t o[32];
+                        tc::ld_32x32b_x32(t_o + c0, o);
+                        tc::wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                            tc::st_32x32b_x32(t_o + c0, o);
-                        }
-                        tc::wait_st();
-                        l *= alpha;
-                        m_ref = m_new;
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tc::st_32x32b_x32(t_o + c0, o);
                     }
+                    tc::wait_st();
+                    l *= alpha;
+                    m_ref = m_new;
                 }
-                float rs = 0.f;
-                uint32_t pk[BN / 2];
+                // p = 2^(s * scale_log2 - m_ref): one FFMA + one MUFU each; partial sums as a tree
+                const float neg = -m_ref;
+                float s8[8];
+                uint32_t pk[HALF / 2];
 #pragma unroll
-                for (int c = 0; c < BN; c += 2) {
-                    const float p0 = ex2(x[c] - m_ref), p1 = ex2(x[c + 1] - m_ref);
-                    rs += p0 + p1;
+                for (int c = 0; c < HALF; c += 2) {
+                    const float p0 = ex2(fmaf(x[c], p.scale_log2, neg));
+                    const float p1 = ex2(fmaf(x[c + 1], p.scale_log2, neg));
+                    const int k = (c >> 1) & 7;
+                    s8[k] = (c < 16) ? (p0 + p1) : (s8[k] + (p0 + p1));
                     pk[c >> 1] = pack_bf16x2(p0, p1);
                 }
-                l += rs;
-                // PV(j-1) must be done: it read the other P buffer's predecessor, and
-                // waiting for it keeps p_ready from running two phases ahead of the
-                // MMA issuer (mbarrier parity only tells adjacent phases apart)
-                if (j >= 1) {
-                    ok = __all_sync(0xffffffffu, wait_ab(&sh.pv_done[hh], (j - 1) & 1, sh, p.status));
-                    if (!ok) break;
+                l += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+                // P buffer j % NPB was last read by PV(j - NPB).  Waiting for that also keeps
+                // each p_ready / pv_done barrier within one phase of its waiter (mbarrier
+                // parity only tells adjacent phases apart).
+                if (j >= NPB) {
+                    ok = __all_sync(0xffffffffu,
+                                    wait_ab(&sh.pv_done[hh][j % NPB], ((j / NPB) - 1) & 1, sh, p.status));
+                    if (!ok) continue;
                 }
-                uint8_t* prow = sP + (hh * 2 + (j & 1)) * C::P_BYTES + r * 128;
+                uint8_t* prow = sP + (hh * NPB + (j % NPB)) * C::P_BYTES + r * 128;
 #pragma unroll
-                for (int c8 = 0; c8 < BN / 8; ++c8)
+                for (int i = 0; i < HALF / 8; ++i) {
+                    const int c8 = half * (HALF / 8) + i;
                     *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) =
-                        make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
-                if (hh == 0 && j == n_kv - 1 && (j + 1) * BN > seq_len) {
-                    // keys past the sequence end: their V rows may hold anything (0 * NaN = NaN)
-                    const int iv = 2 * j + 1;
-                    ok = __all_sync(0xffffffffu, wait_ab(&sh.kv_full[iv % NSTAGE], (iv / NSTAGE) & 1, sh, p.status));
-                    if (!ok) break;
-                    if (r < BN && j * BN + r >= seq_len) {
-                        uint8_t* vrow = sKV + (iv % NSTAGE) * C::KV_BYTES + r * 128;
-#pragma unroll
-                        for (int kb = 0; kb < C::KB; ++kb)
-#pragma unroll
-                            for (int c = 0; c < 8; ++c)
-                                *reinterpret_cast<uint4*>(vrow + kb * C::KV_KB + c * 16) = make_uint4(0, 0, 0, 0);
-                    }
+                        make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                 }
                 fence_proxy_async_smem();
                 tc::fence_before_sync();
-                mbar_arrive(&sh.p_ready[hh]);
+                mbar_arrive(&sh.p_ready[hh][j % NPB]);
             }
-            // ---- epilogue: O / l -> bf16
-            if (ok) ok = __all_sync(0xffffffffu, wait_ab(&sh.pv_done[hh], (n_kv - 1) & 1, sh, p.status));
+            // ---- epilogue: O / l -> bf16, each half stores its D/2 columns
+            sh.xsum[hh][half][r] = l;
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + hh), "r"(8 * 32) : "memory");
+            const float lt = half == 0 ? l + sh.xsum[hh][1][r] : sh.xsum[hh][0][r] + l;
+            if (ok)
+                ok = __all_sync(0xffffffffu,
+                                wait_ab(&sh.pv_done[hh][(n_kv - 1) % NPB], ((n_kv - 1) / NPB) & 1, sh, p.status));
             if (ok) {
                 tc::fence_after_sync();
-                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float inv = lt > 0.f ? 1.f / lt : 0.f;
                 const bool store = r < rows_valid;
                 const int h = h0 + hh;
-                __nv_bfloat16* orow = p.out + ((size_t)(row0 + r) * p.Hq + h) * D;
+                __nv_bfloat16* orow = p.out + ((size_t)(row0 + r) * p.Hq + h) * D + half * (D / 2);
 #pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int c0 = 0; c0 < D / 2; c0 += 32) {
                     uint32_t o[32];
                     tc::ld_32x32b_x32(t_o + c0, o);
                     tc::wait_ld();
@@ -457,14 +581,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
                     }
                 }
-                if (store && p.lse != nullptr)
-                    p.lse[(size_t)(row0 + r) * p.Hq + h] = l > 0.f ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+                if (store && half == 0 && p.lse != nullptr)
+                    p.lse[(size_t)(row0 + r) * p.Hq + h] = lt > 0.f ? (m_ref + lg2(lt)) * kLn2 : -INFINITY;
             }
         }
     }
 
     tc::fence_before_sync();
     __syncthreads();
+    if (CS > 1) cluster_sync();  // nobody multicasts into or arrives on this CTA any more
     tc::fence_after_sync();
     if (warp == WARP_TMA) tc::tmem_dealloc(tmem, C::TM_COLS);
 }
@@ -490,6 +615,7 @@ extern "C" int attn_prefill_varlen_causal(void* out, float* lse, const void* q, 
     if (batch < 0 || total_q < 0 || max_q_len < 0 || max_seq_len < 0) return PA_ERR_SHAPE;
     int rc = check_common_shapes(page_size, num_q_heads, num_kv_heads, head_dim);
     if (rc != PA_OK) return rc;
+    if (!(softmax_scale > 0.f) || softmax_scale == INFINITY) return PA_ERR_SHAPE;  // also rejects NaN
     if (batch == 0 || total_q == 0) return PA_OK;
     if (!out || !q || !k_pool || !v_pool || !block_table || !cu_seqlens_q || !seq_lens) return PA_ERR_NULL;
     if (num_pages < 1 || max_pages_per_seq < 1) return PA_ERR_SHAPE;
@@ -503,7 +629,9 @@ extern "C" int attn_prefill_varlen_causal(void* out, float* lse, const void* q, 
     if (rc != PA_OK) return rc;
 
     const int group = num_q_heads / num_kv_heads;
-    const int NP = (group + 1) / 2;
+    const int pairs = (group + 1) / 2;
+    const int CS = pairs < pf::MAX_CLUSTER ? pairs : pf::MAX_CLUSTER;
+    const int NP = (pairs + CS - 1) / CS * CS;  // padded: a cluster never spans two KV heads
     const long long tiles_upper = (long long)(total_q + pf::BM - 1) / pf::BM + batch;
     const long long grid = tiles_upper * num_kv_heads * NP;
     if (grid >= (1ll << 31)) return PA_ERR_SHAPE;
@@ -519,6 +647,8 @@ extern "C" int attn_prefill_varlen_causal(void* out, float* lse, const void* q, 
     prm.block_table = block_table;
     prm.seq_lens = seq_lens;
     prm.cu_q = cu_seqlens_q;
+    prm.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
+    prm.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
     prm.status = status;
     prm.num_pages = num_pages;
     prm.max_pages = max_pages_per_seq;
@@ -528,6 +658,7 @@ extern "C" int attn_prefill_varlen_causal(void* out, float* lse, const void* q, 
     prm.Hkv = num_kv_heads;
     prm.group = group;
     prm.NP = NP;
+    prm.CS = CS;
     prm.skip_single = 1;  // q_len == 1 entries go to the split-K decode kernel below
     prm.scale_log2 = softmax_scale * kLog2e;
 
@@ -538,17 +669,30 @@ extern "C" int attn_prefill_varlen_causal(void* out, float* lse, const void* q, 
     if (rc != PA_OK) return rc;
     if (max_q_len < 2) return PA_OK;  // no entry needs the prefill kernel
 
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(pf::NTHREADS, 1, 1);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t err;
     if (head_dim == 128) {
-        constexpr int smem = pf::Cfg<128>::SMEM_BYTES;
-        if (set_smem_limit_once((const void*)pf::prefill_kernel<128>, smem, dev.device, 2) != PA_OK)
+        cfg.dynamicSmemBytes = pf::Cfg<128>::SMEM_BYTES;
+        if (set_smem_limit_once((const void*)pf::prefill_kernel<128>, pf::Cfg<128>::SMEM_BYTES, dev.device, 2) !=
+            PA_OK)
             return PA_ERR_CUDA;
-        pf::prefill_kernel<128><<<(unsigned)grid, pf::NTHREADS, smem, st>>>(qmap, kmap, vmap, prm);
+        err = cudaLaunchKernelEx(&cfg, pf::prefill_kernel<128>, qmap, kmap, vmap, prm);
     } else {
-        constexpr int smem = pf::Cfg<64>::SMEM_BYTES;
-        if (set_smem_limit_once((const void*)pf::prefill_kernel<64>, smem, dev.device, 3) != PA_OK)
+        cfg.dynamicSmemBytes = pf::Cfg<64>::SMEM_BYTES;
+        if (set_smem_limit_once((const void*)pf::prefill_kernel<64>, pf::Cfg<64>::SMEM_BYTES, dev.device, 3) !=
+            PA_OK)
             return PA_ERR_CUDA;
-        pf::prefill_kernel<64><<<(unsigned)grid, pf::NTHREADS, smem, st>>>(qmap, kmap, vmap, prm);
+        err = cudaLaunchKernelEx(&cfg, pf::prefill_kernel<64>, qmap, kmap, vmap, prm);
     }
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
