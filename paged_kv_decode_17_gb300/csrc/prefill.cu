@@ -12,7 +12,7 @@
 // GB300 design (one CTA = one 128-row query tile of one sequence, for two
 // query heads that share a KV head, so each K/V tile is loaded once for both):
 // * warp 16 (producer): loads the two Q tiles once by TMA, then gathers K and
-//   V tiles through a 7-stage ring: a 64-key tile is four 16-row page blocks
+//   V tiles through an 8-stage ring: a 64-key tile is four 16-row page blocks
 //   found through the block table (one tile ahead), copied with coalesced
 //   16-byte cp.async into the 128-byte-swizzled operand layout.
 // * warps 17 / 18 (MMA, one per head): one thread issues tcgen05.mma:
@@ -22,8 +22,9 @@
 // * warps 0-15 (softmax): per head two warpgroups, each owning half of the
 //   64 score columns of every row (thread = TMEM lane = row); the two halves
 //   exchange their row maxima through shared memory at a named barrier.  They
-//   write P (bf16) to shared memory in the MMA operand layout and at the end
-//   normalise O and store it.  O is rescaled only when a row's maximum grows by
+//   write P (bf16 pairs) into TMEM with tcgen05.st, where the P.V MMA reads it
+//   as its A operand (no shared-memory round trip, no proxy fence), and at the
+//   end normalise O and store it.  O is rescaled only when a row's maximum grows by
 //   more than TAU = 8 (log2 units): until then the exponentials are taken
 //   against the older, smaller maximum, which keeps them <= 2^8 and the result
 //   exact, because the final division uses the same reference maximum for
@@ -39,7 +40,7 @@ namespace pf {
 constexpr int BM = 128;      // query rows per tile (= TMEM lanes)
 constexpr int BN = 64;       // keys per KV tile
 #ifndef PA_PF_NSTAGE
-#define PA_PF_NSTAGE 5
+#define PA_PF_NSTAGE 8
 #endif
 #ifndef PA_PF_NPB
 #define PA_PF_NPB 2
@@ -68,12 +69,15 @@ struct Cfg {
     static constexpr int Q_KB = BM * 128;           // bytes per column block of a Q tile
     static constexpr int KV_KB = BN * 128;          // bytes per column block of a K/V tile
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_P = 2 * Q_BYTES;       // P[head][buffer]
-    static constexpr int OFF_KV = OFF_P + 2 * NPB * P_BYTES;
+    static constexpr int OFF_KV = 2 * Q_BYTES;
     static constexpr int SMEM_BYTES = 1024 + OFF_KV + NSTAGE * KV_BYTES;
+    // TMEM columns: S[head] (BN fp32), O[head] (D fp32), P[head][buffer] (BN bf16 = BN/2)
     static constexpr int TM_S0 = 0;
     static constexpr int TM_O0 = 2 * BN;
-    static constexpr int TM_COLS = (2 * BN + 2 * D) <= 256 ? 256 : 512;
+    static constexpr int TM_P0 = 2 * BN + 2 * D;
+    static constexpr int TM_USED = TM_P0 + 2 * NPB * (BN / 2);
+    static constexpr int TM_COLS = TM_USED <= 256 ? 256 : 512;
+    static_assert(TM_USED <= 512, "TMEM budget");
     static constexpr uint32_t IDESC_S = tc::idesc_bf16(BM, BN, 0, 0);   // Q K-major, K K-major
     static constexpr uint32_t IDESC_PV = tc::idesc_bf16(BM, D, 0, 1);   // P K-major, V MN-major
 };
@@ -275,7 +279,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t tmem = sh.tmem_base;
 
     uint8_t* sQ = smem + C::OFF_Q;
-    uint8_t* sP = smem + C::OFF_P;
     uint8_t* sKV = smem + C::OFF_KV;
 
     if (warp == WARP_TMA) {
@@ -382,7 +385,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int hh = warp - WARP_MMA0;
         if (lane == 0 && hh < nheads) {
             const uint32_t qaddr = smem_u32(sQ) + hh * C::Q_BYTES;
-            const uint32_t p_base = smem_u32(sP) + hh * NPB * C::P_BYTES;
+            const uint32_t t_p = tmem + C::TM_P0 + hh * NPB * (BN / 2);
             const uint32_t kv_base = smem_u32(sKV);
             const uint32_t t_s = tmem + C::TM_S0 + hh * BN;
             const uint32_t t_o = tmem + C::TM_O0 + hh * D;
@@ -400,12 +403,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             };
             auto issue_pv = [&](int j) {
                 const uint32_t vaddr = kv_base + ((2 * j + 1) % NSTAGE) * C::KV_BYTES;
-                const uint32_t paddr = p_base + (j % NPB) * C::P_BYTES;
+                const uint32_t pcol = t_p + (j % NPB) * (BN / 2);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t ad = tc::smem_desc_sw128(paddr + kk * 32, 16, 1024);
                     const uint64_t bd = tc::smem_desc_sw128(vaddr + kk * 2048, C::KV_KB, 1024);
-                    tc::mma_ss(t_o, ad, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_ts(t_o, pcol + kk * 8, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc::commit(&sh.pv_done[hh][j % NPB]);
             };
@@ -453,6 +455,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
             const uint32_t t_s = tmem + lane_off + C::TM_S0 + hh * BN + half * HALF;
             const uint32_t t_o = tmem + lane_off + C::TM_O0 + hh * D + half * (D / 2);
+            const uint32_t t_p = tmem + lane_off + C::TM_P0 + hh * NPB * (BN / 2);
             const int qpos = qmin + r;
             const int key_off = half * HALF;
             float m_ref = -INFINITY, l = 0.f;
@@ -541,14 +544,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                     wait_ab(&sh.pv_done[hh][j % NPB], ((j / NPB) - 1) & 1, sh, p.status));
                     if (!ok) continue;
                 }
-                uint8_t* prow = sP + (hh * NPB + (j % NPB)) * C::P_BYTES + r * 128;
-#pragma unroll
-                for (int i = 0; i < HALF / 8; ++i) {
-                    const int c8 = half * (HALF / 8) + i;
-                    *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) =
-                        make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                }
-                fence_proxy_async_smem();
+                // P (bf16 pairs, low half = even key) into this head's TMEM P columns
+                tc::st_32x32b_x16(t_p + (j % NPB) * (BN / 2) + half * (HALF / 2), pk);
+                tc::wait_st();
                 tc::fence_before_sync();
                 mbar_arrive(&sh.p_ready[hh][j % NPB]);
             }
