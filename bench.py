@@ -453,7 +453,8 @@ def measure_prefill(pa, steps, warmup, peaks):
            "tokens_per_s": case.total_q / ((a + w) * 1e-3),
            "kv_write": {"ms": w, "bytes": wbytes, "gbs": wbytes / (w * 1e-3) / 1e9,
                         "frac_hbm": wbytes / (w * 1e-3) / 1e9 / peaks["hbm_gbs"]},
-           "l2": "flushed (256 MiB write) between iterations", "steps": steps, "launches_per_step": 3}
+           "l2": "flushed (256 MiB write) between iterations", "steps": steps,
+           "launches_per_step": 4}  # writeback, split-K decode (no entry to serve here), plan, prefill
     del case, flush
     torch.cuda.empty_cache()
     return res
@@ -487,9 +488,10 @@ def measure_mixed(pa, steps, warmup, peaks):
         torch.cuda.synchronize()
         ms.append(e0.elapsed_time(e1))
     t = statistics.median(ms)
-    dec = [(L, q) for L, q in zip(case.seq_lens_host, case.q_lens_host) if q == 1]
-    pre_q = [q for q in case.q_lens_host if q > 1]
-    pre_L = [L for L, q in zip(case.seq_lens_host, case.q_lens_host) if q > 1]
+    # entries with up to 8 query rows run on the split-K decode path (HBM-bound), longer ones on the prefill kernel
+    dec = [(L, q) for L, q in zip(case.seq_lens_host, case.q_lens_host) if q <= 8]
+    pre_q = [q for q in case.q_lens_host if q > 8]
+    pre_L = [L for L, q in zip(case.seq_lens_host, case.q_lens_host) if q > 8]
     dbytes = roofline.decode_kv_bytes([L for L, _ in dec], case.num_kv_heads, case.head_dim)
     flops = roofline.prefill_flops(pre_q, pre_L, case.num_q_heads, case.head_dim)
     t_bytes = dbytes / (peaks["hbm_gbs"] * 1e9)
@@ -499,8 +501,49 @@ def measure_mixed(pa, steps, warmup, peaks):
            "step_ms": t, "decode_kv_bytes": dbytes, "prefill_flops": flops,
            "t_roofline_ms": 1e3 * max(t_bytes, t_flops), "t_serial_roofline_ms": 1e3 * (t_bytes + t_flops),
            "frac_of_roofline": max(t_bytes, t_flops) / (t * 1e-3),
-           "tokens_per_s": case.total_q / (t * 1e-3), "launches_per_step": 2, "steps": steps,
+           "tokens_per_s": case.total_q / (t * 1e-3), "launches_per_step": 3, "steps": steps,
            "l2": "inputs larger than L2 (about 9 GB of KV)"}
+    del case
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_multiquery(pa, steps, warmup, peaks, q_len=4):
+    """Multi-query decode (speculative-decode verification): the qwen7b_decode
+    shape with q_len query rows per sequence, causal inside the block; the
+    KV (512 MiB) exceeds L2, so no flush is needed."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = workloads.qwen7b_multiquery(device=dev, q_len=q_len)
+    stream = torch.cuda.current_stream()
+    B, Hq, D = case.batch, case.num_q_heads, case.head_dim
+    ws = pa.Workspace(pa.decode_multiquery_workspace_bytes(B, q_len, Hq, case.num_kv_heads, D), dev)
+    out = torch.empty_like(case.q)
+
+    def attn():
+        pa.attn_decode_multiquery_paged(case.q, case.k_pool, case.v_pool, case.block_table, case.cu_seqlens_q,
+                                        case.seq_lens, case.softmax_scale, max_q_len=q_len,
+                                        max_seq_len=case.max_seq_len, out=out, workspace=ws)
+
+    for _ in range(warmup):
+        attn()
+    torch.cuda.synchronize()
+    ev = _events(stream, 2 * steps)
+    for i in range(steps):
+        ev[2 * i].record(stream)
+        attn()
+        ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(steps)]
+    t = statistics.mean(ms)
+    kv = roofline.decode_kv_bytes(case.seq_lens_host, case.num_kv_heads, D)
+    gbs = kv / (t * 1e-3) / 1e9
+    res = {"workload": "qwen7b_multiquery: batch 32 x 8192-token contexts, %d query rows per sequence (causal "
+                       "inside the block), Hq=28, Hkv=4, head_dim 128, 16-token pages" % q_len,
+           "q_len": q_len, "ms": t, "kv_bytes": kv,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]},
+           "tokens_per_s": B * q_len / (t * 1e-3), "steps": steps, "launches_per_step": 1,
+           "l2": "inputs larger than L2 (512 MiB of KV), no flush"}
     del case
     torch.cuda.empty_cache()
     return res
@@ -514,7 +557,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-only", action="store_true", help="skip the prefill and mixed-step measurements")
-    ap.add_argument("--only", choices=["prefill", "mixed"], default=None,
+    ap.add_argument("--only", choices=["prefill", "mixed", "multiquery"], default=None,
                     help="run just this extra measurement (for profiling); prints its object only")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
@@ -529,7 +572,7 @@ def main(argv=None):
     peaks = load_peaks()
     dev = torch.device("cuda", torch.cuda.current_device())
     if args.only is not None:
-        fn = measure_prefill if args.only == "prefill" else measure_mixed
+        fn = {"prefill": measure_prefill, "mixed": measure_mixed, "multiquery": measure_multiquery}[args.only]
         res = fn(pa, args.steps, args.warmup, peaks)
         if rank == 0:
             print(json.dumps({"only": args.only, args.only: res}), flush=True)
@@ -578,7 +621,8 @@ def main(argv=None):
         psteps = max(3, min(args.steps, 20))
         line["prefill"] = measure_prefill(pa, psteps, 3, peaks)
         line["mixed"] = measure_mixed(pa, psteps, 3, peaks)
-        line["gpu_launches"] += world * psteps * (3 + 2)
+        line["multiquery"] = measure_multiquery(pa, psteps, 3, peaks)
+        line["gpu_launches"] += world * psteps * (4 + 3 + 1)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_subprocess()
     if rank == 0:

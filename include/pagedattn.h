@@ -14,6 +14,9 @@
  *                                and merged with the log-sum-exp identity
  *                                ("The Stack Below the Stack, Part 2",
  *                                section 2.2 Flash-Decoding, steps 1-3).
+ *   attn_decode_multiquery_paged the same for a short block (2-8) of query
+ *                                rows per sequence, causal inside the block
+ *                                (speculative-decode verification).
  *   attn_prefill_varlen_causal   causal attention of variable-length query
  *                                blocks against their paged K/V, tiled with
  *                                the online softmax ("The Stack Below the
@@ -92,10 +95,14 @@ const char* pa_status_string(int status);
  * Workspace bytes attn_decode_paged needs for these sizes on the current
  * device.  The workspace holds the split partials (normalised partial
  * outputs and their log-sum-exps) and one arrival counter per
- * (sequence, KV head, head block).  The caller must ZERO it once after
- * allocating it; every successful call leaves the counters zero again.  If
- * a call reports a device error, zero it again before reuse.  Two calls that
- * may run concurrently need separate workspaces.
+ * (sequence, KV head, segment of query rows) at its start.  The caller must
+ * ZERO it once after allocating it; every successful call leaves the
+ * counters zero again.  A workspace may serve calls of different sizes: the
+ * library remembers, per workspace address, the size of the last call's
+ * counter region and clears the counters (one small asynchronous memset on
+ * `stream`) when it changes.  If a call reports a device error, zero it
+ * again before reuse.  Two calls that may run concurrently need separate
+ * workspaces.
  */
 size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim);
 
@@ -116,9 +123,46 @@ int attn_decode_paged(void* out, float* lse, const void* q, const void* k_pool, 
                       void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
+ * Workspace bytes attn_decode_multiquery_paged needs when no entry has more
+ * than max_q_len (1..8) query rows; same zeroing rules as the decode
+ * workspace.  Returns 0 for unsupported sizes.
+ */
+size_t pa_decode_multiquery_workspace_bytes(int batch, int max_q_len, int num_q_heads, int num_kv_heads,
+                                            int head_dim);
+
+/*
+ * Multi-query decode: a short block of q_len = cu_seqlens_q[b+1] -
+ * cu_seqlens_q[b] query rows per sequence (1 <= q_len <= 8), e.g. the tokens
+ * a draft model proposed, verified in one pass ("Inside Ion", section "What
+ * Is Next": speculative decoding).  Row i of sequence b sits at position
+ * seq_lens[b] - q_len + i and attends keys 0 .. that position (causal inside
+ * the block, every earlier cached token visible), exactly as in
+ * attn_prefill_varlen_causal; the work is split along the KV sequence and
+ * merged as in attn_decode_paged, so the KV of a sequence is read from HBM
+ * once for all its query rows and heads.
+ *   out        bf16 [total_q][num_q_heads][head_dim]          (written)
+ *   lse        float [total_q][num_q_heads] or NULL            (written)
+ *   q          bf16 [total_q][num_q_heads][head_dim]
+ *   cu_seqlens_q  int32 [batch+1], non-decreasing, cu_seqlens_q[batch] <= total_q
+ *   max_q_len  host upper bound of q_len, 1..8 (PA_ERR_SHAPE otherwise); it
+ *              sizes the workspace (pa_decode_multiquery_workspace_bytes)
+ * An entry with q_len = 0 is skipped.  On the device, q_len > max_q_len,
+ * cu_seqlens_q outside [0, total_q] or 0 < seq_lens[b] < q_len (for q_len > 1)
+ * report PA_ERR_BAD_LEN; rows with no visible key get out = 0 and lse = -inf.
+ */
+int attn_decode_multiquery_paged(void* out, float* lse, const void* q, const void* k_pool,
+                                 const void* v_pool, int num_pages, const int32_t* block_table,
+                                 int max_pages_per_seq, const int32_t* cu_seqlens_q,
+                                 const int32_t* seq_lens, int batch, int total_q, int max_q_len,
+                                 int max_seq_len, int page_size, int num_q_heads, int num_kv_heads,
+                                 int head_dim, float softmax_scale, void* workspace,
+                                 size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
  * Workspace bytes attn_prefill_varlen_causal needs (same zeroing rules as
- * the decode workspace; it also holds the split partials of q_len = 1
- * entries).
+ * the decode workspace; it also holds the split partials of the entries
+ * with at most 8 query rows, which the call serves on the split-K decode
+ * path).
  */
 size_t pa_prefill_workspace_bytes(int batch, int total_q, int num_q_heads, int num_kv_heads, int head_dim);
 
@@ -129,8 +173,9 @@ size_t pa_prefill_workspace_bytes(int batch, int total_q, int num_q_heads, int n
  * position seq_lens[b] - q_len + i and attends keys 0 .. that position
  * (bottom-right causal alignment: earlier cached tokens are all visible).
  * The K/V of the query rows themselves must already be in the pool (call
- * kv_write_paged first, on the same stream).  Entries with q_len = 1 are
- * ordinary decode rows, so one call serves a mixed prefill + decode step.
+ * kv_write_paged first, on the same stream).  Entries with q_len <= 8 are
+ * served exactly as attn_decode_multiquery_paged serves them (q_len = 1 is
+ * ordinary decode), so one call serves a mixed prefill + decode step.
  *   out        bf16 [total_q][num_q_heads][head_dim]          (written)
  *   lse        float [total_q][num_q_heads] or NULL            (written)
  *   q          bf16 [total_q][num_q_heads][head_dim]
@@ -173,9 +218,10 @@ int kv_write_paged(void* k_pool, void* v_pool, int num_pages, const void* k_new,
  * which every GPU that loads the library holds until the process exits.
  * Problems whose workspace (pa_decode_workspace_bytes) exceeds 8 MiB are
  * rejected with PA_ERR_SCRATCH_LIMIT before anything is enqueued; roughly,
- * batch * num_kv_heads * ceil((num_q_heads/num_kv_heads)/16) plus twice the
- * SM count must stay below about 1000 at head_dim 128 (about 2000 at
- * head_dim 64).
+ * (batch * num_kv_heads * ceil(group / 64) + twice the SM count) * rows must
+ * stay below about 16,000 at head_dim 128 (about 32,000 at head_dim 64),
+ * where group = num_q_heads / num_kv_heads and rows = 16 for group <= 16,
+ * 32 for group <= 32 and 64 above.
  *
  * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
  * The first call on each device looks up the array's device address

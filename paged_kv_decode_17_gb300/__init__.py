@@ -4,6 +4,9 @@ Public calls (same names as the C ABI in include/pagedattn.h):
 
 * ``kv_write_paged``              eager writeback of new K/V rows into pages
 * ``attn_decode_paged``           split-K Flash-Decoding over pages
+* ``attn_decode_multiquery_paged`` the same for 1-8 query rows per sequence,
+                                  causal inside the block (speculative
+                                  decoding's verification pass)
 * ``attn_prefill_varlen_causal``  varlen causal prefill (and mixed
                                   prefill + decode steps) over pages
 
@@ -14,9 +17,11 @@ with ``paged_kv_decode_17_gb300.build.build()``.
 
 from .ops import (  # noqa: F401
     Workspace,
+    attn_decode_multiquery_paged,
     attn_decode_paged,
     attn_prefill_varlen_causal,
     check_status,
+    decode_multiquery_workspace_bytes,
     decode_workspace_bytes,
     kv_write_paged,
     new_status,

@@ -9,10 +9,10 @@
 // section 2.1 (running max and running sum, rescaled when the max grows).
 //
 // GB300 design
-// * Work is measured in "units": 16 consecutive tokens of one
-//   (sequence b, KV head g, head block hb) segment.  A unit is one 16 x D bf16
-//   block of K plus one of V, contiguous in the [page][Hkv][page_size][D]
-//   pools.  All units of all segments are laid end to end and every CTA of a
+// * Work is measured in "units": 16 consecutive tokens of one row block of a
+//   (sequence b, KV head g, row segment sb) segment (row blocks below).  A
+//   unit is one 16 x D bf16 block of K plus one of V, contiguous in the
+//   [page][Hkv][page_size][D] pools.  All units of all segments are laid end to end and every CTA of a
 //   persistent grid (a multiple of the SM count) takes one equal contiguous
 //   range of them, so a 1-token sequence and a 131k-token one balance the
 //   same way.  The ranges are derived on the device from seq_lens (no host
@@ -25,18 +25,26 @@
 //   the TMA engine's per-request cost capped the read rate near 18 bytes per
 //   cycle per SM.)  There is no cross-warp producer/consumer handshake in the
 //   loop.
-// * Q.K^T and P.V run on bf16 mma.sync (m16n8k16) with the GQA head block as
-//   the M dimension (up to 16 query heads share one KV head's K/V tiles);
-//   scores, running max/sum and O stay in fp32 registers.
-// * At the end of the CTA's part of a segment the warps' states are merged
-//   in shared memory in a fixed order.  A segment covered by one CTA is
-//   normalised and stored directly; otherwise the partial (o_c, lse_c) goes
-//   to the workspace and the last CTA to arrive (atomic ticket, no waiting)
-//   merges all partials of that segment in a fixed order, so results are
-//   bit-identical run to run.
+// * Q.K^T and P.V run on bf16 mma.sync (m16n8k16) with query rows as the M
+//   dimension: the rows of one (sequence, KV head) are its q_len query tokens
+//   times the GQA group's heads (numbered token-major), cut into row blocks of
+//   at most 16.  Up to 4 row blocks (64 rows) form one segment; its units are
+//   ordered key block by key block, row block fastest, so the warps that take
+//   the row blocks of one key block stage it at the same moment and all but
+//   the first find it in L2.  With q_len > 1 (multi-query decode, e.g. the
+//   verification of speculated tokens) row i of the query block sees keys
+//   0 .. seq_len - q_len + i.  Scores, running max/sum and O stay in fp32
+//   registers.
+// * At the end of the CTA's part of a segment the states of the warps that
+//   hold the same row block are merged in shared memory in a fixed order.  A
+//   segment covered by one CTA is normalised and stored directly; otherwise
+//   the partial (o_c, lse_c) goes to the workspace and the last CTA to arrive
+//   (atomic ticket, no waiting) merges all partials of that segment in a
+//   fixed order, so results are bit-identical run to run.
 #include "pa_common.cuh"
 #include "pa_host.h"
 
+#include <climits>
 #include <mutex>
 
 namespace pa {
@@ -44,20 +52,21 @@ namespace dec {
 
 constexpr int W = 4;           // warps per CTA
 constexpr int UNIT = 16;       // tokens per unit
-constexpr int MAXR = 16;       // query heads per head block (mma M)
+constexpr int RB = 16;         // rows per row block (mma M)
+constexpr int SBR = 64;        // rows per segment (at most W row blocks)
 constexpr int MIN_CHUNK = 16;  // minimum units per CTA
 constexpr int CTAS_PER_SM = 2;  // two CTAs (8 warps) per SM hide each other's latency
 
 template <int D>
 struct Cfg {
     static constexpr int DEPTH = (D == 128) ? 3 : 6;
-    static constexpr int BOXES = D / 64;             // 128-byte-wide TMA boxes per row
+    static constexpr int BOXES = D / 64;             // 128-byte-wide column blocks per row
     static constexpr int BOX_BYTES = UNIT * 128;     // 16 rows x 128 bytes
     static constexpr int UNIT_BYTES = UNIT * D * 2;  // one K or V unit
     static constexpr int STAGE_BYTES = 2 * UNIT_BYTES;
     static constexpr int STAGES_BYTES = W * DEPTH * STAGE_BYTES;
     static constexpr int MSTRIDE = D + 4;  // fp32 row stride of the merge buffer
-    static constexpr int MERGE_BYTES = MAXR * MSTRIDE * 4;  // warps add into it one after another
+    static constexpr int MERGE_BYTES = RB * MSTRIDE * 4;  // warps add into it one after another
     static constexpr int SMEM_BYTES = 1024 + STAGES_BYTES + MERGE_BYTES;
 };
 
@@ -69,43 +78,92 @@ struct Params {
     const __nv_bfloat16* v_pool;
     const int32_t* block_table;
     const int32_t* seq_lens;
-    const int32_t* cu_q;  // non-null in a mixed call: only entries with one query row are decoded here
+    const int32_t* cu_q;  // null: one query row per sequence (row b); else rows cu_q[b] .. cu_q[b+1]
     int32_t* counters;
-    float* ws_lse;  // [slots][MAXR], log2 domain
-    float* ws_o;    // [slots][MAXR][D], normalised
+    float* ws_lse;  // [slots][RS], log2 domain
+    float* ws_o;    // [slots][RS][D], normalised
     int32_t* status;
     int num_pages, max_pages, batch, page_size, ps_shift;  // page_size = 1 << ps_shift
-    int Hq, Hkv, group, HB, R;
+    int total_q;  // rows of q / out
+    int qmax;     // entries with 1 <= q_len <= qmax are served here
+    int qcap;     // q_len in (qmax, qcap] is an error (larger ones belong to the prefill kernel)
+    int Hq, Hkv, group;
+    int SBmax;    // segments per (sequence, KV head) at q_len = qmax
+    int RS;       // rows per workspace slot (16 x the largest row-block count)
     float scale_log2;
 };
 
-// One (b, g, hb) segment: its units are [start, end) in the global order
-// b-major, then g, then hb.
-struct Seg {
-    int b, g, hb, len, n, start, end;
+// Row geometry of one served sequence: rows = q_len * group, split into SB
+// segments of RSB rows, each split into 1 << nrb_shift row blocks of R rows.
+struct SeqShape {
+    int len, qlen, nkb, SB, RSB, nrb_shift, R;
 };
 
-// Is sequence b served by this kernel?  Always in a decode call; in a mixed
-// call only when it contributes exactly one query row.
-__device__ __forceinline__ bool is_decode_entry(const Params& p, int b) {
-    return p.cu_q == nullptr || __ldg(p.cu_q + b + 1) - __ldg(p.cu_q + b) == 1;
+__device__ __forceinline__ SeqShape seq_shape(const Params& p, int b) {
+    SeqShape s;
+    s.len = 0;
+    s.nkb = 0;
+    s.SB = 1;
+    s.RSB = 0;
+    s.nrb_shift = 0;
+    s.R = 0;
+    s.qlen = 1;
+    if (p.cu_q != nullptr) {
+        const int c0 = __ldg(p.cu_q + b), c1 = __ldg(p.cu_q + b + 1);
+        s.qlen = c1 - c0;
+        if (c0 < 0 || c1 > p.total_q || (s.qlen > p.qmax && s.qlen <= p.qcap)) {
+            report(p.status, PA_ERR_BAD_LEN);
+            s.qlen = 0;
+        }
+        if (s.qlen < 1 || s.qlen > p.qmax) {
+            s.qlen = 0;  // not served by this kernel
+            return s;
+        }
+    }
+    int len = __ldg(p.seq_lens + b);
+    const int cap = p.max_pages * p.page_size;
+    if (len < 0 || len > cap || (s.qlen > 1 && len < s.qlen)) {
+        report(p.status, PA_ERR_BAD_LEN);
+        len = len < 0 ? 0 : (len > cap ? cap : len);
+    }
+    s.len = len;
+    s.nkb = (len + UNIT - 1) / UNIT;
+    const int rows = s.qlen * p.group;
+    s.SB = (rows + SBR - 1) / SBR;
+    s.RSB = (rows + s.SB - 1) / s.SB;
+    const int nrb = (s.RSB + RB - 1) / RB;
+    s.nrb_shift = nrb <= 1 ? 0 : (nrb == 2 ? 1 : 2);
+    s.R = (s.RSB + (1 << s.nrb_shift) - 1) >> s.nrb_shift;
+    return s;
 }
 
-// Row of q / out holding sequence b's query.
+// Units of all segments of sequence b.
+__device__ __forceinline__ int seq_units(const Params& p, const SeqShape& s) {
+    return (s.nkb << s.nrb_shift) * p.Hkv * s.SB;
+}
+
+// Row of q / out holding token 0 of sequence b's query block.
 __device__ __forceinline__ size_t q_row(const Params& p, int b) {
     return p.cu_q == nullptr ? (size_t)b : (size_t)__ldg(p.cu_q + b);
 }
 
-// Keys of sequence b this kernel attends over (0 for entries it does not serve).
-__device__ __forceinline__ int load_len(const Params& p, int b) {
-    if (!is_decode_entry(p, b)) return 0;
-    int len = __ldg(p.seq_lens + b);
-    const int cap = p.max_pages * p.page_size;
-    if (len < 0 || len > cap) {
-        report(p.status, PA_ERR_BAD_LEN);
-        len = len < 0 ? 0 : cap;
+// One (b, g, sb) segment: its units are [start, end) in the global order
+// b-major, then g, then sb; inside, key block major, row block fastest.
+struct Seg {
+    int b, g, sb, n, start, end;
+    SeqShape sh;
+};
+
+__device__ __forceinline__ void seg_set_seq(Seg& s, const Params& p, int b) {
+    s.b = b;
+    if (b < p.batch) {
+        s.sh = seq_shape(p, b);
+    } else {
+        s.sh.nkb = 0;
+        s.sh.SB = 1;
+        s.sh.nrb_shift = 0;
     }
-    return len;
+    s.n = s.sh.nkb << s.sh.nrb_shift;
 }
 
 // Advance to the next segment with at least one unit.  The caller makes sure
@@ -113,13 +171,11 @@ __device__ __forceinline__ int load_len(const Params& p, int b) {
 __device__ __forceinline__ void seg_next(Seg& s, const Params& p) {
     do {
         s.start = s.end;
-        if (++s.hb == p.HB) {
-            s.hb = 0;
+        if (++s.sb == s.sh.SB) {
+            s.sb = 0;
             if (++s.g == p.Hkv) {
                 s.g = 0;
-                ++s.b;
-                s.len = (s.b < p.batch) ? load_len(p, s.b) : 0;
-                s.n = (s.len + UNIT - 1) / UNIT;
+                seg_set_seq(s, p, s.b + 1);
             }
         }
         s.end = s.start + s.n;
@@ -157,7 +213,7 @@ __device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, 
                                            int lane, uint64_t policy) {
     using C = Cfg<D>;
     constexpr int CH = D / 8;  // 16-byte chunks per row
-    const int j = it.u - it.seg.start;  // unit index within the sequence
+    const int j = (it.u - it.seg.start) >> it.seg.sh.nrb_shift;  // key block within the sequence
     const int tok0 = j * UNIT;
     const int page = tok0 >> p.ps_shift;
     const int sub = (tok0 - (page << p.ps_shift)) / UNIT;
@@ -170,7 +226,7 @@ __device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, 
     } else {
         if (lane == 0) *phys_slot = phys;
         const size_t row = (size_t)(phys * p.Hkv + it.seg.g) * p.page_size + sub * UNIT;
-        const int valid = min(UNIT, it.seg.len - tok0);
+        const int valid = min(UNIT, it.seg.sh.len - tok0);
         const char* ksrc = reinterpret_cast<const char*>(p.k_pool + row * D);
         const char* vsrc = reinterpret_cast<const char*>(p.v_pool + row * D);
         const uint32_t sbase = smem_u32(stage);
@@ -206,7 +262,7 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
     uint8_t* stages = smem;
     float* merge_o = reinterpret_cast<float*>(smem + C::STAGES_BYTES);
     __shared__ int s_phys[W][DEPTH];
-    __shared__ float s_m[W][MAXR], s_l[W][MAXR], s_M[MAXR], s_L[MAXR];
+    __shared__ float s_m[W][RB], s_l[W][RB], s_M[RB], s_L[RB];
     __shared__ int s_plan[8];
     __shared__ int s_last;
 
@@ -220,16 +276,18 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
             const int b = b0 + lane;
             int n = 0;
             if (b < p.batch) {
-                const int len = load_len(p, b);
-                n = (len + UNIT - 1) / UNIT * p.Hkv * p.HB;
-                if (len == 0 && (b % gridDim.x) == blockIdx.x && is_decode_entry(p, b)) {
+                const SeqShape sh = seq_shape(p, b);
+                n = seq_units(p, sh);
+                if (sh.qlen > 0 && sh.len == 0 && (b % gridDim.x) == blockIdx.x) {
                     // empty sequence: defined result, out = 0, lse = -inf
-                    const size_t row = q_row(p, b);
-                    for (int h = 0; h < p.Hq; ++h) {
-                        uint4* o = reinterpret_cast<uint4*>(p.out + (row * p.Hq + h) * D);
-                        for (int c = 0; c < D / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
-                        if (p.lse) p.lse[row * p.Hq + h] = -INFINITY;
-                    }
+                    const size_t row0 = q_row(p, b);
+                    for (int i = 0; i < sh.qlen; ++i)
+                        for (int h = 0; h < p.Hq; ++h) {
+                            const size_t row = (row0 + i) * p.Hq + h;
+                            uint4* o = reinterpret_cast<uint4*>(p.out + row * D);
+                            for (int c = 0; c < D / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
+                            if (p.lse) p.lse[row] = -INFINITY;
+                        }
                 }
             }
             T += warp_sum_int(n);
@@ -243,7 +301,7 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
             int P = 0;
             for (int b0 = 0; b0 < p.batch && sb < 0; b0 += 32) {
                 const int b = b0 + lane;
-                const int n = (b < p.batch) ? (load_len(p, b) + UNIT - 1) / UNIT * p.Hkv * p.HB : 0;
+                const int n = (b < p.batch) ? seq_units(p, seq_shape(p, b)) : 0;
                 const int incl = warp_incl_scan(n);
                 const int tot = __shfl_sync(0xffffffffu, incl, 31);
                 if (U0 < P + tot) {
@@ -272,17 +330,12 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
     // segment holding U0
     Seg seg0;
     {
-        const int b = s_plan[4];
-        const int len = load_len(p, b);
-        const int n = (len + UNIT - 1) / UNIT;
-        const int idx = (U0 - s_plan[5]) / n;  // (g, hb) index within sequence b
-        seg0.b = b;
-        seg0.g = idx / p.HB;
-        seg0.hb = idx - seg0.g * p.HB;
-        seg0.len = len;
-        seg0.n = n;
-        seg0.start = s_plan[5] + idx * n;
-        seg0.end = seg0.start + n;
+        seg_set_seq(seg0, p, s_plan[4]);
+        const int idx = (U0 - s_plan[5]) / seg0.n;  // (g, sb) index within sequence b
+        seg0.g = idx / seg0.sh.SB;
+        seg0.sb = idx - seg0.g * seg0.sh.SB;
+        seg0.start = s_plan[5] + idx * seg0.n;
+        seg0.end = seg0.start + seg0.n;
     }
 
     const uint64_t policy = policy_evict_first();
@@ -321,16 +374,28 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
     int pa_ = U0;
     while (true) {
         const int pe = min(U1, cs.end);
-        const int rows = min(p.R, p.group - cs.hb * p.R);
-        const int h0 = cs.g * p.group + cs.hb * p.R;
+        const int nrb = 1 << cs.sh.nrb_shift;
+        const int rbase = (pa_ - cs.start) & (nrb - 1);  // row block of warp 0 in this piece
+        const int wrb = (rbase + warp) & (nrb - 1);      // this warp's row block
+        const int row_sb = cs.sb * cs.sh.RSB;             // first row of the segment
+        const int rows_sb = min(cs.sh.RSB, cs.sh.qlen * p.group - row_sb);
+        const int my_rows = max(0, min(cs.sh.R, rows_sb - wrb * cs.sh.R));
+        const int qlast = cs.sh.len - cs.sh.qlen;  // position of query token 0
 
-        // Q fragments of the head block (rows >= `rows` are zero)
+        // Q fragments of this warp's rows (rows >= my_rows are zero) and the
+        // number of keys each of the lane's two rows may see
         uint32_t qa[KSTEPS][4];
+        int lim0 = cs.sh.len, lim1 = cs.sh.len;
         {
             const size_t qrow = q_row(p, cs.b);
-            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(p.q + (qrow * p.Hq + h0 + qr) * D);
-            const uint32_t* q8 = reinterpret_cast<const uint32_t*>(p.q + (qrow * p.Hq + h0 + qr + 8) * D);
-            const bool r0ok = qr < rows, r8ok = qr + 8 < rows;
+            const bool r0ok = qr < my_rows, r8ok = qr + 8 < my_rows;
+            const int f0 = row_sb + wrb * cs.sh.R + qr, f8 = f0 + 8;
+            const int i0 = f0 / p.group, i8 = f8 / p.group;
+            const int h0 = cs.g * p.group + (f0 - i0 * p.group), h8 = cs.g * p.group + (f8 - i8 * p.group);
+            if (r0ok) lim0 = qlast + i0 + 1;
+            if (r8ok) lim1 = qlast + i8 + 1;
+            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(p.q + ((qrow + (r0ok ? i0 : 0)) * p.Hq + h0) * D);
+            const uint32_t* q8 = reinterpret_cast<const uint32_t*>(p.q + ((qrow + (r8ok ? i8 : 0)) * p.Hq + h8) * D);
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
                 const int c = (kk * 16 + qc) >> 1;
@@ -353,7 +418,8 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
             uint8_t* sk = my_stages + st * C::STAGE_BYTES;
             uint8_t* sv = sk + C::UNIT_BYTES;
             if (phys >= 0) {
-                const int valid = min(UNIT, cs.len - (u - cs.start) * UNIT);
+                const int tok0 = ((u - cs.start) >> cs.sh.nrb_shift) * UNIT;
+                const int vis0 = lim0 - tok0, vis1 = lim1 - tok0;  // keys of this unit each row sees
                 const uint32_t kb = smem_u32(sk), vb = smem_u32(sv);
                 // S = Q K^T  (16 heads x 16 keys)
                 // two independent accumulator chains (even / odd k-steps) halve the
@@ -379,14 +445,14 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
                 for (int j = 0; j < 2; ++j)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) s[j][e] += s2[j][e];
-                // scale to log2 domain, mask keys >= valid
+                // scale to log2 domain, mask keys past the sequence end or the row's position
                 float x[2][4];
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int key = j * 8 + qc + (e & 1);
-                        x[j][e] = key < valid ? s[j][e] * p.scale_log2 : -INFINITY;
+                        x[j][e] = key < ((e & 2) ? vis1 : vis0) ? s[j][e] * p.scale_log2 : -INFINITY;
                     }
                 }
                 float rm0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
@@ -396,16 +462,19 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
                 rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 1));
                 rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 2));
                 const float mn0 = fmaxf(m0, rm0), mn1 = fmaxf(m1, rm1);
-                const float a0 = ex2(m0 - mn0), a1 = ex2(m1 - mn1);  // 0 when m was -inf
+                // a row with no visible key yet keeps m = -inf; measure from 0 then so
+                // that nothing computes -inf - (-inf)
+                const float mr0 = mn0 == -INFINITY ? 0.f : mn0, mr1 = mn1 == -INFINITY ? 0.f : mn1;
+                const float a0 = ex2(m0 - mr0), a1 = ex2(m1 - mr1);  // 0 when m was -inf
                 m0 = mn0;
                 m1 = mn1;
                 float pr[2][4];
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    pr[j][0] = ex2(x[j][0] - mn0);
-                    pr[j][1] = ex2(x[j][1] - mn0);
-                    pr[j][2] = ex2(x[j][2] - mn1);
-                    pr[j][3] = ex2(x[j][3] - mn1);
+                    pr[j][0] = ex2(x[j][0] - mr0);
+                    pr[j][1] = ex2(x[j][1] - mr0);
+                    pr[j][2] = ex2(x[j][2] - mr1);
+                    pr[j][3] = ex2(x[j][3] - mr1);
                 }
                 l0 = l0 * a0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
                 l1 = l1 * a1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
@@ -446,7 +515,7 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
             }
         }
 
-        // ---- merge the W warp states of this segment piece (fixed order)
+        // ---- merge the states of the warps that hold the same row block (fixed order)
         l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
         l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
@@ -458,40 +527,47 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
             s_l[warp][qr + 8] = l1;
         }
         __syncthreads();
-        {
-            float M0 = -INFINITY, M1 = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < W; ++w) {
-                M0 = fmaxf(M0, s_m[w][qr]);
-                M1 = fmaxf(M1, s_m[w][qr + 8]);
-            }
-            float L0 = 0.f, L1 = 0.f;
-#pragma unroll
-            for (int w = 0; w < W; ++w) {
-                const float mw0 = s_m[w][qr], mw1 = s_m[w][qr + 8];
-                L0 += (mw0 == -INFINITY) ? 0.f : s_l[w][qr] * ex2(mw0 - M0);
-                L1 += (mw1 == -INFINITY) ? 0.f : s_l[w][qr + 8] * ex2(mw1 - M1);
-            }
-            const float sc0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - M0);
-            const float sc1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - M1);
-            if (warp == 0 && (lane & 3) == 0) {
-                s_M[qr] = M0;
-                s_L[qr] = L0;
-                s_M[qr + 8] = M1;
-                s_L[qr + 8] = L1;
+        const int c0 = cs.start / chunk, c1 = (cs.end - 1) / chunk;
+        const int sid = (cs.b * p.Hkv + cs.g) * p.SBmax + cs.sb;
+        const bool single = (c0 == c1);
+        const size_t orow = q_row(p, cs.b);
+        for (int r = 0; r < nrb; ++r) {
+            const int wfirst = (r - rbase) & (nrb - 1);  // lowest warp holding row block r
+            if (wrb == r) {
+                float M0 = -INFINITY, M1 = -INFINITY;
+                for (int w = wfirst; w < W; w += nrb) {
+                    M0 = fmaxf(M0, s_m[w][qr]);
+                    M1 = fmaxf(M1, s_m[w][qr + 8]);
+                }
+                float L0 = 0.f, L1 = 0.f;
+                for (int w = wfirst; w < W; w += nrb) {
+                    const float mw0 = s_m[w][qr], mw1 = s_m[w][qr + 8];
+                    L0 += (mw0 == -INFINITY) ? 0.f : s_l[w][qr] * ex2(mw0 - M0);
+                    L1 += (mw1 == -INFINITY) ? 0.f : s_l[w][qr + 8] * ex2(mw1 - M1);
+                }
+                const float sc0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - M0);
+                const float sc1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - M1);
+                if (warp == wfirst && (lane & 3) == 0) {
+                    s_M[qr] = M0;
+                    s_L[qr] = L0;
+                    s_M[qr + 8] = M1;
+                    s_L[qr + 8] = L1;
+                }
+                m0 = sc0;  // m and l are not needed any more: keep the scale factors
+                m1 = sc1;
             }
             // warps add their rescaled O into one buffer in a fixed order
 #pragma unroll 1
-            for (int w = 0; w < W; ++w) {
+            for (int w = wfirst; w < W; w += nrb) {
                 if (warp == w) {
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         const int col = n * 8 + qc;
                         float2* a0 = reinterpret_cast<float2*>(merge_o + qr * C::MSTRIDE + col);
                         float2* a1 = reinterpret_cast<float2*>(merge_o + (qr + 8) * C::MSTRIDE + col);
-                        float2 v0 = make_float2(o[n][0] * sc0, o[n][1] * sc0);
-                        float2 v1 = make_float2(o[n][2] * sc1, o[n][3] * sc1);
-                        if (w > 0) {
+                        float2 v0 = make_float2(o[n][0] * m0, o[n][1] * m0);
+                        float2 v1 = make_float2(o[n][2] * m1, o[n][3] * m1);
+                        if (w > wfirst) {
                             const float2 p0 = *a0, p1 = *a1;
                             v0.x += p0.x;
                             v0.y += p0.y;
@@ -504,30 +580,30 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
                 }
                 __syncthreads();
             }
-        }
-        const int c0 = cs.start / chunk, c1 = (cs.end - 1) / chunk;
-        const int sid = (cs.b * p.Hkv + cs.g) * p.HB + cs.hb;
-        const bool single = (c0 == c1);
-        const size_t orow = q_row(p, cs.b);
-        for (int idx = tid; idx < rows * (D / 4); idx += W * 32) {
-            const int r = idx / (D / 4);
-            const int d4 = idx - r * (D / 4);
-            const float4 acc = *reinterpret_cast<const float4*>(merge_o + r * C::MSTRIDE + d4 * 4);
-            const float L = s_L[r];
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            if (single) {
-                uint2 ob;
-                ob.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-                ob.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-                *reinterpret_cast<uint2*>(p.out + (orow * p.Hq + h0 + r) * D + d4 * 4) = ob;
-                if (p.lse != nullptr && d4 == 0)
-                    p.lse[orow * p.Hq + h0 + r] = L > 0.f ? (s_M[r] + lg2(L)) * kLn2 : -INFINITY;
-            } else {
-                const size_t slot = (size_t)blockIdx.x + sid;
-                *reinterpret_cast<float4*>(p.ws_o + (slot * MAXR + r) * D + d4 * 4) =
-                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-                if (d4 == 0) p.ws_lse[slot * MAXR + r] = L > 0.f ? s_M[r] + lg2(L) : -INFINITY;
+            const int nr = max(0, min(cs.sh.R, rows_sb - r * cs.sh.R));
+            for (int idx = tid; idx < nr * (D / 4); idx += W * 32) {
+                const int rr = idx / (D / 4);
+                const int d4 = idx - rr * (D / 4);
+                const float4 acc = *reinterpret_cast<const float4*>(merge_o + rr * C::MSTRIDE + d4 * 4);
+                const float L = s_L[rr];
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                if (single) {
+                    const int f = row_sb + r * cs.sh.R + rr;
+                    const int i = f / p.group;
+                    const size_t orr = (orow + i) * p.Hq + cs.g * p.group + (f - i * p.group);
+                    uint2 ob;
+                    ob.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+                    ob.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+                    *reinterpret_cast<uint2*>(p.out + orr * D + d4 * 4) = ob;
+                    if (p.lse != nullptr && d4 == 0) p.lse[orr] = L > 0.f ? (s_M[rr] + lg2(L)) * kLn2 : -INFINITY;
+                } else {
+                    const size_t srow = ((size_t)blockIdx.x + sid) * p.RS + r * RB + rr;
+                    *reinterpret_cast<float4*>(p.ws_o + srow * D + d4 * 4) =
+                        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                    if (d4 == 0) p.ws_lse[srow] = L > 0.f ? s_M[rr] + lg2(L) : -INFINITY;
+                }
             }
+            __syncthreads();  // the merge buffer and s_M / s_L are reused by the next row block
         }
         if (!single) {
             __threadfence();
@@ -540,20 +616,23 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
             if (s_last) {
                 // last CTA of this segment: merge all partials in slot order
                 __threadfence();
-                for (int idx = tid; idx < rows * (D / 4); idx += W * 32) {
-                    const int r = idx / (D / 4);
-                    const int d4 = idx - r * (D / 4);
+                for (int idx = tid; idx < nrb * RB * (D / 4); idx += W * 32) {
+                    const int rw = idx / (D / 4);
+                    const int d4 = idx - rw * (D / 4);
+                    const int r = rw / RB, rr = rw - r * RB;
+                    if (rr >= min(cs.sh.R, rows_sb - r * cs.sh.R)) continue;
                     float M = -INFINITY;
-                    for (int c = c0; c <= c1; ++c) M = fmaxf(M, __ldcg(p.ws_lse + ((size_t)c + sid) * MAXR + r));
+                    for (int c = c0; c <= c1; ++c)
+                        M = fmaxf(M, __ldcg(p.ws_lse + ((size_t)c + sid) * p.RS + rw));
                     float L = 0.f;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (M != -INFINITY) {
                         for (int c = c0; c <= c1; ++c) {
-                            const size_t slot = (size_t)c + sid;
-                            const float lc = __ldcg(p.ws_lse + slot * MAXR + r);
+                            const size_t srow = ((size_t)c + sid) * p.RS + rw;
+                            const float lc = __ldcg(p.ws_lse + srow);
                             if (lc == -INFINITY) continue;
                             const float wgt = ex2(lc - M);
-                            const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (slot * MAXR + r) * D) + d4);
+                            const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws_o + srow * D) + d4);
                             L += wgt;
                             acc.x += wgt * v.x;
                             acc.y += wgt * v.y;
@@ -562,12 +641,14 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
                         }
                     }
                     const float inv = L > 0.f ? 1.f / L : 0.f;
+                    const int f = row_sb + r * cs.sh.R + rr;
+                    const int i = f / p.group;
+                    const size_t orr = (orow + i) * p.Hq + cs.g * p.group + (f - i * p.group);
                     uint2 ob;
                     ob.x = pack_bf16x2(acc.x * inv, acc.y * inv);
                     ob.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-                    *reinterpret_cast<uint2*>(p.out + (orow * p.Hq + h0 + r) * D + d4 * 4) = ob;
-                    if (p.lse != nullptr && d4 == 0)
-                        p.lse[orow * p.Hq + h0 + r] = L > 0.f ? (M + lg2(L)) * kLn2 : -INFINITY;
+                    *reinterpret_cast<uint2*>(p.out + orr * D + d4 * 4) = ob;
+                    if (p.lse != nullptr && d4 == 0) p.lse[orr] = L > 0.f ? (M + lg2(L)) * kLn2 : -INFINITY;
                 }
                 if (tid == 0) p.counters[sid] = 0;  // leave the workspace ready for the next call
             }
@@ -581,49 +662,74 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
     cp_async_wait_group<0>();  // never exit with a copy still landing in shared memory
 }
 
-// Workspace layout: [counters: S int32][ws_lse: slots x MAXR f32][ws_o: slots x MAXR x D f32]
+// Workspace layout: [counters: segs int32][ws_lse: slots x RS f32][ws_o: slots x RS x D f32]
 struct WsLayout {
     size_t counters, lse, o, total;
 };
 
-inline WsLayout ws_layout(int slots, int segs, int D) {
+inline WsLayout ws_layout(int slots, int segs, int RS, int D) {
     WsLayout w;
     w.counters = 0;
     w.lse = align_up((size_t)segs * 4, 256);
-    w.o = w.lse + align_up((size_t)slots * MAXR * 4, 256);
-    w.total = w.o + (size_t)slots * MAXR * D * 4;
+    w.o = w.lse + align_up((size_t)slots * RS * 4, 256);
+    w.total = w.o + (size_t)slots * RS * D * 4;
     return w;
 }
 
-inline int head_blocks(int group) { return (group + MAXR - 1) / MAXR; }
+// Largest segment count per (sequence, KV head) and rows per workspace slot
+// over every q_len <= qmax (the device's seq_shape never exceeds them).
+struct Bounds {
+    int SBmax, RS;
+};
+
+inline Bounds bounds(int group, int qmax) {
+    const int rows = group * qmax;
+    Bounds bd;
+    bd.SBmax = (rows + SBR - 1) / SBR;
+    const int nrb = rows > SBR ? 4 : (rows + RB - 1) / RB;
+    bd.RS = RB * (nrb <= 1 ? 1 : (nrb == 2 ? 2 : 4));
+    return bd;
+}
+
+inline size_t ws_bytes(int sm_count, int batch, int num_q_heads, int num_kv_heads, int head_dim, int qmax) {
+    const Bounds bd = bounds(num_q_heads / num_kv_heads, qmax);
+    const int segs = batch * num_kv_heads * bd.SBmax;
+    const int slots = sm_count * CTAS_PER_SM + segs;
+    return ws_layout(slots, segs, bd.RS, head_dim).total;
+}
 
 }  // namespace dec
 }  // namespace pa
 
 using namespace pa;
 
-extern "C" size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim) {
+extern "C" size_t pa_decode_multiquery_workspace_bytes(int batch, int max_q_len, int num_q_heads, int num_kv_heads,
+                                                       int head_dim) {
     if (batch <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads) return 0;
+    if (max_q_len < 1 || max_q_len > kDecodeMaxQ || num_q_heads / num_kv_heads > 128) return 0;
     DeviceInfo dev;
     if (current_device(&dev) != PA_OK) return 0;
-    const int group = num_q_heads / num_kv_heads;
-    const int segs = batch * num_kv_heads * dec::head_blocks(group);
-    const int slots = dev.sm_count * dec::CTAS_PER_SM + segs;
-    return dec::ws_layout(slots, segs, head_dim).total;
+    return dec::ws_bytes(dev.sm_count, batch, num_q_heads, num_kv_heads, head_dim, max_q_len);
+}
+
+extern "C" size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim) {
+    return pa_decode_multiquery_workspace_bytes(batch, 1, num_q_heads, num_kv_heads, head_dim);
 }
 
 namespace pa {
 namespace dec {
 
 // Launch the split-K decode.  cu_q == nullptr: one query row per sequence
-// (row b).  Otherwise (a mixed prefill + decode call): only sequences with
-// exactly one query row are served, reading/writing row cu_q[b].
+// (row b).  Otherwise entries with 1 <= q_len <= qmax are served (rows
+// cu_q[b] ..), q_len in (qmax, qcap] is reported as PA_ERR_BAD_LEN and
+// longer entries are left to the prefill kernel.
 int launch_decode(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool, int num_pages,
                   const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
-                  const int32_t* cu_q, int batch, int max_seq_len, int page_size, int num_q_heads,
-                  int num_kv_heads, int head_dim, float softmax_scale, void* workspace, size_t workspace_bytes,
-                  int32_t* status, void* stream) {
-    if (batch < 0 || max_seq_len < 0) return PA_ERR_SHAPE;
+                  const int32_t* cu_q, int total_q, int qmax, int qcap, int batch, int max_seq_len, int page_size,
+                  int num_q_heads, int num_kv_heads, int head_dim, float softmax_scale, void* workspace,
+                  size_t workspace_bytes, int32_t* status, void* stream) {
+    if (batch < 0 || max_seq_len < 0 || total_q < 0) return PA_ERR_SHAPE;
+    if (qmax < 1 || qmax > kDecodeMaxQ || (cu_q == nullptr && qmax != 1)) return PA_ERR_SHAPE;
     int rc = check_common_shapes(page_size, num_q_heads, num_kv_heads, head_dim);
     if (rc != PA_OK) return rc;
     if (batch == 0) return PA_OK;
@@ -639,26 +745,29 @@ int launch_decode(void* out, float* lse, const void* q, const void* k_pool, cons
     if (rc != PA_OK) return rc;
 
     const int group = num_q_heads / num_kv_heads;
-    const int HB = dec::head_blocks(group);
-    const int R = (group + HB - 1) / HB;
-    const int segs = batch * num_kv_heads * HB;
-    const long long units_upper = (long long)segs * ((max_seq_len + dec::UNIT - 1) / dec::UNIT);
+    const Bounds bd = bounds(group, qmax);
+    const int nrb_max = bd.RS / RB;
+    const long long segs = (long long)batch * num_kv_heads * bd.SBmax;
+    const long long units_upper = segs * nrb_max * ((max_seq_len + UNIT - 1) / UNIT);
     // every unit index and grid * chunk must fit in int32
-    if ((long long)segs * ((max_pages_per_seq * (long long)page_size + dec::UNIT - 1) / dec::UNIT) +
-            (long long)dev.sm_count * dec::CTAS_PER_SM * dec::MIN_CHUNK >=
+    if (segs * nrb_max * ((max_pages_per_seq * (long long)page_size + UNIT - 1) / UNIT) +
+            (long long)dev.sm_count * CTAS_PER_SM * MIN_CHUNK >=
         (1ll << 31))
         return PA_ERR_SHAPE;
-    const int gmax = dev.sm_count * dec::CTAS_PER_SM;
-    long long g = (units_upper + dec::MIN_CHUNK - 1) / dec::MIN_CHUNK;
+    const int gmax = dev.sm_count * CTAS_PER_SM;
+    long long g = (units_upper + MIN_CHUNK - 1) / MIN_CHUNK;
     if (g < 1) g = 1;
     const int grid = (int)(g < gmax ? g : gmax);
 
-    const int slots = gmax + segs;
-    const dec::WsLayout wl = dec::ws_layout(slots, segs, head_dim);
+    const int slots = gmax + (int)segs;
+    const WsLayout wl = ws_layout(slots, (int)segs, bd.RS, head_dim);
     if (workspace == nullptr) return PA_ERR_WORKSPACE;
     if (workspace_bytes < wl.total) return PA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_WORKSPACE;
-
+    // the counter region [0, wl.lse) is what must be zero; partials start right after it, so two calls
+    // with the same region size never write each other's counters
+    rc = prepare_counters(workspace, wl.lse, (uint64_t)wl.lse, stream);
+    if (rc != PA_OK) return rc;
 
     dec::Params prm;
     prm.out = static_cast<__nv_bfloat16*>(out);
@@ -669,6 +778,11 @@ int launch_decode(void* out, float* lse, const void* q, const void* k_pool, cons
     prm.block_table = block_table;
     prm.seq_lens = seq_lens;
     prm.cu_q = cu_q;
+    prm.total_q = cu_q == nullptr ? batch : total_q;
+    prm.qmax = qmax;
+    prm.qcap = qcap;
+    prm.SBmax = bd.SBmax;
+    prm.RS = bd.RS;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     prm.counters = reinterpret_cast<int32_t*>(ws + wl.counters);
     prm.ws_lse = reinterpret_cast<float*>(ws + wl.lse);
@@ -682,8 +796,6 @@ int launch_decode(void* out, float* lse, const void* q, const void* k_pool, cons
     prm.Hq = num_q_heads;
     prm.Hkv = num_kv_heads;
     prm.group = group;
-    prm.HB = HB;
-    prm.R = R;
     prm.scale_log2 = softmax_scale * kLog2e;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -710,8 +822,23 @@ extern "C" int attn_decode_paged(void* out, float* lse, const void* q, const voi
                                  int num_kv_heads, int head_dim, float softmax_scale, void* workspace,
                                  size_t workspace_bytes, int32_t* status, void* stream) {
     return dec::launch_decode(out, lse, q, k_pool, v_pool, num_pages, block_table, max_pages_per_seq, seq_lens,
-                              nullptr, batch, max_seq_len, page_size, num_q_heads, num_kv_heads, head_dim,
-                              softmax_scale, workspace, workspace_bytes, status, stream);
+                              nullptr, batch, 1, 1, batch, max_seq_len, page_size, num_q_heads, num_kv_heads,
+                              head_dim, softmax_scale, workspace, workspace_bytes, status, stream);
+}
+
+extern "C" int attn_decode_multiquery_paged(void* out, float* lse, const void* q, const void* k_pool,
+                                            const void* v_pool, int num_pages, const int32_t* block_table,
+                                            int max_pages_per_seq, const int32_t* cu_seqlens_q,
+                                            const int32_t* seq_lens, int batch, int total_q, int max_q_len,
+                                            int max_seq_len, int page_size, int num_q_heads, int num_kv_heads,
+                                            int head_dim, float softmax_scale, void* workspace,
+                                            size_t workspace_bytes, int32_t* status, void* stream) {
+    if (max_q_len < 1 || max_q_len > kDecodeMaxQ) return PA_ERR_SHAPE;
+    if (batch > 0 && cu_seqlens_q == nullptr) return PA_ERR_NULL;
+    return dec::launch_decode(out, lse, q, k_pool, v_pool, num_pages, block_table, max_pages_per_seq, seq_lens,
+                              cu_seqlens_q, total_q, max_q_len, INT_MAX, batch, max_seq_len, page_size,
+                              num_q_heads, num_kv_heads, head_dim, softmax_scale, workspace, workspace_bytes,
+                              status, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -774,7 +901,7 @@ extern "C" int attn_decode_paged_noalloc(void* out, float* lse, const void* q, c
     if (rc != PA_OK) return rc;
     // The arrival counters must start at zero; an earlier call that stopped
     // on a device error may have left them dirty, so clear them every call.
-    const int segs = batch * num_kv_heads * dec::head_blocks(num_q_heads / num_kv_heads);
+    const int segs = batch * num_kv_heads * dec::bounds(num_q_heads / num_kv_heads, 1).SBmax;
     const size_t counter_bytes = align_up((size_t)segs * 4, 256);
     if (cudaMemsetAsync(scratch, 0, counter_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PA_ERR_CUDA;

@@ -49,15 +49,29 @@ inline int check_common_shapes(int page_size, int num_q_heads, int num_kv_heads,
     return PA_OK;
 }
 
+// Entries with q_len <= kDecodeMaxQ are served by the split-K decode kernel
+// (also inside a mixed prefill + decode call); longer ones by the prefill kernel.
+constexpr int kDecodeMaxQ = 8;
+
 namespace dec {
-// Split-K decode launcher (decode.cu); cu_q != nullptr serves the q_len == 1
-// entries of a mixed prefill + decode call.
+// Split-K decode launcher (decode.cu).  cu_q == nullptr: one query row per
+// sequence.  Otherwise the entries with 1 <= q_len <= qmax are served, q_len
+// in (qmax, qcap] is reported as an error and longer entries are skipped.
 int launch_decode(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool, int num_pages,
                   const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
-                  const int32_t* cu_q, int batch, int max_seq_len, int page_size, int num_q_heads,
-                  int num_kv_heads, int head_dim, float softmax_scale, void* workspace, size_t workspace_bytes,
-                  int32_t* status, void* stream);
+                  const int32_t* cu_q, int total_q, int qmax, int qcap, int batch, int max_seq_len, int page_size,
+                  int num_q_heads, int num_kv_heads, int head_dim, float softmax_scale, void* workspace,
+                  size_t workspace_bytes, int32_t* status, void* stream);
 }  // namespace dec
+
+// The split-K arrival counters at the start of a workspace must be zero when
+// a call starts.  Every successful call leaves its own counters zero, but a
+// workspace whose last call had a different layout may hold that call's
+// partial outputs where this call's counters are.  The library remembers the
+// last layout (the size of the counter region) per workspace address and,
+// when it changes (or on first use), clears `counter_bytes` with one
+// asynchronous memset on `stream`.
+int prepare_counters(void* workspace, size_t counter_bytes, uint64_t layout, void* stream);
 
 // Set the dynamic shared-memory limit of a kernel once per device.
 int set_smem_limit_once(const void* kernel, int bytes, int device, int slot);

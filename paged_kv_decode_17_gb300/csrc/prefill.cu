@@ -184,12 +184,12 @@ __device__ __forceinline__ int seq_tiles(const int32_t* cu_q, const int32_t* seq
         report(status, PA_ERR_BAD_LEN);
         return 0;
     }
-    if (q_len <= 1) return 0;  // q_len == 1 entries go to the split-K decode kernel
+    if (q_len <= kDecodeMaxQ) return 0;  // short query blocks go to the split-K decode kernel
     return (q_len + BM - 1) / BM;
 }
 
 // ---------------------------------------------------------------------------------- plan
-// List every (sequence, query tile) of entries with q_len >= 2, sorted by the number
+// List every (sequence, query tile) of entries with q_len > kDecodeMaxQ, sorted by the number
 // of 128-key tiles the tile attends (counting sort, heaviest first).  One CTA.
 __global__ void __launch_bounds__(PLAN_THREADS) prefill_plan_kernel(const int32_t* __restrict__ cu_q,
                                                                      const int32_t* __restrict__ seq_lens,
@@ -692,7 +692,7 @@ using namespace pa;
 
 extern "C" size_t pa_prefill_workspace_bytes(int batch, int total_q, int num_q_heads, int num_kv_heads,
                                              int head_dim) {
-    const size_t dec = pa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim);
+    const size_t dec = pa_decode_multiquery_workspace_bytes(batch, kDecodeMaxQ, num_q_heads, num_kv_heads, head_dim);
     if (dec == 0 || total_q < 0) return 0;
     return align_up(dec, 256) + pf::plan_bytes(batch, total_q);
 }
@@ -759,14 +759,17 @@ extern "C" int attn_prefill_varlen_causal(void* out, float* lse, const void* q, 
     if (workspace == nullptr || need == 0) return PA_ERR_WORKSPACE;
     if (workspace_bytes < need) return PA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_WORKSPACE;
-    const size_t dec_bytes = pa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim);
+    const size_t dec_bytes =
+        pa_decode_multiquery_workspace_bytes(batch, kDecodeMaxQ, num_q_heads, num_kv_heads, head_dim);
 
-    // decode rows (q_len == 1) of a mixed step: split-K over their KV
+    // decode entries (q_len <= kDecodeMaxQ) of a mixed step: split-K over their KV
+    const int dec_qmax = max_q_len < 1 ? 1 : (max_q_len < kDecodeMaxQ ? max_q_len : kDecodeMaxQ);
     rc = dec::launch_decode(out, lse, q, k_pool, v_pool, num_pages, block_table, max_pages_per_seq, seq_lens,
-                            cu_seqlens_q, batch, max_seq_len, page_size, num_q_heads, num_kv_heads, head_dim,
-                            softmax_scale, workspace, dec_bytes, status, stream);
+                            cu_seqlens_q, total_q, dec_qmax, kDecodeMaxQ, batch, max_seq_len, page_size,
+                            num_q_heads, num_kv_heads, head_dim, softmax_scale, workspace, dec_bytes, status,
+                            stream);
     if (rc != PA_OK) return rc;
-    if (max_q_len < 2) return PA_OK;  // no entry needs the prefill kernel
+    if (max_q_len <= kDecodeMaxQ) return PA_OK;  // no entry needs the prefill kernel
 
     const int group = num_q_heads / num_kv_heads;
     const int pairs = (group + 1) / 2;

@@ -63,6 +63,12 @@ def decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head
     return int(_lib.load().pa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim))
 
 
+def decode_multiquery_workspace_bytes(batch: int, max_q_len: int, num_q_heads: int, num_kv_heads: int,
+                                      head_dim: int) -> int:
+    return int(_lib.load().pa_decode_multiquery_workspace_bytes(batch, max_q_len, num_q_heads, num_kv_heads,
+                                                                head_dim))
+
+
 def prefill_workspace_bytes(batch: int, total_q: int, num_q_heads: int, num_kv_heads: int, head_dim: int) -> int:
     return int(_lib.load().pa_prefill_workspace_bytes(batch, total_q, num_q_heads, num_kv_heads, head_dim))
 
@@ -157,6 +163,60 @@ def attn_decode_paged(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tenso
                                float(softmax_scale), workspace.ptr, workspace.nbytes, _ptr(status),
                                _stream_handle(stream))
     _lib.check(rc, "attn_decode_paged")
+    return (out, lse) if return_lse else out
+
+
+def attn_decode_multiquery_paged(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                                 block_table: torch.Tensor, cu_seqlens_q: torch.Tensor, seq_lens: torch.Tensor,
+                                 softmax_scale: Optional[float] = None, *, max_q_len: Optional[int] = None,
+                                 max_seq_len: Optional[int] = None, out: Optional[torch.Tensor] = None,
+                                 lse: Optional[torch.Tensor] = None, return_lse: bool = False,
+                                 workspace: Optional[Workspace] = None, status: Optional[torch.Tensor] = None,
+                                 stream=None):
+    """Multi-query decode: 1..8 query rows per sequence, causal inside the block.
+
+    q [total_q][Hq][D] bf16; cu_seqlens_q [B+1] int32; seq_lens [B] int32
+    (total keys, the query rows' own K/V already written).  ``max_q_len``
+    (1..8, default min(8, total_q)) is a host upper bound of the per-entry
+    row counts; it sizes the workspace and the launch.
+    """
+    lib = _lib.load()
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pool, "k_pool", torch.bfloat16, 4)
+    _need(v_pool, "v_pool", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    Tq, Hq, D = q.shape
+    P, Hkv, ps, D2 = k_pool.shape
+    B = seq_lens.shape[0]
+    if D2 != D or v_pool.shape != k_pool.shape:
+        raise ValueError("inconsistent head_dim / pool shapes")
+    if cu_seqlens_q.shape[0] != B + 1 or block_table.shape[0] != B:
+        raise ValueError("cu_seqlens_q must have batch+1 entries and block_table batch rows")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if max_seq_len is None:
+        max_seq_len = block_table.shape[1] * ps
+    if max_q_len is None:
+        max_q_len = max(1, min(8, Tq))
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.bfloat16, 3)
+    if return_lse and lse is None:
+        lse = torch.empty((Tq, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    need = int(lib.pa_decode_multiquery_workspace_bytes(B, int(max_q_len), Hq, Hkv, D)) if B > 0 else 0
+    if workspace is None:
+        workspace = _cached_ws("decode", need, q.device)
+    rc = lib.attn_decode_multiquery_paged(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_pool), _ptr(v_pool), P,
+                                          _ptr(block_table), block_table.shape[1], _ptr(cu_seqlens_q),
+                                          _ptr(seq_lens), B, Tq, int(max_q_len), int(max_seq_len), ps, Hq, Hkv, D,
+                                          float(softmax_scale), workspace.ptr, workspace.nbytes, _ptr(status),
+                                          _stream_handle(stream))
+    _lib.check(rc, "attn_decode_multiquery_paged")
     return (out, lse) if return_lse else out
 
 

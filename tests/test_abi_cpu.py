@@ -106,3 +106,23 @@ def test_ops_refuse_cpu_tensors():
     lens = torch.ones(2, dtype=torch.int32)
     with pytest.raises(ValueError, match="CUDA"):
         pa.attn_decode_paged(q, kp, kp, bt, lens)
+
+
+def test_multiquery_host_validation(lib):
+    f = lib.attn_decode_multiquery_paged
+    P = 1 << 20
+    # out, lse, q, k, v, num_pages, bt, maxp, cu, lens, batch, total_q, max_q_len, max_seq_len, ps, hq, hkv, d, ...
+    args = [P, None, P, P, P, 16, P, 8, P, P, 2, 8, 4, 100, 16, 4, 2, 64, 0.125, None, 0, None, None]
+    for bad_q in (0, 9):  # the block must hold 1..8 query rows
+        a = list(args)
+        a[12] = bad_q
+        assert f(*a) == -2
+    a = list(args)
+    a[8] = None  # cu_seqlens_q
+    assert f(*a) == -1
+    a = list(args)
+    a[15] = 3  # Hq not a multiple of Hkv
+    assert f(*a) == -2
+    a = list(args)
+    a[10], a[2] = 0, None  # empty batch: nothing to do
+    assert f(*a) == 0

@@ -95,6 +95,30 @@ def test_oracle_matches_torch_sdpa_fp64(name, seq_lens, q_lens):
             np.testing.assert_allclose(out[cu[b]:cu[b + 1], h, :], ref.numpy(), rtol=0, atol=1e-10)
 
 
+def test_multiquery_rows_are_truncated_decodes():
+    """A block of q_len query rows at the end of a sequence: row i is exactly a
+    one-row decode of the same sequence cut to seq_len - q_len + i + 1 keys
+    (causal inside the block, every earlier token visible).  Pins the
+    position offset of short query blocks against the oracle's decode."""
+    q_lens = [4, 8, 1, 3]
+    seq_lens = [40, 8, 17, 3]
+    case = workloads.make_paged_case("mq_pin", seq_lens, q_lens, 14, 2, 16, page_size=8, seed=41)
+    a = oracle_args(case)
+    out, lse = paged_attention(**a)
+    cu = case.cu_seqlens_q.tolist()
+    for b, (L, ql) in enumerate(zip(seq_lens, q_lens)):
+        for i in range(ql):
+            row = cu[b] + i
+            one = dict(a)
+            one["q_bits"] = a["q_bits"][row:row + 1]
+            one["block_table"] = a["block_table"][b:b + 1]
+            one["seq_lens"] = [L - ql + i + 1]
+            one["cu_seqlens_q"] = np.array([0, 1], dtype=np.int32)
+            o1, l1 = paged_attention(**one)
+            np.testing.assert_allclose(out[row], o1[0], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse[row], l1[0], rtol=0, atol=1e-12)
+
+
 def test_tiled_online_softmax_equals_untiled():
     rng = np.random.default_rng(3)
     for trial in range(20):

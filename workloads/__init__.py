@@ -286,6 +286,17 @@ def qwen7b_decode(seed: int = 1, device="cpu", batch: int = 32, ctx: int = 8192)
     )
 
 
+def qwen7b_multiquery(seed: int = 5, device="cpu", batch: int = 32, ctx: int = 8192, q_len: int = 4) -> PagedCase:
+    """The qwen7b_decode shape with a block of q_len query rows per sequence
+    (speculative-decode verification: the last q_len of the ctx tokens are
+    the proposed ones, their K/V already in the pages)."""
+    return make_paged_case(
+        "qwen7b_multiquery", seq_lens=[ctx] * batch, q_lens=[q_len] * batch, num_q_heads=28,
+        num_kv_heads=4, head_dim=128, page_size=16, num_pages=batch * (-(-ctx // 16)),
+        seed=seed, device=device,
+    )
+
+
 def llama8b_ragged_lens(seed: int = 2, batch: int = 64, max_len: int = 32768) -> List[int]:
     gen = torch.Generator().manual_seed(seed)
     return _uniform_ints(gen, 1, max_len, batch)
