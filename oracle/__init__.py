@@ -15,6 +15,8 @@ Modules
 ``attention``  materialised-score attention over gathered pages, and the
                K/V writeback scatter (the reference definitions).
 ``brute``      an independent scalar pure-Python restatement, for tiny inputs.
+``rope``       the rotary position embedding and RMS normalisation that the
+               fused writeback applies to K (and Q) rows, and bf16 rounding.
 ``tiled``      a CPU model of the online-softmax recurrence and of the
                log-sum-exp combine of split chunks, used to pin that the
                tiled/split algorithm equals the materialised one.
@@ -29,4 +31,12 @@ from .attention import (  # noqa: F401
     attention_rows,
     paged_attention,
     kv_write_paged,
+)
+from .rope import (  # noqa: F401
+    bf16_ulp,
+    rms_norm,
+    rope_angles,
+    rope_rotate_half,
+    rope_writeback_rows,
+    round_to_bf16_f64,
 )

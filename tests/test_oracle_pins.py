@@ -390,3 +390,82 @@ def test_planted_oracle_mistakes_are_caught(mutant):
     with np.errstate(all="ignore"):
         out, _ = mutant(**a)
     assert not (np.isfinite(out).all() and np.allclose(out, bout, atol=1e-6)), "planted mistake went unnoticed"
+
+
+# ------------------------------------------------------------------ rotary embedding / RMS norm
+def test_rope_position_zero_is_identity():
+    x = np.random.default_rng(50).standard_normal((3, 128))
+    np.testing.assert_array_equal(oracle.rope_rotate_half(x, 0, 10000.0), x)
+
+
+def test_rope_two_dims_is_a_plane_rotation():
+    """D = 2: one pair with frequency base**0 = 1, rotated by `pos` radians."""
+    x = np.array([0.3, -1.7])
+    for pos in (1, 5, 1000):
+        c, s = math.cos(pos), math.sin(pos)
+        want = np.array([0.3 * c + 1.7 * s, -1.7 * c + 0.3 * s])
+        np.testing.assert_allclose(oracle.rope_rotate_half(x, pos, 500.0), want, rtol=0, atol=1e-12)
+
+
+def test_rope_worked_example_rotate_half_pairing():
+    """D = 4, base 10000: pair 0 = dims (0, 2) turns by pos rad, pair 1 = dims
+    (1, 3) by pos * 10000**(-1/2) = pos / 100 rad.  Unit vectors show the pairing."""
+    e0 = np.array([1.0, 0.0, 0.0, 0.0])
+    e1 = np.array([0.0, 1.0, 0.0, 0.0])
+    np.testing.assert_allclose(oracle.rope_rotate_half(e0, 1, 10000.0),
+                               [math.cos(1.0), 0.0, math.sin(1.0), 0.0], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(oracle.rope_rotate_half(e1, 100, 10000.0),
+                               [0.0, math.cos(1.0), 0.0, math.sin(1.0)], rtol=0, atol=1e-12)
+
+
+def test_rope_preserves_pair_norms():
+    rng = np.random.default_rng(51)
+    x = rng.standard_normal(128)
+    y = oracle.rope_rotate_half(x, 12345, 1e6)
+    np.testing.assert_allclose(np.hypot(y[:64], y[64:]), np.hypot(x[:64], x[64:]), rtol=1e-13)
+
+
+def test_rope_scores_depend_only_on_relative_position():
+    """The defining property of rotary embeddings: <R(m) q, R(n) k> = <q, R(n - m) k>."""
+    rng = np.random.default_rng(52)
+    q, k = rng.standard_normal(64), rng.standard_normal(64)
+    for m, n in ((0, 7), (100, 37), (5000, 5003), (131071, 2)):
+        lhs = oracle.rope_rotate_half(q, m, 10000.0) @ oracle.rope_rotate_half(k, n, 10000.0)
+        rhs = q @ oracle.rope_rotate_half(k, n - m, 10000.0)
+        assert abs(lhs - rhs) <= 1e-9 * (1 + abs(rhs))
+
+
+def test_rms_norm_closed_forms():
+    np.testing.assert_allclose(oracle.rms_norm(np.array([3.0, 4.0]), None, 0.0),
+                               np.array([3.0, 4.0]) / math.sqrt(12.5), rtol=1e-15)
+    x = np.random.default_rng(53).standard_normal(128)
+    y = oracle.rms_norm(x, None, 0.0)
+    assert abs(np.mean(y * y) - 1.0) < 1e-13
+    np.testing.assert_allclose(oracle.rms_norm(7.5 * x, None, 0.0), y, rtol=1e-13)
+    w = np.linspace(0.5, 2.0, 128)
+    np.testing.assert_allclose(oracle.rms_norm(x, w, 1e-6), oracle.rms_norm(x, None, 1e-6) * w, rtol=1e-15)
+
+
+def test_bf16_rounding_ties_to_even():
+    # 1 + 2^-8 lies halfway between bf16 neighbours 1 and 1 + 2^-7: rounds to the even one (1)
+    v = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -2.0 - 2.0 ** -7, 1.0 + 2.0 ** -9, 3.0])
+    want = np.array([1.0, 1.0 + 2.0 ** -6, -2.0, 1.0, 3.0])
+    np.testing.assert_array_equal(oracle.round_to_bf16_f64(v), want)
+    np.testing.assert_array_equal(oracle.bf16_ulp(np.array([1.0, 1.5, 2.0, -0.75])),
+                                  [2.0 ** -7, 2.0 ** -7, 2.0 ** -6, 2.0 ** -8])
+
+
+def test_rope_writeback_rows_positions_and_norm_order():
+    """Row i of n new rows of a sequence of length L is rotated at L - n + i,
+    after its RMS norm (the rotation keeps the norm, so the normalised row's
+    mean square survives it)."""
+    rng = np.random.default_rng(54)
+    T, Hkv, D = 5, 2, 16
+    k = (rng.standard_normal((T, Hkv, D)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    cu, lens = [0, 3, 5], [10, 2]
+    w = np.full(D, 0x3F80, dtype=np.uint16)  # bf16 1.0
+    out, _, pos = oracle.rope_writeback_rows(k, None, cu, lens, 10000.0, k_norm_weight_bits=w, eps=0.0)
+    np.testing.assert_array_equal(pos, [7, 8, 9, 0, 1])
+    np.testing.assert_allclose(np.mean(out * out, axis=-1), 1.0, rtol=1e-12)
+    kf = oracle.bf16_bits_to_f64(k)
+    np.testing.assert_allclose(out[3], oracle.rms_norm(kf[3], None, 0.0), rtol=0, atol=1e-15)  # position 0
