@@ -460,6 +460,48 @@ def measure_prefill(pa, steps, warmup, peaks):
     return res
 
 
+def measure_rope_writeback(pa, steps, warmup, peaks):
+    """Fused Q/K RMS norm + rotary embedding + KV writeback of the
+    varlen_prefill rows (34k tokens: K and V into their pages, the queries
+    rotated in place), L2 flushed between iterations; HBM-bound."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = workloads.varlen_prefill(device=dev)
+    stream = torch.cuda.current_stream()
+    g = torch.Generator().manual_seed(7)
+    kw = (0.5 + torch.rand(case.head_dim, generator=g)).to(torch.bfloat16).to(dev)
+    qw = (0.5 + torch.rand(case.head_dim, generator=g)).to(torch.bfloat16).to(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def write():
+        pa.kv_write_paged_rope(case.k_pool, case.v_pool, case.k_new, case.v_new, case.cu_seqlens_q, case.seq_lens,
+                               case.block_table, 1e6, q=case.q, q_norm_weight=qw, k_norm_weight=kw)
+
+    for _ in range(warmup):
+        write()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(steps):
+        _flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        write()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    t = statistics.median(ms)
+    nbytes = roofline.kv_write_rope_bytes(case.total_q, case.num_kv_heads, case.num_q_heads, case.head_dim)
+    gbs = nbytes / (t * 1e-3) / 1e9
+    res = {"workload": "varlen_prefill rows (16 sequences, 512..4096 tokens; Hq=28, Hkv=4, head_dim 128): K/V "
+                       "RMS norm + rotary embedding (base 1e6) + writeback, queries rotated in place",
+           "tokens": case.total_q, "ms": t, "bytes": nbytes,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]},
+           "l2": "flushed (256 MiB write) between iterations", "steps": steps, "launches_per_step": 1}
+    del case, flush
+    torch.cuda.empty_cache()
+    return res
+
+
 def measure_mixed(pa, steps, warmup, peaks):
     """Mixed serving step in one call: 4 prefill chunks of 2048 tokens after
     0..8192 cached tokens + 60 decodes (1k..64k context) + one 131,072-token
@@ -557,7 +599,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-only", action="store_true", help="skip the prefill and mixed-step measurements")
-    ap.add_argument("--only", choices=["prefill", "mixed", "multiquery"], default=None,
+    ap.add_argument("--only", choices=["prefill", "mixed", "multiquery", "rope_writeback"], default=None,
                     help="run just this extra measurement (for profiling); prints its object only")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
@@ -572,7 +614,8 @@ def main(argv=None):
     peaks = load_peaks()
     dev = torch.device("cuda", torch.cuda.current_device())
     if args.only is not None:
-        fn = {"prefill": measure_prefill, "mixed": measure_mixed, "multiquery": measure_multiquery}[args.only]
+        fn = {"prefill": measure_prefill, "mixed": measure_mixed, "multiquery": measure_multiquery,
+              "rope_writeback": measure_rope_writeback}[args.only]
         res = fn(pa, args.steps, args.warmup, peaks)
         if rank == 0:
             print(json.dumps({"only": args.only, args.only: res}), flush=True)
@@ -622,7 +665,8 @@ def main(argv=None):
         line["prefill"] = measure_prefill(pa, psteps, 3, peaks)
         line["mixed"] = measure_mixed(pa, psteps, 3, peaks)
         line["multiquery"] = measure_multiquery(pa, psteps, 3, peaks)
-        line["gpu_launches"] += world * psteps * (4 + 3 + 1)
+        line["rope_writeback"] = measure_rope_writeback(pa, psteps, 3, peaks)
+        line["gpu_launches"] += world * psteps * (4 + 3 + 1 + 1)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_subprocess()
     if rank == 0:

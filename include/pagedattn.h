@@ -9,6 +9,8 @@
  *                                pages ("Inside Ion", section "IonAttention
  *                                in One Paragraph": KV pages are written back
  *                                eagerly as they are produced).
+ *   kv_write_paged_rope          the same with the Q/K RMS norm and rotary
+ *                                embedding fused in.
  *   attn_decode_paged            one query row per sequence against its whole
  *                                paged history, split along the KV sequence
  *                                and merged with the log-sum-exp identity
@@ -204,6 +206,32 @@ int kv_write_paged(void* k_pool, void* v_pool, int num_pages, const void* k_new,
                    const int32_t* cu_seqlens_new, const int32_t* seq_lens,
                    const int32_t* block_table, int max_pages_per_seq, int batch, int total_new,
                    int page_size, int num_kv_heads, int head_dim, int32_t* status, void* stream);
+
+/*
+ * Fused Q/K normalisation, rotary embedding and KV writeback ("The Stack
+ * Below the Stack, Part 2", section 2.1, kernel fusion: fused Q-norm,
+ * KV-RoPE and K-insert).  Same placement as kv_write_paged: new row i of
+ * sequence b goes to position pos = seq_lens[b] - n_b + i.  Before it is
+ * written, each K head row is
+ *     x <- x / sqrt(mean(x^2) + norm_eps) * k_norm_weight   (if k_norm_weight)
+ *     (x[j], x[j + D/2]) <- rotated by pos * rope_base^(-2j/D)   (j < D/2)
+ * in fp32 and rounded once to bf16 (round to nearest even); V rows are copied
+ * bit for bit.  When q is not NULL its rows (bf16 [total_new][num_q_heads]
+ * [head_dim], the queries of the same new tokens) get the same treatment in
+ * place, with q_norm_weight.  The rotation pairs dimension j with j + D/2
+ * (the "rotate-half" layout of Llama- and Qwen-family models).
+ *   rope_base      > 1 and finite (PA_ERR_SHAPE otherwise)
+ *   q_norm_weight, k_norm_weight  bf16 [head_dim] or NULL (no normalisation)
+ *   norm_eps       >= 0 and finite
+ * Angles are reduced exactly (64-bit fixed-point turns), so positions up to
+ * 2^31 keep full fp32 accuracy.
+ */
+int kv_write_paged_rope(void* k_pool, void* v_pool, int num_pages, const void* k_new, const void* v_new,
+                        void* q, int num_q_heads, const int32_t* cu_seqlens_new, const int32_t* seq_lens,
+                        const int32_t* block_table, int max_pages_per_seq, int batch, int total_new,
+                        int page_size, int num_kv_heads, int head_dim, float rope_base,
+                        const void* q_norm_weight, const void* k_norm_weight, float norm_eps,
+                        int32_t* status, void* stream);
 
 /*
  * Allocation-free variant of attn_decode_paged.  This entry point has no

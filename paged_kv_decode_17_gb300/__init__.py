@@ -3,6 +3,8 @@
 Public calls (same names as the C ABI in include/pagedattn.h):
 
 * ``kv_write_paged``              eager writeback of new K/V rows into pages
+* ``kv_write_paged_rope``         the same with the Q/K RMS norm and rotary
+                                  embedding fused in
 * ``attn_decode_paged``           split-K Flash-Decoding over pages
 * ``attn_decode_multiquery_paged`` the same for 1-8 query rows per sequence,
                                   causal inside the block (speculative
@@ -24,6 +26,7 @@ from .ops import (  # noqa: F401
     decode_multiquery_workspace_bytes,
     decode_workspace_bytes,
     kv_write_paged,
+    kv_write_paged_rope,
     new_status,
     prefill_workspace_bytes,
 )

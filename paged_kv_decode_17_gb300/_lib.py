@@ -57,6 +57,14 @@ SIGNATURES = {
         c_int, c_int, c_int, c_int, c_float,  # page_size, Hq, Hkv, D, scale
         c_void_p, c_size_t, c_void_p, c_void_p,  # workspace, bytes, status, stream
     ]),
+    "kv_write_paged_rope": (c_int, [
+        c_void_p, c_void_p, c_int, c_void_p, c_void_p,  # k_pool, v_pool, num_pages, k_new, v_new
+        c_void_p, c_int,  # q (nullable), num_q_heads
+        c_void_p, c_void_p, c_void_p, c_int,  # cu_seqlens_new, seq_lens, block_table, max_pages
+        c_int, c_int, c_int, c_int, c_int,  # batch, total_new, page_size, Hkv, D
+        c_float, c_void_p, c_void_p, c_float,  # rope_base, q_norm_weight, k_norm_weight, norm_eps
+        c_void_p, c_void_p,  # status, stream
+    ]),
     "kv_write_paged": (c_int, [
         c_void_p, c_void_p, c_int, c_void_p, c_void_p,  # k_pool, v_pool, num_pages, k_new, v_new
         c_void_p, c_void_p, c_void_p, c_int,  # cu_seqlens_new, seq_lens, block_table, max_pages

@@ -5,8 +5,22 @@
 // over cu_seqlens_new, resolves (page, slot) through the block table, and
 // copies the token's [Hkv][D] K and V rows with 16-byte vector loads and
 // stores.  A bit-exact copy; nothing else in the pools is written.
+//
+// kv_write_paged_rope fuses the step before it ("The Stack Below the Stack,
+// Part 2", section 2.1: fused Q-norm, KV-RoPE and K-insert): each K head row
+// (and, optionally, each query head row, in place) is RMS-normalised when a
+// weight is given and rotated by the rotary position embedding at the row's
+// position, in fp32, then rounded once to bf16; V rows are copied.  Lane l of
+// the token's warp owns the pairs (i, i + D/2) for i in [l * D/64, (l+1) *
+// D/64), so each pair is rotated by one thread and the cos / sin of the
+// token's angles are computed once and reused for every head.  Angles are
+// reduced exactly: the host passes frac(theta_i / 2 pi) as a 64-bit binary
+// fraction, the position times it (mod 2^64) is the angle in turns, and
+// sincospif turns its top 24 bits into cos and sin.
 #include "pa_common.cuh"
 #include "pa_host.h"
+
+#include <cmath>
 
 namespace pa {
 namespace kvw {
@@ -58,6 +72,161 @@ __global__ void __launch_bounds__(kWarps * 32) kv_write_kernel(
     }
 }
 
+struct RopeParams {
+    __nv_bfloat16* k_pool;
+    __nv_bfloat16* v_pool;
+    const __nv_bfloat16* k_new;
+    const __nv_bfloat16* v_new;
+    __nv_bfloat16* q;  // may be null
+    const __nv_bfloat16* q_norm_w;  // may be null
+    const __nv_bfloat16* k_norm_w;  // may be null
+    const int32_t* cu_new;
+    const int32_t* seq_lens;
+    const int32_t* block_table;
+    int32_t* status;
+    int num_pages, max_pages, batch, total_new, page_size, Hkv, Hq;
+    float eps;
+    unsigned long long turns[64];  // frac(base^(-2i/D) / (2 pi)) * 2^64, i < D/2
+};
+
+// Pair elements of one head row held by a lane: x1[j] = row[i_j], x2[j] = row[i_j + D/2].
+template <int D>
+struct PairIO {
+    static constexpr int PPL = D / 64;  // pairs per lane
+    __device__ static void load(const __nv_bfloat16* row, int lane, float* x1, float* x2) {
+        if constexpr (PPL == 2) {
+            const __nv_bfloat162 a = reinterpret_cast<const __nv_bfloat162*>(row)[lane];
+            const __nv_bfloat162 b = reinterpret_cast<const __nv_bfloat162*>(row + D / 2)[lane];
+            x1[0] = __low2float(a);
+            x1[1] = __high2float(a);
+            x2[0] = __low2float(b);
+            x2[1] = __high2float(b);
+        } else {
+            x1[0] = __bfloat162float(row[lane]);
+            x2[0] = __bfloat162float(row[lane + D / 2]);
+        }
+    }
+    __device__ static void store(__nv_bfloat16* row, int lane, const float* y1, const float* y2) {
+        if constexpr (PPL == 2) {
+            reinterpret_cast<__nv_bfloat162*>(row)[lane] = __floats2bfloat162_rn(y1[0], y1[1]);
+            reinterpret_cast<__nv_bfloat162*>(row + D / 2)[lane] = __floats2bfloat162_rn(y2[0], y2[1]);
+        } else {
+            row[lane] = __float2bfloat16_rn(y1[0]);
+            row[lane + D / 2] = __float2bfloat16_rn(y2[0]);
+        }
+    }
+};
+
+// Normalise (optional) and rotate NH head rows held as pairs.  All NH rows
+// are loaded before any is processed, so NH loads are in flight at once.
+template <int D, int NH>
+__device__ __forceinline__ void rope_rows(const __nv_bfloat16* src, size_t src_stride, __nv_bfloat16* const* dst,
+                                          const __nv_bfloat16* w, float eps, int lane, const float* c,
+                                          const float* s) {
+    constexpr int PPL = D / 64;
+    float x1[NH][PPL], x2[NH][PPL];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) PairIO<D>::load(src + h * src_stride, lane, x1[h], x2[h]);
+    if (w != nullptr) {
+        float w1[PPL], w2[PPL];
+        PairIO<D>::load(w, lane, w1, w2);
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+            float ss = 0.f;
+#pragma unroll
+            for (int j = 0; j < PPL; ++j) ss += x1[h][j] * x1[h][j] + x2[h][j] * x2[h][j];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float r = rsqrtf(ss * (1.f / D) + eps);
+#pragma unroll
+            for (int j = 0; j < PPL; ++j) {
+                x1[h][j] *= r * w1[j];
+                x2[h][j] *= r * w2[j];
+            }
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+        float y1[PPL], y2[PPL];
+#pragma unroll
+        for (int j = 0; j < PPL; ++j) {
+            y1[j] = x1[h][j] * c[j] - x2[h][j] * s[j];
+            y2[j] = x2[h][j] * c[j] + x1[h][j] * s[j];
+        }
+        PairIO<D>::store(dst[h], lane, y1, y2);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32) kv_write_rope_kernel(const __grid_constant__ RopeParams p) {
+    constexpr int PPL = D / 64;
+    const int lane = threadIdx.x & 31;
+    const int nwarps = gridDim.x * kWarps;
+    for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < p.total_new; t += nwarps) {
+        int lo = 0, hi = p.batch - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(p.cu_new + mid) <= t) lo = mid; else hi = mid - 1;
+        }
+        const int b = lo;
+        const int n_b = __ldg(p.cu_new + b + 1) - __ldg(p.cu_new + b);
+        const int i = t - __ldg(p.cu_new + b);
+        const int L = __ldg(p.seq_lens + b);
+        const int pos = L - n_b + i;
+        if (n_b <= 0 || i >= n_b || pos < 0 || pos >= p.max_pages * p.page_size) {
+            if (lane == 0) report(p.status, PA_ERR_BAD_LEN);
+            continue;
+        }
+        const int phys = __ldg(p.block_table + (size_t)b * p.max_pages + pos / p.page_size);
+        if (phys < 0 || phys >= p.num_pages) {
+            if (lane == 0) report(p.status, PA_ERR_BAD_PAGE);
+            continue;
+        }
+        const int slot = pos % p.page_size;
+        // cos / sin of this position's angles, one pair at a time
+        float c[PPL], s[PPL];
+#pragma unroll
+        for (int j = 0; j < PPL; ++j) {
+            const unsigned long long turn = (unsigned long long)pos * p.turns[lane * PPL + j];  // mod 2^64
+            const float frac = (float)(unsigned)(turn >> 40) * 0x1p-24f;                     // exact
+            sincospif(2.f * frac, &s[j], &c[j]);
+        }
+        // K heads (rotated) and V heads (copied), four at a time
+        for (int g0 = 0; g0 < p.Hkv; g0 += 4) {
+            const int nh = min(4, p.Hkv - g0);
+            __nv_bfloat16* kd[4];
+            float v1[4][PPL], v2[4][PPL];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const int g = g0 + (h < nh ? h : 0);
+                kd[h] = p.k_pool + (((size_t)phys * p.Hkv + g) * p.page_size + slot) * D;
+                if (h < nh) PairIO<D>::load(p.v_new + ((size_t)t * p.Hkv + g) * D, lane, v1[h], v2[h]);
+            }
+            const __nv_bfloat16* ks = p.k_new + ((size_t)t * p.Hkv + g0) * D;
+            if (nh == 4) {
+                rope_rows<D, 4>(ks, D, kd, p.k_norm_w, p.eps, lane, c, s);
+            } else {
+                for (int h = 0; h < nh; ++h) rope_rows<D, 1>(ks + h * D, D, kd + h, p.k_norm_w, p.eps, lane, c, s);
+            }
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+                if (h < nh) PairIO<D>::store(kd[h] - p.k_pool + p.v_pool, lane, v1[h], v2[h]);  // exact copy
+        }
+        if (p.q != nullptr) {
+            __nv_bfloat16* qrow = p.q + (size_t)t * p.Hq * D;
+            int h = 0;
+            for (; h + 4 <= p.Hq; h += 4) {
+                __nv_bfloat16* qd[4] = {qrow + h * D, qrow + (h + 1) * D, qrow + (h + 2) * D, qrow + (h + 3) * D};
+                rope_rows<D, 4>(qrow + h * D, D, qd, p.q_norm_w, p.eps, lane, c, s);
+            }
+            for (; h < p.Hq; ++h) {
+                __nv_bfloat16* qd[1] = {qrow + h * D};
+                rope_rows<D, 1>(qrow + h * D, D, qd, p.q_norm_w, p.eps, lane, c, s);
+            }
+        }
+    }
+}
+
 }  // namespace kvw
 }  // namespace pa
 
@@ -83,5 +252,70 @@ extern "C" int kv_write_paged(void* k_pool, void* v_pool, int num_pages, const v
         static_cast<__nv_bfloat16*>(k_pool), static_cast<__nv_bfloat16*>(v_pool),
         static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new), cu_seqlens_new, seq_lens,
         block_table, num_pages, max_pages_per_seq, batch, total_new, page_size, num_kv_heads, head_dim, status);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" int kv_write_paged_rope(void* k_pool, void* v_pool, int num_pages, const void* k_new, const void* v_new,
+                                   void* q, int num_q_heads, const int32_t* cu_seqlens_new, const int32_t* seq_lens,
+                                   const int32_t* block_table, int max_pages_per_seq, int batch, int total_new,
+                                   int page_size, int num_kv_heads, int head_dim, float rope_base,
+                                   const void* q_norm_weight, const void* k_norm_weight, float norm_eps,
+                                   int32_t* status, void* stream) {
+    using namespace pa;
+    if (batch < 0 || total_new < 0) return PA_ERR_SHAPE;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_SHAPE;
+    if (page_size < 16 || page_size > 256 || page_size % 16 != 0) return PA_ERR_SHAPE;
+    if (num_kv_heads < 1) return PA_ERR_SHAPE;
+    if (q != nullptr && (num_q_heads < num_kv_heads || num_q_heads % num_kv_heads != 0)) return PA_ERR_SHAPE;
+    if (!(rope_base > 1.f) || rope_base == INFINITY) return PA_ERR_SHAPE;  // also rejects NaN
+    if (!(norm_eps >= 0.f) || norm_eps == INFINITY) return PA_ERR_SHAPE;
+    if (batch == 0 || total_new == 0) return PA_OK;
+    if (!k_pool || !v_pool || !k_new || !v_new || !cu_seqlens_new || !seq_lens || !block_table) return PA_ERR_NULL;
+    if (num_pages < 1 || max_pages_per_seq < 1) return PA_ERR_SHAPE;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_new) || !aligned16(v_new)) return PA_ERR_SHAPE;
+    if ((q && !aligned16(q)) || (q_norm_weight && !aligned16(q_norm_weight)) ||
+        (k_norm_weight && !aligned16(k_norm_weight)))
+        return PA_ERR_SHAPE;
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc != PA_OK) return rc;
+
+    kvw::RopeParams prm;
+    prm.k_pool = static_cast<__nv_bfloat16*>(k_pool);
+    prm.v_pool = static_cast<__nv_bfloat16*>(v_pool);
+    prm.k_new = static_cast<const __nv_bfloat16*>(k_new);
+    prm.v_new = static_cast<const __nv_bfloat16*>(v_new);
+    prm.q = static_cast<__nv_bfloat16*>(q);
+    prm.q_norm_w = static_cast<const __nv_bfloat16*>(q_norm_weight);
+    prm.k_norm_w = static_cast<const __nv_bfloat16*>(k_norm_weight);
+    prm.cu_new = cu_seqlens_new;
+    prm.seq_lens = seq_lens;
+    prm.block_table = block_table;
+    prm.status = status;
+    prm.num_pages = num_pages;
+    prm.max_pages = max_pages_per_seq;
+    prm.batch = batch;
+    prm.total_new = total_new;
+    prm.page_size = page_size;
+    prm.Hkv = num_kv_heads;
+    prm.Hq = q != nullptr ? num_q_heads : 0;
+    prm.eps = norm_eps;
+    // frequencies as 64-bit fractions of a turn: theta_i = base^(-2i/D) <= 1 rad < 1 turn
+    for (int i = 0; i < 64; ++i) {
+        if (i < head_dim / 2) {
+            const double theta = std::pow((double)rope_base, -2.0 * i / head_dim);
+            const double turns = theta / (2.0 * M_PI);  // in (0, 0.16]
+            prm.turns[i] = (unsigned long long)(turns * 18446744073709551616.0);
+        } else {
+            prm.turns[i] = 0;
+        }
+    }
+    const int blocks_needed = (total_new + kvw::kWarps - 1) / kvw::kWarps;
+    const int grid = blocks_needed < dev.sm_count * 16 ? blocks_needed : dev.sm_count * 16;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (head_dim == 128)
+        kvw::kv_write_rope_kernel<128><<<grid, kvw::kWarps * 32, 0, st>>>(prm);
+    else
+        kvw::kv_write_rope_kernel<64><<<grid, kvw::kWarps * 32, 0, st>>>(prm);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

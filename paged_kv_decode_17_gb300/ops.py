@@ -118,6 +118,49 @@ def kv_write_paged(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch.Tens
     _lib.check(rc, "kv_write_paged")
 
 
+def kv_write_paged_rope(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                        cu_seqlens_new: torch.Tensor, seq_lens: torch.Tensor, block_table: torch.Tensor,
+                        rope_base: float = 10000.0, *, q: Optional[torch.Tensor] = None,
+                        q_norm_weight: Optional[torch.Tensor] = None, k_norm_weight: Optional[torch.Tensor] = None,
+                        norm_eps: float = 1e-6, status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Writeback with the Q/K RMS norm (optional) and rotary embedding fused in.
+
+    K rows are normalised (if ``k_norm_weight``) and rotated at their
+    position before they are written; V rows are copied; ``q`` (the same
+    tokens' queries, [total_new][Hq][D]) is normalised / rotated in place.
+    """
+    lib = _lib.load()
+    _need(k_pool, "k_pool", torch.bfloat16, 4)
+    _need(v_pool, "v_pool", torch.bfloat16, 4)
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(cu_seqlens_new, "cu_seqlens_new", torch.int32, 1)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(block_table, "block_table", torch.int32, 2)
+    P, Hkv, ps, D = k_pool.shape
+    if v_pool.shape != k_pool.shape or k_new.shape != v_new.shape or k_new.shape[1:] != (Hkv, D):
+        raise ValueError("inconsistent K/V shapes")
+    Hq = 0
+    if q is not None:
+        _need(q, "q", torch.bfloat16, 3)
+        if q.shape[0] != k_new.shape[0] or q.shape[2] != D:
+            raise ValueError("q must be [total_new][Hq][head_dim]")
+        Hq = q.shape[1]
+    for name, w in (("q_norm_weight", q_norm_weight), ("k_norm_weight", k_norm_weight)):
+        if w is not None:
+            _need(w, name, torch.bfloat16, 1)
+            if w.shape[0] != D:
+                raise ValueError("%s must have head_dim entries" % name)
+    B = seq_lens.shape[0]
+    if cu_seqlens_new.shape[0] != B + 1 or block_table.shape[0] != B:
+        raise ValueError("cu_seqlens_new must have batch+1 entries and block_table batch rows")
+    rc = lib.kv_write_paged_rope(_ptr(k_pool), _ptr(v_pool), P, _ptr(k_new), _ptr(v_new), _ptr(q), Hq,
+                                 _ptr(cu_seqlens_new), _ptr(seq_lens), _ptr(block_table), block_table.shape[1], B,
+                                 k_new.shape[0], ps, Hkv, D, float(rope_base), _ptr(q_norm_weight),
+                                 _ptr(k_norm_weight), float(norm_eps), _ptr(status), _stream_handle(stream))
+    _lib.check(rc, "kv_write_paged_rope")
+
+
 def attn_decode_paged(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor,
                       seq_lens: torch.Tensor, softmax_scale: Optional[float] = None, *,
                       max_seq_len: Optional[int] = None, out: Optional[torch.Tensor] = None,

@@ -36,3 +36,11 @@ def prefill_flops(q_lens: Sequence[int], seq_lens: Sequence[int], num_q_heads: i
 
 def kv_write_bytes(total_new: int, num_kv_heads: int, head_dim: int, elem_bytes: int = 2) -> int:
     return 2 * 2 * int(total_new) * num_kv_heads * head_dim * elem_bytes
+
+
+def kv_write_rope_bytes(total_new: int, num_kv_heads: int, num_q_heads: int, head_dim: int,
+                        elem_bytes: int = 2) -> int:
+    """Fused writeback: K and V rows read and written, query rows read and
+    written back in place (the norm weights, 2 x head_dim elements, are not counted)."""
+    return kv_write_bytes(total_new, num_kv_heads, head_dim, elem_bytes) + \
+        2 * int(total_new) * num_q_heads * head_dim * elem_bytes

@@ -126,3 +126,23 @@ def test_multiquery_host_validation(lib):
     a = list(args)
     a[10], a[2] = 0, None  # empty batch: nothing to do
     assert f(*a) == 0
+
+
+def test_kv_write_rope_host_validation(lib):
+    f = lib.kv_write_paged_rope
+    P = 1 << 20
+    # k_pool, v_pool, num_pages, k_new, v_new, q, Hq, cu, lens, bt, maxp, batch, total, ps, Hkv, D, base, qw, kw, eps
+    args = [P, P, 8, P, P, None, 0, P, P, P, 4, 2, 10, 16, 2, 64, 10000.0, None, None, 1e-6, None, None]
+    for i, bad in ((16, 1.0), (16, float("nan")), (16, float("inf")), (19, -1.0), (15, 96)):
+        a = list(args)
+        a[i] = bad
+        assert f(*a) == -2, (i, bad)
+    a = list(args)
+    a[5], a[6] = P, 3  # q given with Hq not a multiple of Hkv
+    assert f(*a) == -2
+    a = list(args)
+    a[0] = None
+    assert f(*a) == -1
+    a = list(args)
+    a[11] = 0  # empty batch
+    assert f(*a) == 0
