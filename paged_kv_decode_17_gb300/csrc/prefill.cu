@@ -20,9 +20,11 @@
 //   item's Q and K/V are loaded while the current item finishes.
 // * warp 8 (producer): publishes each item through a 2-slot ring in shared
 //   memory, loads the two Q tiles by TMA (3-D tensor map over [rows][Hq][D],
-//   128-byte swizzle) and gathers K and V tiles through a 3-stage ring: a
-//   128-key tile is eight 16-row page blocks found through the block table
-//   (one tile ahead), each 64-column half a 128-byte-swizzled TMA box.
+//   128-byte swizzle) and gathers K and V tiles: a 128-key tile is eight
+//   16-row page blocks found through the block table (one tile ahead), each
+//   64-column half a 128-byte-swizzled TMA box.  K and V tiles have
+//   separate rings (1 and 2 stages), so the next K tile loads as soon as the
+//   current scores are computed.
 // * warps 9 / 10 (MMA, one per head): one thread issues tcgen05.mma:
 //   S_h = Q_h K^T into TMEM (fp32, 128 columns) and O_h += P_h V into TMEM
 //   (fp32, D columns); the next tile's scores are issued as soon as the
@@ -50,13 +52,20 @@ namespace pf {
 constexpr int BM = 128;      // query rows per tile (= TMEM lanes)
 constexpr int BN = 128;      // keys per KV tile
 constexpr int UPT = BN / 16; // 16-key page blocks per KV tile
-#ifndef PA_PF_NSTAGE
-#define PA_PF_NSTAGE 3
+#ifndef PA_PF_NK
+#define PA_PF_NK 1
+#endif
+#ifndef PA_PF_NV
+#define PA_PF_NV 2
 #endif
 #ifndef PA_PF_MAX_CLUSTER
 #define PA_PF_MAX_CLUSTER 4
 #endif
-constexpr int NSTAGE = PA_PF_NSTAGE;  // K/V ring depth (K and V tiles alternate)
+// K and V tiles go through separate rings: the next K tile only waits for the
+// current scores (S) to be computed, not for the previous P.V to finish.
+constexpr int NK = PA_PF_NK;  // K ring depth
+constexpr int NV = PA_PF_NV;  // V ring depth
+constexpr int NSTAGE = NK + NV;  // stages 0 .. NK-1 hold K tiles, NK .. NSTAGE-1 V tiles
 constexpr int MAX_CLUSTER = PA_PF_MAX_CLUSTER;
 constexpr float TAU = 8.f;   // rescale threshold, log2 units
 // warps 0-7: softmax (head = warp / 4, row quarter = warp & 3)
@@ -292,7 +301,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             prefetch_tensormap(&vmap);
         }
         const long long n_items = (long long)__ldg(p.n_tiles) * p.Hkv * p.NPC;
-        int ring = 0;                 // K/V ring entries issued so far (K and V of a tile are two)
+        int kring = 0, vring = 0;     // K / V tiles issued so far
         int tails = 0;                // uses of the v_tail barrier
         int qloads[2] = {0, 0};       // Q tiles loaded per head
         bool ok = true;
@@ -375,10 +384,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const bool mine = lane < UPT * C::KB && (lane % CS) == crank && box_row >= 0;
                 const bool tail = (j + 1) * BN > itm.seq_len;
                 for (int x = 0; x < 2 && ok; ++x) {
-                    const int i = ring++;
-                    const int st = i % NSTAGE;
+                    const int i = x == 0 ? kring++ : vring++;
+                    const int depth = x == 0 ? NK : NV;
+                    const int st = (x == 0 ? 0 : NK) + i % depth;
                     ok = __all_sync(0xffffffffu,
-                                    wait_ab(&sh.kv_empty[st], ((i / NSTAGE) & 1) ^ 1, sh, p.status));
+                                    wait_ab(&sh.kv_empty[st], ((i / depth) & 1) ^ 1, sh, p.status));
                     if (!ok) break;
                     uint8_t* dst = sKV + st * C::KV_BYTES;
                     const bool via_tail = (x == 1) && tail;
@@ -426,9 +436,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) {
             for (int hh = 0; hh < 2; ++hh)
                 if (qloads[hh] > 0) mbar_wait(&sh.bar_q[hh], (qloads[hh] - 1) & 1);
-            for (int i = max(0, ring - NSTAGE); i < ring; ++i) {
-                mbar_wait(&sh.kv_full[i % NSTAGE], (i / NSTAGE) & 1);
-                mbar_wait(&sh.kv_empty[i % NSTAGE], (i / NSTAGE) & 1);
+            for (int i = max(0, kring - NK); i < kring; ++i) {
+                mbar_wait(&sh.kv_full[i % NK], (i / NK) & 1);
+                mbar_wait(&sh.kv_empty[i % NK], (i / NK) & 1);
+            }
+            for (int i = max(0, vring - NV); i < vring; ++i) {
+                mbar_wait(&sh.kv_full[NK + i % NV], (i / NV) & 1);
+                mbar_wait(&sh.kv_empty[NK + i % NV], (i / NV) & 1);
             }
         }
         __syncwarp();
@@ -448,7 +462,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 else
                     tc::commit(bar);
             };
-            int ring = 0;   // K/V ring position (same walk as the producer)
+            int kr = 0, vr = 0;  // K / V ring positions (same walk as the producer)
+            // stage and phase of the K / V tile of key tile j of the current item
+            auto kst = [&](int j) { return (kr + j) % NK; };
+            auto kph = [&](int j) { return (uint32_t)(((kr + j) / NK) & 1); };
+            auto vst = [&](int j) { return NK + (vr + j) % NV; };
+            auto vph = [&](int j) { return (uint32_t)(((vr + j) / NV) & 1); };
             int J = 0;      // tiles this head has computed (phase counter of its S / P barriers)
             int items = 0;  // items this head has computed
             int qn = 0;     // Q tiles consumed
@@ -461,16 +480,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int n = itm.n_kv;
                 if (hh >= itm.nheads) {
                     // not our head this time: still release every stage we pass
-                    for (int j = 0; j < 2 * n && ok; ++j) {
-                        const int i = ring + j;
-                        ok = wait_ab(&sh.kv_full[i % NSTAGE], (i / NSTAGE) & 1, sh, p.status);
-                        if (ok) release(&sh.kv_empty[i % NSTAGE]);
+                    for (int j = 0; j < n && ok; ++j) {
+                        ok = wait_ab(&sh.kv_full[kst(j)], kph(j), sh, p.status);
+                        if (ok) release(&sh.kv_empty[kst(j)]);
+                        if (ok) ok = wait_ab(&sh.kv_full[vst(j)], vph(j), sh, p.status);
+                        if (ok) release(&sh.kv_empty[vst(j)]);
                     }
                 } else {
                     ok = wait_ab(&sh.bar_q[hh], qn & 1, sh, p.status);
                     ++qn;
                     auto issue_s = [&](int j) {
-                        const uint32_t kaddr = kv_base + ((ring + 2 * j) % NSTAGE) * C::KV_BYTES;
+                        const uint32_t kaddr = kv_base + kst(j) * C::KV_BYTES;
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint64_t ad =
@@ -483,7 +503,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         if (j == n - 1) tc::commit(&sh.q_empty[hh]);  // last read of this Q tile
                     };
                     auto issue_pv = [&](int j) {
-                        const uint32_t vaddr = kv_base + ((ring + 2 * j + 1) % NSTAGE) * C::KV_BYTES;
+                        const uint32_t vaddr = kv_base + vst(j) * C::KV_BYTES;
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk) {
                             const uint64_t ad =
@@ -494,37 +514,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         tc::commit(&sh.pv_done[hh]);
                     };
                     // scores of key tile 0 (the S buffer was freed by the previous tile's softmax)
-                    if (ok) ok = wait_ab(&sh.kv_full[ring % NSTAGE], (ring / NSTAGE) & 1, sh, p.status);
+                    if (ok) ok = wait_ab(&sh.kv_full[kst(0)], kph(0), sh, p.status);
                     if (ok && J > 0) ok = wait_ab(&sh.s_free[hh], (J - 1) & 1, sh, p.status);
                     if (ok) {
                         tc::fence_after_sync();
                         issue_s(0);
-                        release(&sh.kv_empty[ring % NSTAGE]);
+                        release(&sh.kv_empty[kst(0)]);
                     }
                     for (int j = 0; j < n && ok; ++j) {
-                        const int ik = ring + 2 * (j + 1), iv = ring + 2 * j + 1;
                         if (j + 1 < n) {
                             // next scores as soon as the softmax has pulled the current ones out of TMEM
-                            ok = wait_ab(&sh.kv_full[ik % NSTAGE], (ik / NSTAGE) & 1, sh, p.status) &&
+                            ok = wait_ab(&sh.kv_full[kst(j + 1)], kph(j + 1), sh, p.status) &&
                                  wait_ab(&sh.s_free[hh], (J + j) & 1, sh, p.status);
                             if (!ok) break;
                             tc::fence_after_sync();
                             issue_s(j + 1);
-                            release(&sh.kv_empty[ik % NSTAGE]);
+                            release(&sh.kv_empty[kst(j + 1)]);
                         }
-                        ok = wait_ab(&sh.kv_full[iv % NSTAGE], (iv / NSTAGE) & 1, sh, p.status) &&
+                        ok = wait_ab(&sh.kv_full[vst(j)], vph(j), sh, p.status) &&
                              wait_ab(&sh.p_ready[hh], (J + j) & 1, sh, p.status);
                         // the first P.V overwrites O: the previous item's epilogue must have read it
                         if (ok && j == 0 && items > 0) ok = wait_ab(&sh.o_free[hh], (items - 1) & 1, sh, p.status);
                         if (!ok) break;
                         tc::fence_after_sync();
                         issue_pv(j);
-                        release(&sh.kv_empty[iv % NSTAGE]);
+                        release(&sh.kv_empty[vst(j)]);
                     }
                     J += n;
                     ++items;
                 }
-                ring += 2 * n;
+                kr += n;
+                vr += n;
                 mbar_arrive(&sh.item_empty[k & 1]);
             }
         }
