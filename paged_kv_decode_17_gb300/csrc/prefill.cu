@@ -622,6 +622,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         l *= alpha;
                         m_ref = m_new;
                     }
+                    // p = 2^(s * scale_log2 - m_ref): one FFMA + one MUFU each, packed to bf16 in
+                    // registers while the previous tile's P.V may still be running; sums as a tree
+                    const float neg = -m_ref;
+                    float s8[8];
+                    uint32_t pk[BN / 2];
+#pragma unroll
+                    for (int q = 0; q < BN / 8; ++q) {  // 16-byte chunk q = keys 8q .. 8q+7
+                        float part = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float p0 = ex2(fmaf(x[8 * q + 2 * i], p.scale_log2, neg));
+                            const float p1 = ex2(fmaf(x[8 * q + 2 * i + 1], p.scale_log2, neg));
+                            part += p0 + p1;
+                            pk[4 * q + i] = pack_bf16x2(p0, p1);
+                        }
+                        s8[q & 7] = q < 8 ? part : s8[q & 7] + part;
+                    }
                     // the P buffer was last read by the previous tile's P.V (possibly of the
                     // previous item).  Waiting for it also keeps p_ready / pv_done within one
                     // phase of their waiters (mbarrier parity only tells adjacent phases apart).
@@ -629,25 +646,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         ok = __all_sync(0xffffffffu, wait_ab(&sh.pv_done[hh], (jj - 1) & 1, sh, p.status));
                         if (!ok) break;
                     }
-                    // p = 2^(s * scale_log2 - m_ref): one FFMA + one MUFU each; sums as a tree;
-                    // P (bf16) goes to shared memory in the 128-byte-swizzled K-major layout
-                    const float neg = -m_ref;
-                    float s8[8];
+                    // P (bf16) to shared memory in the 128-byte-swizzled K-major layout
 #pragma unroll
-                    for (int q = 0; q < BN / 8; ++q) {  // 16-byte chunk q = keys 8q .. 8q+7
-                        uint32_t pk[4];
-                        float part = 0.f;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float p0 = ex2(fmaf(x[8 * q + 2 * i], p.scale_log2, neg));
-                            const float p1 = ex2(fmaf(x[8 * q + 2 * i + 1], p.scale_log2, neg));
-                            part += p0 + p1;
-                            pk[i] = pack_bf16x2(p0, p1);
-                        }
-                        s8[q & 7] = q < 8 ? part : s8[q & 7] + part;
+                    for (int q = 0; q < BN / 8; ++q) {
                         const int kb = q >> 3, c = q & 7;
                         *reinterpret_cast<uint4*>(prow + kb * C::P_KB + ((c ^ (r & 7)) << 4)) =
-                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                     }
                     l += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
                     fence_proxy_async_smem();
