@@ -15,6 +15,8 @@ Modules
 ``attention``  materialised-score attention over gathered pages, and the
                K/V writeback scatter (the reference definitions).
 ``brute``      an independent scalar pure-Python restatement, for tiny inputs.
+``fp8``        the e4m3 code table, the quantising FP8 writeback and attention
+               over dequantised FP8 pages.
 ``rope``       the rotary position embedding and RMS normalisation that the
                fused writeback applies to K (and Q) rows, and bf16 rounding.
 ``tiled``      a CPU model of the online-softmax recurrence and of the
@@ -31,6 +33,12 @@ from .attention import (  # noqa: F401
     attention_rows,
     paged_attention,
     kv_write_paged,
+)
+from .fp8 import (  # noqa: F401
+    e4m3_decode,
+    e4m3_encode,
+    kv_write_paged_fp8,
+    paged_attention_fp8,
 )
 from .rope import (  # noqa: F401
     bf16_ulp,

@@ -469,3 +469,90 @@ def test_rope_writeback_rows_positions_and_norm_order():
     np.testing.assert_allclose(np.mean(out * out, axis=-1), 1.0, rtol=1e-12)
     kf = oracle.bf16_bits_to_f64(k)
     np.testing.assert_allclose(out[3], oracle.rms_norm(kf[3], None, 0.0), rtol=0, atol=1e-15)  # position 0
+
+
+# ------------------------------------------------------------------ FP8 (e4m3) KV cache
+def test_e4m3_decode_matches_torch_for_every_code():
+    """All 256 codes against torch's float8_e4m3fn (an independent library decoder)."""
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    got = oracle.e4m3_decode(codes)
+    assert (np.isnan(got) == np.isnan(want)).all()
+    ok = ~np.isnan(want)
+    np.testing.assert_array_equal(got[ok], want[ok])
+
+
+def test_e4m3_closed_forms_and_round_trip():
+    vals = oracle.e4m3_decode(np.array([0x7E, 0x01, 0x08, 0x38, 0xB8, 0x80, 0x00], dtype=np.uint8))
+    np.testing.assert_array_equal(vals, [448.0, 2.0 ** -9, 2.0 ** -6, 1.0, -1.0, -0.0, 0.0])
+    assert np.signbit(vals[5])
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    np.testing.assert_array_equal(oracle.e4m3_encode(oracle.e4m3_decode(finite)), finite)
+
+
+def test_e4m3_encode_rounding_and_saturation():
+    x = np.array([1.0625, 1.1875, 2.0 ** -10, 1.5 * 2.0 ** -10, 1000.0, -1e9, 464.0, float("nan")])
+    # 1.0625 is halfway 1 (0x38) / 1.125 (0x39) -> even 0x38; 1.1875 halfway 1.125 / 1.25 -> even 0x3A;
+    # 2^-10 halfway 0 / 2^-9 -> 0; beyond 448 saturates; NaN -> 0x7F
+    np.testing.assert_array_equal(oracle.e4m3_encode(x), [0x38, 0x3A, 0x00, 0x01, 0x7E, 0xFE, 0x7E, 0x7F])
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    """torch's float32 -> float8_e4m3fn cast rounds to nearest even; in range it is the same map."""
+    rng = np.random.default_rng(60)
+    x = np.concatenate([rng.standard_normal(20000) * 50, rng.standard_normal(5000) * 1e-2]).astype(np.float32)
+    x = x[np.abs(x) < 440]
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(oracle.e4m3_encode(x), want)
+
+
+def test_fp8_attention_equals_bf16_attention_on_the_same_values():
+    """With power-of-two scales every dequantised value is exact in bf16: the
+    FP8 oracle must then equal the (pinned) bf16 oracle on those values."""
+    rng = np.random.default_rng(61)
+    P, Hkv, ps, D, Hq = 12, 2, 16, 32, 6
+    kc = rng.integers(0, 256, (P, Hkv, ps, D), dtype=np.uint8)
+    vc = rng.integers(0, 256, (P, Hkv, D, ps), dtype=np.uint8)
+    kc[(kc & 0x7F) == 0x7F] = 0x10  # no NaN codes
+    vc[(vc & 0x7F) == 0x7F] = 0x22
+    ks, vs = [0.25, 2.0], [0.5, 1.0 / 64]
+    bt = np.array([[3, 7, 1, -1], [0, 11, 5, 9]])
+    lens, qlens = [40, 61], [1, 5]
+    cu = np.array([0, 1, 6])
+    q = (rng.standard_normal((6, Hq, D)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+    def bf16_bits(v):
+        return (v.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+    kf = oracle.e4m3_decode(kc) * np.array(ks)[None, :, None, None]
+    vf = np.swapaxes(oracle.e4m3_decode(vc) * np.array(vs)[None, :, None, None], 2, 3)
+    want = paged_attention(q, bf16_bits(kf), bf16_bits(vf), bt, lens, cu, Hq, Hkv, ps, 0.2)
+    got = oracle.paged_attention_fp8(q, kc, vc, ks, vs, bt, lens, cu, Hq, Hkv, ps, 0.2)
+    np.testing.assert_allclose(got[0], want[0], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(got[1], want[1], rtol=0, atol=1e-12)
+
+
+def test_fp8_writeback_placement_and_error_bound():
+    """Rows land at (page, slot) of their position, V transposed; every code
+    reads back within half an e4m3 step of x / scale (relative 2^-4, or 2^-10
+    absolute in the subnormal range)."""
+    rng = np.random.default_rng(62)
+    P, Hkv, ps, D = 6, 2, 16, 16
+    k0 = np.zeros((P, Hkv, ps, D), np.uint8)
+    v0 = np.zeros((P, Hkv, D, ps), np.uint8)
+    kn = (rng.standard_normal((3, Hkv, D)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    vn = (rng.standard_normal((3, Hkv, D)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    ks, vs = [0.01, 0.02], [0.03, 0.005]
+    bt = np.array([[4, 2], [1, 0]])
+    kp, vp = oracle.kv_write_paged_fp8(k0, v0, kn, vn, ks, vs, [0, 2, 3], [17, 1], bt, ps)
+    # sequence 0: rows at positions 15 (page 4 slot 15) and 16 (page 2 slot 0); sequence 1: position 0
+    for (t, page, slot) in ((0, 4, 15), (1, 2, 0), (2, 1, 0)):
+        for g in range(Hkv):
+            x = bf16_bits_to_f64(kn[t, g]) / ks[g]
+            back = oracle.e4m3_decode(kp[page, g, slot])
+            assert (np.abs(back - x) <= np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10) + 1e-12).all()
+            xv = bf16_bits_to_f64(vn[t, g]) / vs[g]
+            np.testing.assert_array_equal(vp[page, g, :, slot], oracle.e4m3_encode(xv.astype(np.float32)))
+    written = np.zeros((P, ps), bool)
+    written[4, 15] = written[2, 0] = written[1, 0] = True
+    assert (np.moveaxis(kp, 2, 1)[~written] == 0).all() and (np.moveaxis(vp, 3, 1)[~written] == 0).all()
