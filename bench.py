@@ -460,6 +460,60 @@ def measure_prefill(pa, steps, warmup, peaks):
     return res
 
 
+def measure_fp8_decode(pa, steps, warmup, peaks):
+    """Decode over an FP8 (e4m3) KV cache on the qwen7b_decode shape (batch 32
+    x 8192, Hq=28, Hkv=4, D=128): 256 MiB of K/V codes per step (half the bf16
+    bytes), random finite codes, per-KV-head scales.  L2 is flushed between
+    iterations (the codes are only twice the size of L2)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = workloads.qwen7b_decode(device=dev)
+    P, Hkv, ps, D = case.k_pool.shape
+    g = torch.Generator(device=dev).manual_seed(11)
+    kc = torch.randint(0, 256, (P, Hkv, ps, D), dtype=torch.uint8, device=dev, generator=g)
+    vc = torch.randint(0, 256, (P, Hkv, D, ps), dtype=torch.uint8, device=dev, generator=g)
+    kc[(kc & 0x7F) == 0x7F] = 0  # no NaN codes
+    vc[(vc & 0x7F) == 0x7F] = 0
+    case.k_pool = case.v_pool = None
+    torch.cuda.empty_cache()
+    ks = torch.full((Hkv,), 0.01, dtype=torch.float32, device=dev)
+    vs = torch.full((Hkv,), 0.01, dtype=torch.float32, device=dev)
+    B, Hq, _ = case.q.shape
+    ws = pa.Workspace(pa.decode_workspace_bytes(B, Hq, Hkv, D), dev)
+    out = torch.empty_like(case.q)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def attn():
+        pa.attn_decode_paged_fp8(case.q, kc, vc, ks, vs, case.block_table, case.seq_lens, case.softmax_scale,
+                                 max_seq_len=case.max_seq_len, out=out, workspace=ws)
+
+    for _ in range(warmup):
+        attn()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(steps):
+        _flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        attn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    t = statistics.median(ms)
+    kv = roofline.decode_kv_bytes(case.seq_lens_host, Hkv, D, elem_bytes=1)
+    gbs = kv / (t * 1e-3) / 1e9
+    res = {"workload": "qwen7b_decode on an FP8 (e4m3) cache: batch 32 x 8192-token contexts, Hq=28, Hkv=4, "
+                       "head_dim 128, 16-token pages, per-KV-head scales",
+           "ms": t, "kv_bytes": kv,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]},
+           "tokens_per_s": B / (t * 1e-3), "l2": "flushed (256 MiB write) between iterations", "steps": steps,
+           "launches_per_step": 1}
+    del case, kc, vc, flush
+    torch.cuda.empty_cache()
+    return res
+
+
 def measure_rope_writeback(pa, steps, warmup, peaks):
     """Fused Q/K RMS norm + rotary embedding + KV writeback of the
     varlen_prefill rows (34k tokens: K and V into their pages, the queries
@@ -599,7 +653,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-only", action="store_true", help="skip the prefill and mixed-step measurements")
-    ap.add_argument("--only", choices=["prefill", "mixed", "multiquery", "rope_writeback"], default=None,
+    ap.add_argument("--only", choices=["prefill", "mixed", "multiquery", "rope_writeback", "fp8_decode"],
+                    default=None,
                     help="run just this extra measurement (for profiling); prints its object only")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
@@ -615,7 +670,7 @@ def main(argv=None):
     dev = torch.device("cuda", torch.cuda.current_device())
     if args.only is not None:
         fn = {"prefill": measure_prefill, "mixed": measure_mixed, "multiquery": measure_multiquery,
-              "rope_writeback": measure_rope_writeback}[args.only]
+              "rope_writeback": measure_rope_writeback, "fp8_decode": measure_fp8_decode}[args.only]
         res = fn(pa, args.steps, args.warmup, peaks)
         if rank == 0:
             print(json.dumps({"only": args.only, args.only: res}), flush=True)
@@ -666,7 +721,8 @@ def main(argv=None):
         line["mixed"] = measure_mixed(pa, psteps, 3, peaks)
         line["multiquery"] = measure_multiquery(pa, psteps, 3, peaks)
         line["rope_writeback"] = measure_rope_writeback(pa, psteps, 3, peaks)
-        line["gpu_launches"] += world * psteps * (4 + 3 + 1 + 1)
+        line["fp8_decode"] = measure_fp8_decode(pa, psteps, 3, peaks)
+        line["gpu_launches"] += world * psteps * (4 + 3 + 1 + 1 + 1)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_subprocess()
     if rank == 0:

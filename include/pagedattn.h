@@ -11,6 +11,8 @@
  *                                eagerly as they are produced).
  *   kv_write_paged_rope          the same with the Q/K RMS norm and rotary
  *                                embedding fused in.
+ *   kv_write_paged_fp8,          writeback into, and decode over, an FP8
+ *   attn_decode_paged_fp8        (e4m3) KV cache with per-KV-head scales.
  *   attn_decode_paged            one query row per sequence against its whole
  *                                paged history, split along the KV sequence
  *                                and merged with the log-sum-exp identity
@@ -232,6 +234,45 @@ int kv_write_paged_rope(void* k_pool, void* v_pool, int num_pages, const void* k
                         int page_size, int num_kv_heads, int head_dim, float rope_base,
                         const void* q_norm_weight, const void* k_norm_weight, float norm_eps,
                         int32_t* status, void* stream);
+
+/*
+ * FP8 KV cache ("The Stack Below the Stack, Part 2", closing recipe: FP8 KV).
+ * K and V elements are stored as e4m3 codes (1 byte; the OCP / CUDA E4M3
+ * format: bias 7, 3 mantissa bits, largest finite value 448, no
+ * infinities), which halves the bytes decode reads.  Element x of KV head g
+ * is stored as the code nearest to x / scale[g] (fp32 quotient, round to
+ * nearest even, saturating at +-448) and reads back as code * scale[g].
+ * Layouts (uint8):
+ *   k_pool  [num_pages][num_kv_heads][page_size][head_dim]   (as the bf16 pool)
+ *   v_pool  [num_pages][num_kv_heads][head_dim][page_size]   (transposed inside
+ *           each page block, so the keys of one value column are contiguous)
+ *   k_scale, v_scale  float [num_kv_heads], device; must be > 0
+ * One scale per KV head (not per page): pages are filled one token at a
+ * time by the eager writeback, so a per-page scale would be fixed by the
+ * page's first token.
+ *
+ * kv_write_paged_fp8: the quantising writeback, placement as kv_write_paged
+ * (k_new, v_new bf16 [total_new][num_kv_heads][head_dim]).
+ */
+int kv_write_paged_fp8(void* k_pool, void* v_pool, int num_pages, const void* k_new, const void* v_new,
+                       const float* k_scale, const float* v_scale, const int32_t* cu_seqlens_new,
+                       const int32_t* seq_lens, const int32_t* block_table, int max_pages_per_seq, int batch,
+                       int total_new, int page_size, int num_kv_heads, int head_dim, int32_t* status,
+                       void* stream);
+
+/*
+ * attn_decode_paged over an FP8 cache: same arguments, results and workspace
+ * (pa_decode_workspace_bytes) as attn_decode_paged, with the pools and
+ * scales above.  Scores use q . (code * k_scale[g]) and the output
+ * sum p * code * v_scale[g] / sum p, computed on fp16 tensor cores (every
+ * e4m3 code is exact in fp16; q is rounded to fp16, so |q| must stay below
+ * 65504) with fp32 accumulation.
+ */
+int attn_decode_paged_fp8(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool,
+                          const float* k_scale, const float* v_scale, int num_pages, const int32_t* block_table,
+                          int max_pages_per_seq, const int32_t* seq_lens, int batch, int max_seq_len,
+                          int page_size, int num_q_heads, int num_kv_heads, int head_dim, float softmax_scale,
+                          void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
  * Allocation-free variant of attn_decode_paged.  This entry point has no

@@ -65,6 +65,21 @@ SIGNATURES = {
         c_float, c_void_p, c_void_p, c_float,  # rope_base, q_norm_weight, k_norm_weight, norm_eps
         c_void_p, c_void_p,  # status, stream
     ]),
+    "kv_write_paged_fp8": (c_int, [
+        c_void_p, c_void_p, c_int, c_void_p, c_void_p,  # k_pool, v_pool, num_pages, k_new, v_new
+        c_void_p, c_void_p,  # k_scale, v_scale
+        c_void_p, c_void_p, c_void_p, c_int,  # cu_seqlens_new, seq_lens, block_table, max_pages
+        c_int, c_int, c_int, c_int, c_int,  # batch, total_new, page_size, Hkv, D
+        c_void_p, c_void_p,  # status, stream
+    ]),
+    "attn_decode_paged_fp8": (c_int, [
+        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,  # out, lse, q, k_pool, v_pool
+        c_void_p, c_void_p,  # k_scale, v_scale
+        c_int, c_void_p, c_int,  # num_pages, block_table, max_pages_per_seq
+        c_void_p, c_int, c_int, c_int,  # seq_lens, batch, max_seq_len, page_size
+        c_int, c_int, c_int, c_float,  # Hq, Hkv, D, scale
+        c_void_p, c_size_t, c_void_p, c_void_p,  # workspace, bytes, status, stream
+    ]),
     "kv_write_paged": (c_int, [
         c_void_p, c_void_p, c_int, c_void_p, c_void_p,  # k_pool, v_pool, num_pages, k_new, v_new
         c_void_p, c_void_p, c_void_p, c_int,  # cu_seqlens_new, seq_lens, block_table, max_pages

@@ -44,6 +44,9 @@
 #include "pa_common.cuh"
 #include "pa_host.h"
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include <climits>
 #include <mutex>
 
@@ -57,12 +60,12 @@ constexpr int SBR = 64;        // rows per segment (at most W row blocks)
 constexpr int MIN_CHUNK = 16;  // minimum units per CTA
 constexpr int CTAS_PER_SM = 2;  // two CTAs (8 warps) per SM hide each other's latency
 
-template <int D>
+template <int D, bool FP8 = false>
 struct Cfg {
-    static constexpr int DEPTH = (D == 128) ? 3 : 6;
-    static constexpr int BOXES = D / 64;             // 128-byte-wide column blocks per row
+    static constexpr int DEPTH = FP8 ? 6 : ((D == 128) ? 3 : 6);
+    static constexpr int BOXES = D / 64;             // 128-byte-wide column blocks per row (bf16)
     static constexpr int BOX_BYTES = UNIT * 128;     // 16 rows x 128 bytes
-    static constexpr int UNIT_BYTES = UNIT * D * 2;  // one K or V unit
+    static constexpr int UNIT_BYTES = UNIT * D * (FP8 ? 1 : 2);  // one K or V unit
     static constexpr int STAGE_BYTES = 2 * UNIT_BYTES;
     static constexpr int STAGES_BYTES = W * DEPTH * STAGE_BYTES;
     static constexpr int MSTRIDE = D + 4;  // fp32 row stride of the merge buffer
@@ -74,8 +77,10 @@ struct Params {
     __nv_bfloat16* out;
     float* lse;
     const __nv_bfloat16* q;
-    const __nv_bfloat16* k_pool;
-    const __nv_bfloat16* v_pool;
+    const __nv_bfloat16* k_pool;  // FP8 variant: e4m3 codes, [page][Hkv][page_size][D]
+    const __nv_bfloat16* v_pool;  // FP8 variant: e4m3 codes, [page][Hkv][D][page_size] (transposed)
+    const float* k_scale;         // FP8 variant: [Hkv], K = code * k_scale[g]
+    const float* v_scale;         // FP8 variant: [Hkv], V = code * v_scale[g]
     const int32_t* block_table;
     const int32_t* seq_lens;
     const int32_t* cu_q;  // null: one query row per sequence (row b); else rows cu_q[b] .. cu_q[b+1]
@@ -208,11 +213,11 @@ struct UnitIter {
 // Rows past the sequence end are not copied; their V rows are zeroed (their
 // slots may hold anything and 0 * NaN = NaN), their K rows are masked later.
 // Every call commits exactly one cp.async group (possibly empty).
-template <int D>
+template <int D, bool FP8>
 __device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, uint8_t* stage, int* phys_slot,
                                            int lane, uint64_t policy) {
-    using C = Cfg<D>;
-    constexpr int CH = D / 8;  // 16-byte chunks per row
+    using C = Cfg<D, FP8>;
+    constexpr int CH = D / 8;  // 16-byte chunks per row (bf16)
     const int j = (it.u - it.seg.start) >> it.seg.sh.nrb_shift;  // key block within the sequence
     const int tok0 = j * UNIT;
     const int page = tok0 >> p.ps_shift;
@@ -227,32 +232,81 @@ __device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, 
         if (lane == 0) *phys_slot = phys;
         const size_t row = (size_t)(phys * p.Hkv + it.seg.g) * p.page_size + sub * UNIT;
         const int valid = min(UNIT, it.seg.sh.len - tok0);
-        const char* ksrc = reinterpret_cast<const char*>(p.k_pool + row * D);
-        const char* vsrc = reinterpret_cast<const char*>(p.v_pool + row * D);
         const uint32_t sbase = smem_u32(stage);
+        if constexpr (FP8) {
+            // K: 16 rows of D bytes, 16-byte chunk c of row r at r * D + ((c ^ swz(r)) << 4);
+            // V (transposed in the page): D rows of this unit's 16 key bytes, row d at d * 16
+            constexpr int KCH = D / 16;
+            constexpr int NCH = UNIT * KCH + D;
+            const char* ksrc = reinterpret_cast<const char*>(p.k_pool) + row * D;
+            const char* vsrc = reinterpret_cast<const char*>(p.v_pool) +
+                               (size_t)(phys * p.Hkv + it.seg.g) * D * p.page_size + sub * UNIT;
 #pragma unroll
-        for (int i = 0; i < CH; ++i) {
-            const int q = i * 32 + lane;
-            const int t = q / (UNIT * CH);  // 0 = K, 1 = V
-            const int qq = q - t * UNIT * CH;
-            const int r = qq / CH;
-            const int cc = qq - r * CH;
-            const uint32_t dst = sbase + t * C::UNIT_BYTES + (cc >> 3) * C::BOX_BYTES + r * 128 +
-                                 (((cc & 7) ^ (r & 7)) << 4);
-            if (r < valid) {
-                cp_async_16(dst, (t ? vsrc : ksrc) + r * D * 2 + cc * 16, policy);
-            } else if (t == 1) {
-                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+            for (int i = 0; i < NCH / 32; ++i) {
+                const int q = i * 32 + lane;
+                if (q < UNIT * KCH) {
+                    const int r = q / KCH, c = q - r * KCH;
+                    const int sw = D == 128 ? (r & 7) : 0;
+                    if (r < valid) cp_async_16(sbase + r * D + ((c ^ sw) << 4), ksrc + r * D + c * 16, policy);
+                } else {
+                    const int d = q - UNIT * KCH;  // keys past the end are cleared when the values are read
+                    cp_async_16(sbase + C::UNIT_BYTES + d * 16, vsrc + (size_t)d * p.page_size, policy);
+                }
+            }
+        } else {
+            const char* ksrc = reinterpret_cast<const char*>(p.k_pool + row * D);
+            const char* vsrc = reinterpret_cast<const char*>(p.v_pool + row * D);
+#pragma unroll
+            for (int i = 0; i < CH; ++i) {
+                const int q = i * 32 + lane;
+                const int t = q / (UNIT * CH);  // 0 = K, 1 = V
+                const int qq = q - t * UNIT * CH;
+                const int r = qq / CH;
+                const int cc = qq - r * CH;
+                const uint32_t dst = sbase + t * C::UNIT_BYTES + (cc >> 3) * C::BOX_BYTES + r * 128 +
+                                     (((cc & 7) ^ (r & 7)) << 4);
+                if (r < valid) {
+                    cp_async_16(dst, (t ? vsrc : ksrc) + r * D * 2 + cc * 16, policy);
+                } else if (t == 1) {
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+                }
             }
         }
     }
     cp_async_commit();
 }
 
-template <int D>
+// fp16 tensor-core product (FP8 variant: e4m3 codes are exact in fp16)
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// two e4m3 codes (low byte first) -> two fp16 values (low half first); exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xFFFFu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// FP8 variant, key order inside a 16-key unit: score column c of n-tile t
+// (the mma's n index) is key ((c >> 1) << 2) + 2t + (c & 1), so the four keys a
+// lane feeds to P.V are four consecutive keys, i.e. one 32-bit word of a
+// transposed value row.  The head dimension is likewise permuted: k-index
+// (lane & 3) * 2 + j of k-step kk reads dimension (lane & 3) * D/4 + 4 kk + j,
+// and k-index 8 + (lane & 3) * 2 + j reads that + 2, so each lane's K bytes
+// and Q values are one contiguous run of D/4 dimensions.
+template <int D, bool FP8>
 __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
     decode_kernel(const Params p) {
-    using C = Cfg<D>;
+    using C = Cfg<D, FP8>;
     constexpr int DEPTH = C::DEPTH;
     constexpr int KSTEPS = D / 16;
     constexpr int NT = D / 8;  // n-tiles of O
@@ -353,7 +407,7 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
     // prologue: one cp.async group per stage (empty groups once the warp runs out of units)
     for (int i = 0; i < DEPTH; ++i) {
         if (!it.done) {
-            issue_unit<D>(p, it, my_stages + i * C::STAGE_BYTES, &s_phys[warp][i], lane, policy);
+            issue_unit<D, FP8>(p, it, my_stages + i * C::STAGE_BYTES, &s_phys[warp][i], lane, policy);
             it.u += W;
             it.norm(p, warp);
         } else {
@@ -396,15 +450,37 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
             if (r8ok) lim1 = qlast + i8 + 1;
             const uint32_t* q0 = reinterpret_cast<const uint32_t*>(p.q + ((qrow + (r0ok ? i0 : 0)) * p.Hq + h0) * D);
             const uint32_t* q8 = reinterpret_cast<const uint32_t*>(p.q + ((qrow + (r8ok ? i8 : 0)) * p.Hq + h8) * D);
+            if constexpr (FP8) {
+                // fp16 fragments in the permuted dimension order (see above the kernel)
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-                const int c = (kk * 16 + qc) >> 1;
-                qa[kk][0] = r0ok ? __ldg(q0 + c) : 0u;
-                qa[kk][1] = r8ok ? __ldg(q8 + c) : 0u;
-                qa[kk][2] = r0ok ? __ldg(q0 + c + 4) : 0u;
-                qa[kk][3] = r8ok ? __ldg(q8 + c + 4) : 0u;
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    const int c = ((lane & 3) * (D / 4) + 4 * kk) >> 1;  // bf16 pair index
+                    uint2 v0 = make_uint2(0u, 0u), v8 = make_uint2(0u, 0u);
+                    if (r0ok) v0 = __ldg(reinterpret_cast<const uint2*>(q0 + c));
+                    if (r8ok) v8 = __ldg(reinterpret_cast<const uint2*>(q8 + c));
+                    const __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&v0.x);
+                    const __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&v0.y);
+                    const __nv_bfloat162 e = *reinterpret_cast<__nv_bfloat162*>(&v8.x);
+                    const __nv_bfloat162 f = *reinterpret_cast<__nv_bfloat162*>(&v8.y);
+                    qa[kk][0] = pack_f16x2(__low2float(a), __high2float(a));
+                    qa[kk][2] = pack_f16x2(__low2float(b), __high2float(b));
+                    qa[kk][1] = pack_f16x2(__low2float(e), __high2float(e));
+                    qa[kk][3] = pack_f16x2(__low2float(f), __high2float(f));
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    const int c = (kk * 16 + qc) >> 1;
+                    qa[kk][0] = r0ok ? __ldg(q0 + c) : 0u;
+                    qa[kk][1] = r8ok ? __ldg(q8 + c) : 0u;
+                    qa[kk][2] = r0ok ? __ldg(q0 + c + 4) : 0u;
+                    qa[kk][3] = r8ok ? __ldg(q8 + c + 4) : 0u;
+                }
             }
         }
+        // score scale (log2 domain) and value scale of this KV head
+        const float sl = FP8 ? p.scale_log2 * __ldg(p.k_scale + cs.g) : p.scale_log2;
+        const float vsc = FP8 ? __ldg(p.v_scale + cs.g) : 1.f;
         float o[NT][4];
 #pragma unroll
         for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -426,6 +502,31 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
                 // dependent mma latency; summed below
                 float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
                 float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                if constexpr (FP8) {
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const int krow = ((qr >> 1) << 2) + 2 * t + (qr & 1);  // key of n-tile t, column qr
+                        uint32_t w[D / 16];  // this lane's D/4 bytes of that key row
+#pragma unroll
+                        for (int m = 0; m < D / 64; ++m) {
+                            const int c = (lane & 3) * (D / 64) + m;
+                            const int sw = D == 128 ? (krow & 7) : 0;
+                            uint32_t r0, r1, r2, r3;
+                            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                         : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                                         : "r"(kb + krow * D + ((c ^ sw) << 4)));
+                            w[4 * m] = r0;
+                            w[4 * m + 1] = r1;
+                            w[4 * m + 2] = r2;
+                            w[4 * m + 3] = r3;
+                        }
+#pragma unroll
+                        for (int kk = 0; kk < KSTEPS; ++kk) {
+                            const uint32_t b0 = e4m3x2_to_f16x2(w[kk]), b1 = e4m3x2_to_f16x2(w[kk] >> 16);
+                            mma_16816_f16((kk & 1) ? s2[t] : s[t], qa[kk], b0, b1);
+                        }
+                    }
+                } else {
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; ++kk) {
                     const int dch = kk * 2 + k_dsel;
@@ -441,6 +542,7 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
                         mma_16816(s[1], qa[kk], b2, b3);
                     }
                 }
+                }
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -451,8 +553,8 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
                 for (int j = 0; j < 2; ++j) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int key = j * 8 + qc + (e & 1);
-                        x[j][e] = key < ((e & 2) ? vis1 : vis0) ? s[j][e] * p.scale_log2 : -INFINITY;
+                        const int key = FP8 ? (lane & 3) * 4 + 2 * j + (e & 1) : j * 8 + qc + (e & 1);
+                        x[j][e] = key < ((e & 2) ? vis1 : vis0) ? s[j][e] * sl : -INFINITY;
                     }
                 }
                 float rm0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
@@ -488,6 +590,27 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
                     }
                 }
                 uint32_t pa[4];
+                if constexpr (FP8) {
+                    pa[0] = pack_f16x2(pr[0][0], pr[0][1]);
+                    pa[1] = pack_f16x2(pr[0][2], pr[0][3]);
+                    pa[2] = pack_f16x2(pr[1][0], pr[1][1]);
+                    pa[3] = pack_f16x2(pr[1][2], pr[1][3]);
+                    // O += P V: value row d of the transposed unit holds the 16 keys' codes;
+                    // this lane's keys (lane & 3) * 4 .. + 3 are one word.  Keys past the
+                    // sequence end may hold any code (0 * NaN = NaN), so they are cleared.
+                    const int valid = min(UNIT, cs.sh.len - tok0);
+                    uint32_t keep = 0u;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+                        if ((lane & 3) * 4 + b < valid) keep |= 0xFFu << (8 * b);
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        uint32_t w;
+                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(vb + (n * 8 + qr) * 16 + (lane & 3) * 4));
+                        w &= keep;
+                        mma_16816_f16(o[n], pa, e4m3x2_to_f16x2(w), e4m3x2_to_f16x2(w >> 16));
+                    }
+                } else {
                 pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
                 pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
                 pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
@@ -503,11 +626,12 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
                     mma_16816(o[2 * jj], pa, b0, b1);
                     mma_16816(o[2 * jj + 1], pa, b2, b3);
                 }
+                }
             }
             __syncwarp();  // every lane is done reading this stage
             ++consumed;
             if (!it.done) {
-                issue_unit<D>(p, it, my_stages + st * C::STAGE_BYTES, &s_phys[warp][st], lane, policy);
+                issue_unit<D, FP8>(p, it, my_stages + st * C::STAGE_BYTES, &s_phys[warp][st], lane, policy);
                 it.u += W;
                 it.norm(p, warp);
             } else {
@@ -586,7 +710,7 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
                 const int d4 = idx - rr * (D / 4);
                 const float4 acc = *reinterpret_cast<const float4*>(merge_o + rr * C::MSTRIDE + d4 * 4);
                 const float L = s_L[rr];
-                const float inv = L > 0.f ? 1.f / L : 0.f;
+                const float inv = L > 0.f ? vsc / L : 0.f;  // the value scale folds in here
                 if (single) {
                     const int f = row_sb + r * cs.sh.R + rr;
                     const int i = f / p.group;
@@ -723,11 +847,14 @@ namespace dec {
 // (row b).  Otherwise entries with 1 <= q_len <= qmax are served (rows
 // cu_q[b] ..), q_len in (qmax, qcap] is reported as PA_ERR_BAD_LEN and
 // longer entries are left to the prefill kernel.
-int launch_decode(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool, int num_pages,
-                  const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
-                  const int32_t* cu_q, int total_q, int qmax, int qcap, int batch, int max_seq_len, int page_size,
-                  int num_q_heads, int num_kv_heads, int head_dim, float softmax_scale, void* workspace,
-                  size_t workspace_bytes, int32_t* status, void* stream) {
+// k_scale / v_scale non-null: the pools hold e4m3 codes (V transposed per page block).
+static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool,
+                            const float* k_scale, const float* v_scale, int num_pages, const int32_t* block_table,
+                            int max_pages_per_seq, const int32_t* seq_lens, const int32_t* cu_q, int total_q,
+                            int qmax, int qcap, int batch, int max_seq_len, int page_size, int num_q_heads,
+                            int num_kv_heads, int head_dim, float softmax_scale, void* workspace,
+                            size_t workspace_bytes, int32_t* status, void* stream) {
+    const bool fp8 = k_scale != nullptr;
     if (batch < 0 || max_seq_len < 0 || total_q < 0) return PA_ERR_SHAPE;
     if (qmax < 1 || qmax > kDecodeMaxQ || (cu_q == nullptr && qmax != 1)) return PA_ERR_SHAPE;
     int rc = check_common_shapes(page_size, num_q_heads, num_kv_heads, head_dim);
@@ -775,6 +902,8 @@ int launch_decode(void* out, float* lse, const void* q, const void* k_pool, cons
     prm.q = static_cast<const __nv_bfloat16*>(q);
     prm.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
     prm.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
+    prm.k_scale = k_scale;
+    prm.v_scale = v_scale;
     prm.block_table = block_table;
     prm.seq_lens = seq_lens;
     prm.cu_q = cu_q;
@@ -799,22 +928,47 @@ int launch_decode(void* out, float* lse, const void* q, const void* k_pool, cons
     prm.scale_log2 = softmax_scale * kLog2e;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (head_dim == 128) {
-        constexpr int smem = dec::Cfg<128>::SMEM_BYTES;
-        if (set_smem_limit_once((const void*)dec::decode_kernel<128>, smem, dev.device, 0) != PA_OK)
-            return PA_ERR_CUDA;
-        dec::decode_kernel<128><<<grid, dec::W * 32, smem, st>>>(prm);
-    } else {
-        constexpr int smem = dec::Cfg<64>::SMEM_BYTES;
-        if (set_smem_limit_once((const void*)dec::decode_kernel<64>, smem, dev.device, 1) != PA_OK)
-            return PA_ERR_CUDA;
-        dec::decode_kernel<64><<<grid, dec::W * 32, smem, st>>>(prm);
-    }
+    auto go = [&](auto kernel, int smem, int slot) {
+        if (set_smem_limit_once((const void*)kernel, smem, dev.device, slot) != PA_OK) return PA_ERR_CUDA;
+        kernel<<<grid, W * 32, smem, st>>>(prm);
+        return PA_OK;
+    };
+    if (head_dim == 128)
+        rc = fp8 ? go(decode_kernel<128, true>, Cfg<128, true>::SMEM_BYTES, 5)
+                 : go(decode_kernel<128, false>, Cfg<128, false>::SMEM_BYTES, 0);
+    else
+        rc = fp8 ? go(decode_kernel<64, true>, Cfg<64, true>::SMEM_BYTES, 6)
+                 : go(decode_kernel<64, false>, Cfg<64, false>::SMEM_BYTES, 1);
+    if (rc != PA_OK) return rc;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int launch_decode(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool, int num_pages,
+                  const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
+                  const int32_t* cu_q, int total_q, int qmax, int qcap, int batch, int max_seq_len, int page_size,
+                  int num_q_heads, int num_kv_heads, int head_dim, float softmax_scale, void* workspace,
+                  size_t workspace_bytes, int32_t* status, void* stream) {
+    return launch_decode_kv(out, lse, q, k_pool, v_pool, nullptr, nullptr, num_pages, block_table,
+                            max_pages_per_seq, seq_lens, cu_q, total_q, qmax, qcap, batch, max_seq_len, page_size,
+                            num_q_heads, num_kv_heads, head_dim, softmax_scale, workspace, workspace_bytes, status,
+                            stream);
 }
 
 }  // namespace dec
 }  // namespace pa
+
+extern "C" int attn_decode_paged_fp8(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool,
+                                     const float* k_scale, const float* v_scale, int num_pages,
+                                     const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
+                                     int batch, int max_seq_len, int page_size, int num_q_heads, int num_kv_heads,
+                                     int head_dim, float softmax_scale, void* workspace, size_t workspace_bytes,
+                                     int32_t* status, void* stream) {
+    if (batch > 0 && (k_scale == nullptr || v_scale == nullptr)) return PA_ERR_NULL;
+    return dec::launch_decode_kv(out, lse, q, k_pool, v_pool, k_scale, v_scale, num_pages, block_table,
+                                 max_pages_per_seq, seq_lens, nullptr, batch, 1, 1, batch, max_seq_len, page_size,
+                                 num_q_heads, num_kv_heads, head_dim, softmax_scale, workspace, workspace_bytes,
+                                 status, stream);
+}
 
 extern "C" int attn_decode_paged(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool,
                                  int num_pages, const int32_t* block_table, int max_pages_per_seq,

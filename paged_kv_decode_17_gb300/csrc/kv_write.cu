@@ -17,10 +17,18 @@
 // reduced exactly: the host passes frac(theta_i / 2 pi) as a 64-bit binary
 // fraction, the position times it (mod 2^64) is the angle in turns, and
 // sincospif turns its top 24 bits into cos and sin.
+//
+// kv_write_paged_fp8 is the writeback of an FP8 (e4m3) cache ("The Stack
+// Below the Stack, Part 2", closing recipe: FP8 KV): element x of KV head g
+// is stored as the e4m3 code nearest to x / scale[g] (fp32 quotient, round to
+// nearest even, saturating at +-448).  K rows keep the [page][Hkv][slot][D]
+// layout; V is transposed inside each page block, [page][Hkv][D][slot], so
+// that the decode kernel reads the keys of one value column as one word.
 #include "pa_common.cuh"
 #include "pa_host.h"
 
 #include <cmath>
+#include <cuda_fp8.h>
 
 namespace pa {
 namespace kvw {
@@ -227,6 +235,70 @@ __global__ void __launch_bounds__(kWarps * 32) kv_write_rope_kernel(const __grid
     }
 }
 
+// One warp per new token; lane l quantises elements [l * D/32, (l+1) * D/32) of every head row.
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32) kv_write_fp8_kernel(
+    uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool, const __nv_bfloat16* __restrict__ k_new,
+    const __nv_bfloat16* __restrict__ v_new, const float* __restrict__ k_scale, const float* __restrict__ v_scale,
+    const int32_t* __restrict__ cu_new, const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
+    int num_pages, int max_pages, int batch, int total_new, int page_size, int num_kv_heads, int32_t* status) {
+    constexpr int EPL = D / 32;  // elements per lane (2 or 4)
+    const int lane = threadIdx.x & 31;
+    const int nwarps = gridDim.x * kWarps;
+    for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < total_new; t += nwarps) {
+        int lo = 0, hi = batch - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(cu_new + mid) <= t) lo = mid; else hi = mid - 1;
+        }
+        const int b = lo;
+        const int n_b = __ldg(cu_new + b + 1) - __ldg(cu_new + b);
+        const int i = t - __ldg(cu_new + b);
+        const int pos = __ldg(seq_lens + b) - n_b + i;
+        if (n_b <= 0 || i >= n_b || pos < 0 || pos >= max_pages * page_size) {
+            if (lane == 0) report(status, PA_ERR_BAD_LEN);
+            continue;
+        }
+        const int phys = __ldg(block_table + (size_t)b * max_pages + pos / page_size);
+        if (phys < 0 || phys >= num_pages) {
+            if (lane == 0) report(status, PA_ERR_BAD_PAGE);
+            continue;
+        }
+        const int slot = pos % page_size;
+        for (int g = 0; g < num_kv_heads; ++g) {
+            const float ks = __ldg(k_scale + g), vs = __ldg(v_scale + g);
+            const size_t src = ((size_t)t * num_kv_heads + g) * D + lane * EPL;
+            const size_t blk = (size_t)phys * num_kv_heads + g;
+            float kx[EPL], vx[EPL];
+#pragma unroll
+            for (int e = 0; e < EPL; e += 2) {
+                const __nv_bfloat162 kk = *reinterpret_cast<const __nv_bfloat162*>(k_new + src + e);
+                const __nv_bfloat162 vv = *reinterpret_cast<const __nv_bfloat162*>(v_new + src + e);
+                kx[e] = __low2float(kk) / ks;
+                kx[e + 1] = __high2float(kk) / ks;
+                vx[e] = __low2float(vv) / vs;
+                vx[e + 1] = __high2float(vv) / vs;
+            }
+            uint32_t kcodes = 0;
+#pragma unroll
+            for (int e = 0; e < EPL; e += 2) {
+                const uint32_t kc = __nv_cvt_float2_to_fp8x2(make_float2(kx[e], kx[e + 1]), __NV_SATFINITE, __NV_E4M3);
+                const uint32_t vc = __nv_cvt_float2_to_fp8x2(make_float2(vx[e], vx[e + 1]), __NV_SATFINITE, __NV_E4M3);
+                kcodes |= (kc & 0xFFFFu) << (8 * e);
+                // V is transposed: element d of the row goes to row d of the page block, column slot
+                uint8_t* vcol = v_pool + (blk * D + lane * EPL + e) * page_size + slot;
+                vcol[0] = (uint8_t)(vc & 0xFF);
+                vcol[page_size] = (uint8_t)((vc >> 8) & 0xFF);
+            }
+            uint8_t* krow = k_pool + (blk * page_size + slot) * D + lane * EPL;
+            if constexpr (EPL == 4)
+                *reinterpret_cast<uint32_t*>(krow) = kcodes;
+            else
+                *reinterpret_cast<uint16_t*>(krow) = (uint16_t)kcodes;
+        }
+    }
+}
+
 }  // namespace kvw
 }  // namespace pa
 
@@ -317,5 +389,42 @@ extern "C" int kv_write_paged_rope(void* k_pool, void* v_pool, int num_pages, co
         kvw::kv_write_rope_kernel<128><<<grid, kvw::kWarps * 32, 0, st>>>(prm);
     else
         kvw::kv_write_rope_kernel<64><<<grid, kvw::kWarps * 32, 0, st>>>(prm);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" int kv_write_paged_fp8(void* k_pool, void* v_pool, int num_pages, const void* k_new, const void* v_new,
+                                  const float* k_scale, const float* v_scale, const int32_t* cu_seqlens_new,
+                                  const int32_t* seq_lens, const int32_t* block_table, int max_pages_per_seq,
+                                  int batch, int total_new, int page_size, int num_kv_heads, int head_dim,
+                                  int32_t* status, void* stream) {
+    using namespace pa;
+    if (batch < 0 || total_new < 0) return PA_ERR_SHAPE;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_SHAPE;
+    if (page_size < 16 || page_size > 256 || (page_size & (page_size - 1)) != 0) return PA_ERR_SHAPE;
+    if (num_kv_heads < 1) return PA_ERR_SHAPE;
+    if (batch == 0 || total_new == 0) return PA_OK;
+    if (!k_pool || !v_pool || !k_new || !v_new || !k_scale || !v_scale || !cu_seqlens_new || !seq_lens ||
+        !block_table)
+        return PA_ERR_NULL;
+    if (num_pages < 1 || max_pages_per_seq < 1) return PA_ERR_SHAPE;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_new) || !aligned16(v_new)) return PA_ERR_SHAPE;
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc != PA_OK) return rc;
+    const int blocks_needed = (total_new + kvw::kWarps - 1) / kvw::kWarps;
+    const int grid = blocks_needed < dev.sm_count * 16 ? blocks_needed : dev.sm_count * 16;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    auto* kp = static_cast<uint8_t*>(k_pool);
+    auto* vp = static_cast<uint8_t*>(v_pool);
+    auto* kn = static_cast<const __nv_bfloat16*>(k_new);
+    auto* vn = static_cast<const __nv_bfloat16*>(v_new);
+    if (head_dim == 128)
+        kvw::kv_write_fp8_kernel<128><<<grid, kvw::kWarps * 32, 0, st>>>(
+            kp, vp, kn, vn, k_scale, v_scale, cu_seqlens_new, seq_lens, block_table, num_pages, max_pages_per_seq,
+            batch, total_new, page_size, num_kv_heads, status);
+    else
+        kvw::kv_write_fp8_kernel<64><<<grid, kvw::kWarps * 32, 0, st>>>(
+            kp, vp, kn, vn, k_scale, v_scale, cu_seqlens_new, seq_lens, block_table, num_pages, max_pages_per_seq,
+            batch, total_new, page_size, num_kv_heads, status);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

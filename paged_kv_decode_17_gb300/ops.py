@@ -161,6 +161,84 @@ def kv_write_paged_rope(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch
     _lib.check(rc, "kv_write_paged_rope")
 
 
+def _need_fp8_pools(k_pool, v_pool, k_scale, v_scale):
+    _need(k_pool, "k_pool", torch.uint8, 4)
+    _need(v_pool, "v_pool", torch.uint8, 4)
+    _need(k_scale, "k_scale", torch.float32, 1)
+    _need(v_scale, "v_scale", torch.float32, 1)
+    P, Hkv, ps, D = k_pool.shape
+    if v_pool.shape != (P, Hkv, D, ps):
+        raise ValueError("v_pool must be [num_pages][Hkv][head_dim][page_size] (transposed per page block)")
+    if k_scale.shape[0] != Hkv or v_scale.shape[0] != Hkv:
+        raise ValueError("k_scale / v_scale must have one entry per KV head")
+    return P, Hkv, ps, D
+
+
+def kv_write_paged_fp8(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                       k_scale: torch.Tensor, v_scale: torch.Tensor, cu_seqlens_new: torch.Tensor,
+                       seq_lens: torch.Tensor, block_table: torch.Tensor, status: Optional[torch.Tensor] = None,
+                       stream=None) -> None:
+    """Quantise the new K/V rows to e4m3 (x / scale[g], round to nearest even,
+    saturating) and write them into the FP8 pools (V transposed per page block)."""
+    lib = _lib.load()
+    P, Hkv, ps, D = _need_fp8_pools(k_pool, v_pool, k_scale, v_scale)
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(cu_seqlens_new, "cu_seqlens_new", torch.int32, 1)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(block_table, "block_table", torch.int32, 2)
+    if k_new.shape != v_new.shape or k_new.shape[1:] != (Hkv, D):
+        raise ValueError("k_new / v_new must be [total_new][Hkv][head_dim]")
+    B = seq_lens.shape[0]
+    if cu_seqlens_new.shape[0] != B + 1 or block_table.shape[0] != B:
+        raise ValueError("cu_seqlens_new must have batch+1 entries and block_table batch rows")
+    rc = lib.kv_write_paged_fp8(_ptr(k_pool), _ptr(v_pool), P, _ptr(k_new), _ptr(v_new), _ptr(k_scale),
+                                _ptr(v_scale), _ptr(cu_seqlens_new), _ptr(seq_lens), _ptr(block_table),
+                                block_table.shape[1], B, k_new.shape[0], ps, Hkv, D, _ptr(status),
+                                _stream_handle(stream))
+    _lib.check(rc, "kv_write_paged_fp8")
+
+
+def attn_decode_paged_fp8(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, k_scale: torch.Tensor,
+                          v_scale: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                          softmax_scale: Optional[float] = None, *, max_seq_len: Optional[int] = None,
+                          out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                          return_lse: bool = False, workspace: Optional[Workspace] = None,
+                          status: Optional[torch.Tensor] = None, stream=None):
+    """Split-K paged decode over an FP8 (e4m3) cache with per-KV-head scales."""
+    lib = _lib.load()
+    _need(q, "q", torch.bfloat16, 3)
+    P, Hkv, ps, D = _need_fp8_pools(k_pool, v_pool, k_scale, v_scale)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, Hq, Dq = q.shape
+    if Dq != D:
+        raise ValueError("inconsistent head_dim")
+    if block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_table / seq_lens must have batch rows")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if max_seq_len is None:
+        max_seq_len = block_table.shape[1] * ps
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.bfloat16, 3)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    need = int(lib.pa_decode_workspace_bytes(B, Hq, Hkv, D)) if B > 0 else 0
+    if workspace is None:
+        workspace = _cached_ws("decode", need, q.device)
+    rc = lib.attn_decode_paged_fp8(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
+                                   _ptr(v_scale), P, _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B,
+                                   int(max_seq_len), ps, Hq, Hkv, D, float(softmax_scale), workspace.ptr,
+                                   workspace.nbytes, _ptr(status), _stream_handle(stream))
+    _lib.check(rc, "attn_decode_paged_fp8")
+    return (out, lse) if return_lse else out
+
+
 def attn_decode_paged(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor,
                       seq_lens: torch.Tensor, softmax_scale: Optional[float] = None, *,
                       max_seq_len: Optional[int] = None, out: Optional[torch.Tensor] = None,

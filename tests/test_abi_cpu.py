@@ -146,3 +146,28 @@ def test_kv_write_rope_host_validation(lib):
     a = list(args)
     a[11] = 0  # empty batch
     assert f(*a) == 0
+
+
+def test_fp8_host_validation(lib):
+    P = 1 << 20
+    w = lib.kv_write_paged_fp8
+    # k_pool, v_pool, num_pages, k_new, v_new, k_scale, v_scale, cu, lens, bt, maxp, batch, total, ps, Hkv, D
+    args = [P, P, 8, P, P, P, P, P, P, P, 4, 2, 10, 16, 2, 64, None, None]
+    a = list(args)
+    a[15] = 96
+    assert w(*a) == -2
+    a = list(args)
+    a[5] = None  # k_scale
+    assert w(*a) == -1
+    a = list(args)
+    a[11] = 0
+    assert w(*a) == 0
+    d = lib.attn_decode_paged_fp8
+    # out, lse, q, k, v, k_scale, v_scale, num_pages, bt, maxp, lens, batch, max_seq_len, ps, hq, hkv, d, scale, ...
+    args = [P, None, P, P, P, P, P, 16, P, 8, P, 2, 100, 16, 4, 2, 64, 0.125, None, 0, None, None]
+    a = list(args)
+    a[6] = None  # v_scale
+    assert d(*a) == -1
+    a = list(args)
+    a[14] = 3  # Hq not a multiple of Hkv
+    assert d(*a) == -2
