@@ -13,7 +13,7 @@
 // * Work item = one 128-row query tile of one sequence for the query heads of
 //   one KV head.  A small plan kernel lists the query tiles sorted by their
 //   number of key tiles, heaviest first.  The main kernel is persistent: each
-//   thread-block cluster (up to 4 CTAs, one per SM) walks that list
+//   thread-block cluster (up to 2 CTAs, one per SM) walks that list
 //   round-robin; the CTAs of a cluster take the head pairs of the same item,
 //   so each K/V tile is fetched once per cluster (TMA multicast).  Tensor
 //   memory, barriers and the cluster are set up once per CTA, and the next
@@ -37,7 +37,12 @@
 //   exponentials are taken against the older, smaller maximum, which keeps
 //   them <= 2^8 and the result exact, because the final division uses the
 //   same reference maximum for numerator and denominator.  At the end of an
-//   item they normalise O and store it.
+//   item they normalise O; a full 128-row tile goes as bf16 into the head's
+//   P buffer (free once the last P.V is done), in the swizzled layout of a
+//   TMA box, and one thread writes it out with TMA tensor stores, so the
+//   warps move on to the next item at once (the next P store waits only for
+//   the store to have read the buffer).  A partial tile is stored directly,
+//   row by row, since a whole box would overwrite the next sequence's rows.
 // Every wait is bounded; a timeout sets a CTA-wide abort flag, records
 // PA_ERR_TIMEOUT and all roles fall through to a clean exit.
 #include "pa_common.cuh"
@@ -59,7 +64,7 @@ constexpr int UPT = BN / 16; // 16-key page blocks per KV tile
 #define PA_PF_NV 2
 #endif
 #ifndef PA_PF_MAX_CLUSTER
-#define PA_PF_MAX_CLUSTER 4
+#define PA_PF_MAX_CLUSTER 2
 #endif
 // K and V tiles go through separate rings: the next K tile only waits for the
 // current scores (S) to be computed, not for the previous P.V to finish.
@@ -126,6 +131,8 @@ struct Shared {
     uint64_t s_full[2], s_free[2];
     uint64_t p_ready[2], pv_done[2];
     uint64_t o_free[2];                  // per head: the epilogue has read O out of TMEM
+    uint64_t o_staged[2];                // per head: all 128 rows of O/l are in shared memory
+    uint64_t o_read[2];                  // per head: the TMA store has read them (P buffer free again)
     uint64_t v_tail;                     // TMA copies of a V tile that runs past the sequence end land here
     uint64_t item_full[2], item_empty[2];
     uint32_t tmem_base;
@@ -183,6 +190,18 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
 }
+
+// TMA tensor store of one 64-column x 128-row box of O (3-D map over out [rows][Hq][D]).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* smem_src, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // number of 128-row query tiles of sequence b served by the prefill kernel (0 if none)
 __device__ __forceinline__ int seq_tiles(const int32_t* cu_q, const int32_t* seq_lens, int b, int cap,
@@ -244,7 +263,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) prefill_plan_kernel(const int32_
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                   const __grid_constant__ CUtensorMap vmap, const Params p) {
+                   const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+                   const Params p) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -266,6 +286,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(&sh.p_ready[h], 4 * 32);
             mbar_init(&sh.pv_done[h], 1);
             mbar_init(&sh.o_free[h], 4 * 32);
+            mbar_init(&sh.o_staged[h], 4 * 32);
+            mbar_init(&sh.o_read[h], 1);
             mbar_init(&sh.item_full[h], 1);
             mbar_init(&sh.item_empty[h], 2 + 8);  // lane 0 of both MMA warps and of the 8 softmax warps
         }
@@ -558,7 +580,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t t_s = tmem + lane_off + C::TM_S0 + hh * BN;
         const uint32_t t_o = tmem + lane_off + C::TM_O0 + hh * D;
         uint8_t* prow = sP + hh * C::P_BYTES + r * 128;
+        const bool leader = quarter == 0 && lane == 0;
         int J = 0;  // tiles of this head so far (phase counter, shared with the MMA thread)
+        int nst = 0;               // O tiles written out through the P buffer by TMA stores
+        bool store_pending = false;  // the last of them may still be reading the P buffer
         bool ok = true;
         for (int k = 0; ok; ++k) {
             ok = __all_sync(0xffffffffu, wait_ab(&sh.item_full[k & 1], (k >> 1) & 1, sh, p.status));
@@ -646,6 +671,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         ok = __all_sync(0xffffffffu, wait_ab(&sh.pv_done[hh], (jj - 1) & 1, sh, p.status));
                         if (!ok) break;
                     }
+                    // the previous item's O may still be leaving the P buffer through a TMA store
+                    if (store_pending) {
+                        if (leader) {
+                            bulk_wait_read_all();
+                            mbar_arrive(&sh.o_read[hh]);
+                        }
+                        ok = __all_sync(0xffffffffu, wait_ab(&sh.o_read[hh], (nst - 1) & 1, sh, p.status));
+                        if (!ok) break;
+                        store_pending = false;
+                    }
                     // P (bf16) to shared memory in the 128-byte-swizzled K-major layout
 #pragma unroll
                     for (int q = 0; q < BN / 8; ++q) {
@@ -666,6 +701,40 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const float inv = l > 0.f ? 1.f / l : 0.f;
                     const bool store = r < itm.rows_valid;
                     const int h = itm.h0 + hh;
+                    if (itm.rows_valid == BM) {
+                        // full tile: O/l -> bf16 into the P buffer (free: the last P.V is done) in the
+                        // swizzled layout of a 64-column TMA box, then one thread stores it with TMA
+#pragma unroll 1
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t o[32];
+                            tc::ld_32x32b_x32(t_o + c0, o);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                uint32_t pkd[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    pkd[e] = pack_bf16x2(__uint_as_float(o[8 * i + 2 * e]) * inv,
+                                                         __uint_as_float(o[8 * i + 2 * e + 1]) * inv);
+                                const int c = ((c0 & 63) >> 3) + i;  // 16-byte chunk within the 64-column block
+                                *reinterpret_cast<uint4*>(prow + (c0 >> 6) * C::P_KB + ((c ^ (r & 7)) << 4)) =
+                                    make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive(&sh.o_staged[hh]);
+                        if (leader) {
+                            ok = wait_ab(&sh.o_staged[hh], nst & 1, sh, p.status);
+                            if (ok) {
+#pragma unroll
+                                for (int kb = 0; kb < C::KB; ++kb)
+                                    tma_store_3d(&omap, sP + hh * C::P_BYTES + kb * C::P_KB, kb * 64, h, itm.row0);
+                                bulk_commit();
+                            }
+                        }
+                        ++nst;
+                        store_pending = true;
+                    } else {
                     __nv_bfloat16* orow = p.out + ((size_t)(itm.row0 + r) * p.Hq + h) * D;
 #pragma unroll 1
                     for (int c0 = 0; c0 < D; c0 += 32) {
@@ -684,6 +753,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                 dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
                         }
                     }
+                    }
                     if (store && p.lse != nullptr)
                         p.lse[(size_t)(itm.row0 + r) * p.Hq + h] = l > 0.f ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
                     tc::fence_before_sync();
@@ -694,6 +764,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.item_empty[k & 1]);
         }
+        if (leader && nst > 0) bulk_wait_all();  // the shared-memory source must outlive the stores
     }
 
     tc::fence_before_sync();
@@ -741,7 +812,8 @@ int max_clusters(int device, int CS, cudaLaunchConfig_t cfg) {
 
 template <int D>
 int launch_persistent(cudaLaunchConfig_t& cfg, int device, int CS, long long items_upper, const CUtensorMap& qmap,
-                      const CUtensorMap& kmap, const CUtensorMap& vmap, const pf::Params& prm) {
+                      const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& omap,
+                      const pf::Params& prm) {
     cfg.dynamicSmemBytes = pf::Cfg<D>::SMEM_BYTES;
     if (set_smem_limit_once((const void*)pf::prefill_kernel<D>, pf::Cfg<D>::SMEM_BYTES, device, D == 128 ? 2 : 3) !=
         PA_OK)
@@ -751,7 +823,7 @@ int launch_persistent(cudaLaunchConfig_t& cfg, int device, int CS, long long ite
     if (nc <= 0) return PA_ERR_CUDA;
     if (nc > items_upper) nc = items_upper;
     cfg.gridDim = dim3((unsigned)(nc * CS), 1, 1);
-    return cudaLaunchKernelEx(&cfg, pf::prefill_kernel<D>, qmap, kmap, vmap, prm) == cudaSuccess ? PA_OK
+    return cudaLaunchKernelEx(&cfg, pf::prefill_kernel<D>, qmap, kmap, vmap, omap, prm) == cudaSuccess ? PA_OK
                                                                                                  : PA_ERR_CUDA;
 }
 }  // namespace
@@ -815,8 +887,9 @@ extern "C" int attn_prefill_varlen_causal(void* out, float* lse, const void* q, 
         cu_seqlens_q, seq_lens, batch, max_pages_per_seq * page_size, max_cost, tiles, n_tiles, status);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
 
-    CUtensorMap qmap, kmap, vmap;
+    CUtensorMap qmap, kmap, vmap, omap;
     if (encode_q_map(&qmap, q, total_q, num_q_heads, head_dim) != PA_OK) return PA_ERR_CUDA;
+    if (encode_q_map(&omap, out, total_q, num_q_heads, head_dim) != PA_OK) return PA_ERR_CUDA;
     if (encode_rows_map(&kmap, k_pool, (uint64_t)pool_rows, head_dim, 64, 16) != PA_OK) return PA_ERR_CUDA;
     if (encode_rows_map(&vmap, v_pool, (uint64_t)pool_rows, head_dim, 64, 16) != PA_OK) return PA_ERR_CUDA;
 
@@ -850,6 +923,7 @@ extern "C" int attn_prefill_varlen_causal(void* out, float* lse, const void* q, 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (head_dim == 128) return launch_persistent<128>(cfg, dev.device, CS, items_upper, qmap, kmap, vmap, prm);
-    return launch_persistent<64>(cfg, dev.device, CS, items_upper, qmap, kmap, vmap, prm);
+    if (head_dim == 128)
+        return launch_persistent<128>(cfg, dev.device, CS, items_upper, qmap, kmap, vmap, omap, prm);
+    return launch_persistent<64>(cfg, dev.device, CS, items_upper, qmap, kmap, vmap, omap, prm);
 }
