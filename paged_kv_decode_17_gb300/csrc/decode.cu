@@ -58,11 +58,20 @@ constexpr int UNIT = 16;       // tokens per unit
 constexpr int RB = 16;         // rows per row block (mma M)
 constexpr int SBR = 64;        // rows per segment (at most W row blocks)
 constexpr int MIN_CHUNK = 16;  // minimum units per CTA
-constexpr int CTAS_PER_SM = 2;  // two CTAs (8 warps) per SM hide each other's latency
+#ifndef PA_DEC_CTAS_PER_SM
+#define PA_DEC_CTAS_PER_SM 2
+#endif
+#ifndef PA_DEC_DEPTH_BF16
+#define PA_DEC_DEPTH_BF16 3
+#endif
+#ifndef PA_DEC_DEPTH_FP8
+#define PA_DEC_DEPTH_FP8 6
+#endif
+constexpr int CTAS_PER_SM = PA_DEC_CTAS_PER_SM;  // CTAs (of 4 warps) per SM: they hide each other's latency
 
 template <int D, bool FP8 = false>
 struct Cfg {
-    static constexpr int DEPTH = FP8 ? 6 : ((D == 128) ? 3 : 6);
+    static constexpr int DEPTH = FP8 ? PA_DEC_DEPTH_FP8 : ((D == 128) ? PA_DEC_DEPTH_BF16 : 2 * PA_DEC_DEPTH_BF16);
     static constexpr int BOXES = D / 64;             // 128-byte-wide column blocks per row (bf16)
     static constexpr int BOX_BYTES = UNIT * 128;     // 16 rows x 128 bytes
     static constexpr int UNIT_BYTES = UNIT * D * (FP8 ? 1 : 2);  // one K or V unit
@@ -296,6 +305,21 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// 8x8 b16 transpose across the warp (lane holds row lane/4, columns 2 (lane%4) + {0,1})
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// Swapped-operand variant (SWAP, for at most 8 query rows per segment, e.g.
+// decode with a GQA group of up to 8): the scores are computed transposed,
+// S^T = K Q^T with the 16 keys of a unit as the mma's M and the 8 rows as its
+// N, and the output as O^T = V^T P^T, P^T coming from the S^T accumulators by
+// an 8x8 register transpose (movmatrix).  That is 16 mma per unit instead of
+// 32 (the padded rows of a 16-row M are gone) and half the accumulator
+// registers.  A lane's two softmax rows are 2 (lane & 3) and 2 (lane & 3) + 1.
+//
 // FP8 variant, key order inside a 16-key unit: score column c of n-tile t
 // (the mma's n index) is key ((c >> 1) << 2) + 2t + (c & 1), so the four keys a
 // lane feeds to P.V are four consecutive keys, i.e. one 32-bit word of a
@@ -303,7 +327,7 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 // (lane & 3) * 2 + j of k-step kk reads dimension (lane & 3) * D/4 + 4 kk + j,
 // and k-index 8 + (lane & 3) * 2 + j reads that + 2, so each lane's K bytes
 // and Q values are one contiguous run of D/4 dimensions.
-template <int D, bool FP8>
+template <int D, bool FP8, bool SWAP>
 __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
     decode_kernel(const Params p) {
     using C = Cfg<D, FP8>;
@@ -440,14 +464,20 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
         // number of keys each of the lane's two rows may see
         uint32_t qa[KSTEPS][4];
         int lim0 = cs.sh.len, lim1 = cs.sh.len;
+        // this lane's two softmax rows
+        const int rA = SWAP ? (lane & 3) * 2 : qr, rB = SWAP ? rA + 1 : qr + 8;
         {
             const size_t qrow = q_row(p, cs.b);
-            const bool r0ok = qr < my_rows, r8ok = qr + 8 < my_rows;
+            // rows whose q this lane loads: qr and qr + 8 (SWAP: only qr, as a column of Q^T)
+            const bool r0ok = qr < my_rows, r8ok = !SWAP && qr + 8 < my_rows;
             const int f0 = row_sb + wrb * cs.sh.R + qr, f8 = f0 + 8;
             const int i0 = f0 / p.group, i8 = f8 / p.group;
             const int h0 = cs.g * p.group + (f0 - i0 * p.group), h8 = cs.g * p.group + (f8 - i8 * p.group);
-            if (r0ok) lim0 = qlast + i0 + 1;
-            if (r8ok) lim1 = qlast + i8 + 1;
+            {
+                const int fa = row_sb + wrb * cs.sh.R + rA, fb = row_sb + wrb * cs.sh.R + rB;
+                if (rA < my_rows) lim0 = qlast + fa / p.group + 1;
+                if (rB < my_rows) lim1 = qlast + fb / p.group + 1;
+            }
             const uint32_t* q0 = reinterpret_cast<const uint32_t*>(p.q + ((qrow + (r0ok ? i0 : 0)) * p.Hq + h0) * D);
             const uint32_t* q8 = reinterpret_cast<const uint32_t*>(p.q + ((qrow + (r8ok ? i8 : 0)) * p.Hq + h8) * D);
             if constexpr (FP8) {
@@ -463,18 +493,25 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
                     const __nv_bfloat162 e = *reinterpret_cast<__nv_bfloat162*>(&v8.x);
                     const __nv_bfloat162 f = *reinterpret_cast<__nv_bfloat162*>(&v8.y);
                     qa[kk][0] = pack_f16x2(__low2float(a), __high2float(a));
-                    qa[kk][2] = pack_f16x2(__low2float(b), __high2float(b));
-                    qa[kk][1] = pack_f16x2(__low2float(e), __high2float(e));
-                    qa[kk][3] = pack_f16x2(__low2float(f), __high2float(f));
+                    qa[kk][SWAP ? 1 : 2] = pack_f16x2(__low2float(b), __high2float(b));
+                    if constexpr (!SWAP) {
+                        qa[kk][1] = pack_f16x2(__low2float(e), __high2float(e));
+                        qa[kk][3] = pack_f16x2(__low2float(f), __high2float(f));
+                    }
                 }
             } else {
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; ++kk) {
                     const int c = (kk * 16 + qc) >> 1;
-                    qa[kk][0] = r0ok ? __ldg(q0 + c) : 0u;
-                    qa[kk][1] = r8ok ? __ldg(q8 + c) : 0u;
-                    qa[kk][2] = r0ok ? __ldg(q0 + c + 4) : 0u;
-                    qa[kk][3] = r8ok ? __ldg(q8 + c + 4) : 0u;
+                    if constexpr (SWAP) {
+                        qa[kk][0] = r0ok ? __ldg(q0 + c) : 0u;
+                        qa[kk][1] = r0ok ? __ldg(q0 + c + 4) : 0u;
+                    } else {
+                        qa[kk][0] = r0ok ? __ldg(q0 + c) : 0u;
+                        qa[kk][1] = r8ok ? __ldg(q8 + c) : 0u;
+                        qa[kk][2] = r0ok ? __ldg(q0 + c + 4) : 0u;
+                        qa[kk][3] = r8ok ? __ldg(q8 + c + 4) : 0u;
+                    }
                 }
             }
         }
@@ -493,7 +530,109 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
             const int phys = s_phys[warp][st];
             uint8_t* sk = my_stages + st * C::STAGE_BYTES;
             uint8_t* sv = sk + C::UNIT_BYTES;
-            if (phys >= 0) {
+            if (SWAP && phys >= 0) {
+                const int tok0 = ((u - cs.start) >> cs.sh.nrb_shift) * UNIT;
+                const int vis0 = lim0 - tok0, vis1 = lim1 - tok0;  // keys of this unit rows rA / rB see
+                const uint32_t kb = smem_u32(sk), vb = smem_u32(sv);
+                // S^T = K Q^T (16 keys x 8 rows), two accumulator chains (even / odd k-steps)
+                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+                // keys of this lane's accumulator rows (FP8: permuted, see above the kernel)
+                const int keyA = FP8 ? ((qr >> 1) << 2) + (qr & 1) : qr;
+                const int keyB = FP8 ? keyA + 2 : qr + 8;
+                if constexpr (FP8) {
+                    uint32_t w0[D / 16], w1[D / 16];
+#pragma unroll
+                    for (int m = 0; m < D / 64; ++m) {
+                        const int c = (lane & 3) * (D / 64) + m;
+                        const int swa = D == 128 ? (keyA & 7) : 0, swb = D == 128 ? (keyB & 7) : 0;
+                        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                     : "=r"(w0[4 * m]), "=r"(w0[4 * m + 1]), "=r"(w0[4 * m + 2]), "=r"(w0[4 * m + 3])
+                                     : "r"(kb + keyA * D + ((c ^ swa) << 4)));
+                        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                     : "=r"(w1[4 * m]), "=r"(w1[4 * m + 1]), "=r"(w1[4 * m + 2]), "=r"(w1[4 * m + 3])
+                                     : "r"(kb + keyB * D + ((c ^ swb) << 4)));
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < KSTEPS; ++kk) {
+                        const uint32_t a[4] = {e4m3x2_to_f16x2(w0[kk]), e4m3x2_to_f16x2(w1[kk]),
+                                               e4m3x2_to_f16x2(w0[kk] >> 16), e4m3x2_to_f16x2(w1[kk] >> 16)};
+                        const uint32_t (&qb)[4] = qa[kk];
+                        mma_16816_f16((kk & 1) ? sb : sa, a, qb[0], qb[1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < KSTEPS; ++kk) {
+                        const int dch = kk * 2 + v_dsel;
+                        const uint32_t addr =
+                            kb + (dch >> 3) * C::BOX_BYTES + v_key * 128 + (((dch & 7) ^ (v_key & 7)) << 4);
+                        uint32_t a[4];
+                        ldsm_x4(addr, a[0], a[1], a[2], a[3]);
+                        mma_16816((kk & 1) ? sb : sa, a, qa[kk][0], qa[kk][1]);
+                    }
+                }
+                // scale, mask: element 0 / 1 = (keyA, rows rA / rB), 2 / 3 = (keyB, rows rA / rB)
+                const float x0 = keyA < vis0 ? (sa[0] + sb[0]) * sl : -INFINITY;
+                const float x1 = keyA < vis1 ? (sa[1] + sb[1]) * sl : -INFINITY;
+                const float x2 = keyB < vis0 ? (sa[2] + sb[2]) * sl : -INFINITY;
+                const float x3 = keyB < vis1 ? (sa[3] + sb[3]) * sl : -INFINITY;
+                float rm0 = fmaxf(x0, x2), rm1 = fmaxf(x1, x3);
+#pragma unroll
+                for (int o_ = 4; o_ < 32; o_ <<= 1) {
+                    rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, o_));
+                    rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, o_));
+                }
+                const float mn0 = fmaxf(m0, rm0), mn1 = fmaxf(m1, rm1);
+                const float mr0 = mn0 == -INFINITY ? 0.f : mn0, mr1 = mn1 == -INFINITY ? 0.f : mn1;
+                const float a0 = ex2(m0 - mr0), a1 = ex2(m1 - mr1);
+                m0 = mn0;
+                m1 = mn1;
+                const float p0 = ex2(x0 - mr0), p2 = ex2(x2 - mr0), p1 = ex2(x1 - mr1), p3 = ex2(x3 - mr1);
+                l0 = l0 * a0 + (p0 + p2);
+                l1 = l1 * a1 + (p1 + p3);
+                if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+                    for (int n = 0; n < D / 16; ++n) {
+                        o[n][0] *= a0;
+                        o[n][1] *= a1;
+                        o[n][2] *= a0;
+                        o[n][3] *= a1;
+                    }
+                }
+                // P^T (keys x rows) fragments: transpose the two 8x8 blocks of P
+                const uint32_t b0 = movmatrix_trans(FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
+                const uint32_t b1 = movmatrix_trans(FP8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
+                // O^T += V^T P^T, 16 value dimensions per mma
+                if constexpr (FP8) {
+                    const int valid = min(UNIT, cs.sh.len - tok0);
+                    uint32_t keep = 0u;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+                        if ((lane & 3) * 4 + b < valid) keep |= 0xFFu << (8 * b);
+#pragma unroll
+                    for (int n = 0; n < D / 16; ++n) {
+                        uint32_t wl, wh;
+                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wl) : "r"(vb + (n * 16 + qr) * 16 + (lane & 3) * 4));
+                        asm volatile("ld.shared.u32 %0, [%1];"
+                                     : "=r"(wh)
+                                     : "r"(vb + (n * 16 + 8 + qr) * 16 + (lane & 3) * 4));
+                        wl &= keep;
+                        wh &= keep;
+                        const uint32_t a[4] = {e4m3x2_to_f16x2(wl), e4m3x2_to_f16x2(wh), e4m3x2_to_f16x2(wl >> 16),
+                                               e4m3x2_to_f16x2(wh >> 16)};
+                        mma_16816_f16(o[n], a, b0, b1);
+                    }
+                } else {
+#pragma unroll
+                    for (int n = 0; n < D / 16; ++n) {
+                        const int dch = n * 2 + k_dsel;
+                        const uint32_t addr =
+                            vb + (dch >> 3) * C::BOX_BYTES + k_key * 128 + (((dch & 7) ^ (k_key & 7)) << 4);
+                        uint32_t a[4];
+                        ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
+                        mma_16816(o[n], a, b0, b1);
+                    }
+                }
+            } else if (!SWAP && phys >= 0) {
                 const int tok0 = ((u - cs.start) >> cs.sh.nrb_shift) * UNIT;
                 const int vis0 = lim0 - tok0, vis1 = lim1 - tok0;  // keys of this unit each row sees
                 const uint32_t kb = smem_u32(sk), vb = smem_u32(sv);
@@ -640,15 +779,18 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
         }
 
         // ---- merge the states of the warps that hold the same row block (fixed order)
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-        if ((lane & 3) == 0) {
-            s_m[warp][qr] = m0;
-            s_l[warp][qr] = l0;
-            s_m[warp][qr + 8] = m1;
-            s_l[warp][qr + 8] = l1;
+        // (a row's partial sums are spread over the lanes that hold its other keys)
+#pragma unroll
+        for (int o_ = SWAP ? 4 : 1; o_ < (SWAP ? 32 : 4); o_ <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, o_);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, o_);
+        }
+        const bool row_owner = SWAP ? (lane >> 2) == 0 : (lane & 3) == 0;
+        if (row_owner) {
+            s_m[warp][rA] = m0;
+            s_l[warp][rA] = l0;
+            s_m[warp][rB] = m1;
+            s_l[warp][rB] = l1;
         }
         __syncthreads();
         const int c0 = cs.start / chunk, c1 = (cs.end - 1) / chunk;
@@ -660,22 +802,22 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
             if (wrb == r) {
                 float M0 = -INFINITY, M1 = -INFINITY;
                 for (int w = wfirst; w < W; w += nrb) {
-                    M0 = fmaxf(M0, s_m[w][qr]);
-                    M1 = fmaxf(M1, s_m[w][qr + 8]);
+                    M0 = fmaxf(M0, s_m[w][rA]);
+                    M1 = fmaxf(M1, s_m[w][rB]);
                 }
                 float L0 = 0.f, L1 = 0.f;
                 for (int w = wfirst; w < W; w += nrb) {
-                    const float mw0 = s_m[w][qr], mw1 = s_m[w][qr + 8];
-                    L0 += (mw0 == -INFINITY) ? 0.f : s_l[w][qr] * ex2(mw0 - M0);
-                    L1 += (mw1 == -INFINITY) ? 0.f : s_l[w][qr + 8] * ex2(mw1 - M1);
+                    const float mw0 = s_m[w][rA], mw1 = s_m[w][rB];
+                    L0 += (mw0 == -INFINITY) ? 0.f : s_l[w][rA] * ex2(mw0 - M0);
+                    L1 += (mw1 == -INFINITY) ? 0.f : s_l[w][rB] * ex2(mw1 - M1);
                 }
                 const float sc0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - M0);
                 const float sc1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - M1);
-                if (warp == wfirst && (lane & 3) == 0) {
-                    s_M[qr] = M0;
-                    s_L[qr] = L0;
-                    s_M[qr + 8] = M1;
-                    s_L[qr + 8] = L1;
+                if (warp == wfirst && row_owner) {
+                    s_M[rA] = M0;
+                    s_L[rA] = L0;
+                    s_M[rB] = M1;
+                    s_L[rB] = L1;
                 }
                 m0 = sc0;  // m and l are not needed any more: keep the scale factors
                 m1 = sc1;
@@ -683,7 +825,25 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
             // warps add their rescaled O into one buffer in a fixed order
 #pragma unroll 1
             for (int w = wfirst; w < W; w += nrb) {
-                if (warp == w) {
+                if (SWAP && warp == w) {
+                    // O^T fragment: (d = 16 n + qr (+8), rows rA / rB)
+#pragma unroll
+                    for (int n = 0; n < D / 16; ++n) {
+#pragma unroll
+                        for (int hi = 0; hi < 2; ++hi) {
+                            const int d = n * 16 + qr + 8 * hi;
+                            float* pA = merge_o + rA * C::MSTRIDE + d;
+                            float* pB = merge_o + rB * C::MSTRIDE + d;
+                            float vA = o[n][2 * hi] * m0, vB = o[n][2 * hi + 1] * m1;
+                            if (w > wfirst) {
+                                vA += *pA;
+                                vB += *pB;
+                            }
+                            *pA = vA;
+                            *pB = vB;
+                        }
+                    }
+                } else if (!SWAP && warp == w) {
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         const int col = n * 8 + qc;
@@ -933,12 +1093,23 @@ static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_
         kernel<<<grid, W * 32, smem, st>>>(prm);
         return PA_OK;
     };
-    if (head_dim == 128)
-        rc = fp8 ? go(decode_kernel<128, true>, Cfg<128, true>::SMEM_BYTES, 5)
-                 : go(decode_kernel<128, false>, Cfg<128, false>::SMEM_BYTES, 0);
-    else
-        rc = fp8 ? go(decode_kernel<64, true>, Cfg<64, true>::SMEM_BYTES, 6)
-                 : go(decode_kernel<64, false>, Cfg<64, false>::SMEM_BYTES, 1);
+    // at most 8 rows per segment: the swapped-operand variant (half the mma work)
+    const bool swap = group * qmax <= 8;
+    if (head_dim == 128) {
+        if (fp8)
+            rc = swap ? go(decode_kernel<128, true, true>, Cfg<128, true>::SMEM_BYTES, 7)
+                      : go(decode_kernel<128, true, false>, Cfg<128, true>::SMEM_BYTES, 5);
+        else
+            rc = swap ? go(decode_kernel<128, false, true>, Cfg<128, false>::SMEM_BYTES, 8)
+                      : go(decode_kernel<128, false, false>, Cfg<128, false>::SMEM_BYTES, 0);
+    } else {
+        if (fp8)
+            rc = swap ? go(decode_kernel<64, true, true>, Cfg<64, true>::SMEM_BYTES, 9)
+                      : go(decode_kernel<64, true, false>, Cfg<64, true>::SMEM_BYTES, 6);
+        else
+            rc = swap ? go(decode_kernel<64, false, true>, Cfg<64, false>::SMEM_BYTES, 10)
+                      : go(decode_kernel<64, false, false>, Cfg<64, false>::SMEM_BYTES, 1);
+    }
     if (rc != PA_OK) return rc;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
