@@ -191,6 +191,32 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     return r;
 }
 
+// max of three (one instruction on sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float m;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+    return m;
+}
+
+// (d0, d1) = (x0, x1) * s + (c, c), one packed FFMA (each lane rounded as fmaf)
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float x0, float x1, float s, float c) {
+    uint64_t x, sv, cv, d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(sv) : "f"(s));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(cv) : "f"(c));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(x), "l"(sv), "l"(cv));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+}
+
+// (a0, a1) += (b0, b1), one packed add
+__device__ __forceinline__ void fadd2(float& a0, float& a1, float b0, float b1) {
+    uint64_t a, b, d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(b0), "f"(b1));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(d));
+}
+
 // TMA tensor store of one 64-column x 128-row box of O (3-D map over out [rows][Hq][D]).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* smem_src, int x, int y, int z) {
     asm volatile(
@@ -616,14 +642,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         for (int c = 0; c < BN; ++c)
                             if (j * BN + c > qpos) x[c] = -INFINITY;
                     }
-                    // row max of the raw scores (softmax_scale > 0), as a tree
+                    // row max of the raw scores (softmax_scale > 0): eight chains of 3-input maxima
                     float t8[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) t8[i] = x[i];
+                    for (int i = 0; i < 8; ++i) t8[i] = fmaxf(x[i], x[8 + i]);
 #pragma unroll
-                    for (int c = 8; c < BN; ++c) t8[c & 7] = fmaxf(t8[c & 7], x[c]);
-                    const float mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
-                                           fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7]))) *
+                    for (int c = 16; c < BN; c += 16)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) t8[i] = fmax3(t8[i], x[c + i], x[c + 8 + i]);
+                    const float mx = fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]),
+                                           fmaxf(t8[6], t8[7])) *
                                      p.scale_log2;
                     if (j == 0) {
                         m_ref = mx;
@@ -647,22 +675,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         l *= alpha;
                         m_ref = m_new;
                     }
-                    // p = 2^(s * scale_log2 - m_ref): one FFMA + one MUFU each, packed to bf16 in
-                    // registers while the previous tile's P.V may still be running; sums as a tree
+                    // p = 2^(s * scale_log2 - m_ref): the arguments two at a time (packed FFMA), one
+                    // MUFU each, packed to bf16 in registers while the previous tile's P.V may still
+                    // be running; the sum in four packed accumulators
                     const float neg = -m_ref;
-                    float s8[8];
+                    float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                     uint32_t pk[BN / 2];
 #pragma unroll
                     for (int q = 0; q < BN / 8; ++q) {  // 16-byte chunk q = keys 8q .. 8q+7
-                        float part = 0.f;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const float p0 = ex2(fmaf(x[8 * q + 2 * i], p.scale_log2, neg));
-                            const float p1 = ex2(fmaf(x[8 * q + 2 * i + 1], p.scale_log2, neg));
-                            part += p0 + p1;
+                            float a0, a1;
+                            ffma2(a0, a1, x[8 * q + 2 * i], x[8 * q + 2 * i + 1], p.scale_log2, neg);
+                            const float p0 = ex2(a0), p1 = ex2(a1);
+                            fadd2(s8[2 * i], s8[2 * i + 1], p0, p1);
                             pk[4 * q + i] = pack_bf16x2(p0, p1);
                         }
-                        s8[q & 7] = q < 8 ? part : s8[q & 7] + part;
                     }
                     // the P buffer was last read by the previous tile's P.V (possibly of the
                     // previous item).  Waiting for it also keeps p_ready / pv_done within one
