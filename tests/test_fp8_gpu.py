@@ -159,3 +159,22 @@ def test_fp8_qwen7b_full_size_sampled(cuda_device):
                                                   case.seq_lens_host, np_i32(case.cu_seqlens_q), 28, 4, 16,
                                                   case.softmax_scale, seqs=seqs)
     assert_attention_close(out[seqs], ref_out[seqs], lse[seqs], ref_lse[seqs], what="fp8 qwen7b sampled")
+
+
+def test_fp8_subnormal_codes(cuda_device):
+    """Every K and V code in the e4m3 subnormal range (|code value| < 2^-6), with
+    scales large enough that they dominate the result: the exact decode of
+    subnormal codes (no flushing to zero) is visible in the output."""
+    case = workloads.make_paged_case("fp8_sub", [300, 77], [1, 1], 8, 2, 128, seed=95)
+    rng = np.random.default_rng(96)
+    P = case.num_pages
+    kc = rng.integers(1, 8, (P, 2, 16, 128), dtype=np.uint8) | (rng.integers(0, 2, (P, 2, 16, 128), dtype=np.uint8) << 7)
+    vc = rng.integers(1, 8, (P, 2, 128, 16), dtype=np.uint8) | (rng.integers(0, 2, (P, 2, 128, 16), dtype=np.uint8) << 7)
+    ks = np.array([64.0, 32.0], dtype=np.float32)  # code 1 -> 2^-9 * 64 = 0.125
+    vs = np.array([512.0, 256.0], dtype=np.float32)
+    ref_out, ref_lse = oracle.paged_attention_fp8(bits(case.q), kc, vc, ks, vs, np_i32(case.block_table),
+                                                  case.seq_lens_host, np_i32(case.cu_seqlens_q), 8, 2, 16,
+                                                  case.softmax_scale)
+    assert np.abs(ref_out).max() > 0.1  # the subnormal values carry the output
+    out, lse = _decode_fp8(case, kc, vc, ks, vs, cuda_device)
+    assert_attention_close(out, ref_out, lse, ref_lse, what="fp8 subnormal codes")
