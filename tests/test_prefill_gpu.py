@@ -160,3 +160,26 @@ def test_varlen_prefill_full_size_sampled(cuda_device):
     ref_out, ref_lse = oracle.paged_attention(**args, heads=heads)
     assert_attention_close(out[rows][:, heads], ref_out[:, heads], lse[rows][:, heads], ref_lse[:, heads],
                            what="varlen_prefill sampled")
+
+
+@pytest.mark.slow
+def test_mixed_step_full_size_sampled(cuda_device):
+    """The mixed serving step in one call (4 prefill chunks of 2048 tokens after
+    0..8192 cached tokens, 60 decodes of 1k..64k, one 131,072-token decode;
+    Hq=32, Hkv=8): the chunk with the most prior tokens, the longest decode and
+    a mid-length decode against the oracle on 3 heads."""
+    case = workloads.mixed_step(device=cuda_device)
+    out, lse = _prefill(case, cuda_device)
+    assert torch.isfinite(out.float()).all()
+    lens = case.seq_lens_host
+    chunks = [b for b in range(4)]
+    chunk = max(chunks, key=lambda b: lens[b])
+    decs = list(range(4, len(lens)))
+    longest = max(decs, key=lambda b: lens[b])
+    mid = sorted(decs, key=lambda b: lens[b])[len(decs) // 2]
+    seqs = [chunk, mid, longest]
+    args, rows = compact_for_oracle(case, seqs)
+    heads = [0, 13, 31]
+    ref_out, ref_lse = oracle.paged_attention(**args, heads=heads)
+    assert_attention_close(out[rows][:, heads], ref_out[:, heads], lse[rows][:, heads], ref_lse[:, heads],
+                           what="mixed_step sampled")
