@@ -356,27 +356,35 @@ def measure_decode(pa, case, steps, warmup, pg):
 
 def measure_decode_e2e(pa, case, steps, warmup):
     """Same step through the public API with host buffers: per step the
-    queries and the new K/V rows (and seq_lens) are copied from pinned host
-    memory, the attention output is copied back."""
+    queries, the new K/V rows and seq_lens are copied from pinned host memory
+    (packed in one buffer, one copy, as a serving loop would stage a step's
+    inputs), the attention output is copied back."""
     dev = case.q.device
     stream = torch.cuda.current_stream()
     B, Hq, D = case.q.shape
     ws = pa.Workspace(pa.decode_workspace_bytes(B, Hq, case.num_kv_heads, D), dev)
-    h_q = case.q.cpu().pin_memory()
-    h_k = case.k_new.cpu().pin_memory()
-    h_v = case.v_new.cpu().pin_memory()
-    h_len = case.seq_lens.cpu().pin_memory()
-    h_out = torch.empty_like(h_q).pin_memory()
-    d_q, d_k, d_v, d_len = torch.empty_like(case.q), torch.empty_like(case.k_new), torch.empty_like(case.v_new), \
-        torch.empty_like(case.seq_lens)
+    parts = [case.q, case.k_new, case.v_new, case.seq_lens]
+    offs, off = [], 0
+    for t in parts:  # 256-byte aligned segments of one staging buffer
+        offs.append(off)
+        off += (t.numel() * t.element_size() + 255) // 256 * 256
+    h_pack = torch.empty(off, dtype=torch.uint8).pin_memory()
+    d_pack = torch.empty(off, dtype=torch.uint8, device=dev)
+
+    def view(buf, i):
+        t = parts[i]
+        n = t.numel() * t.element_size()
+        return buf[offs[i]:offs[i] + n].view(t.dtype).view(t.shape)
+
+    for i, t in enumerate(parts):
+        view(h_pack, i).copy_(t.cpu())
+    d_q, d_k, d_v, d_len = (view(d_pack, i) for i in range(4))
+    h_out = torch.empty(case.q.shape, dtype=case.q.dtype).pin_memory()
     d_out = torch.empty_like(case.q)
     ones = torch.arange(B + 1, dtype=torch.int32, device=dev)
 
     def step():
-        d_q.copy_(h_q, non_blocking=True)
-        d_k.copy_(h_k, non_blocking=True)
-        d_v.copy_(h_v, non_blocking=True)
-        d_len.copy_(h_len, non_blocking=True)
+        d_pack.copy_(h_pack, non_blocking=True)
         pa.kv_write_paged(case.k_pool, case.v_pool, d_k, d_v, ones, d_len, case.block_table)
         pa.attn_decode_paged(d_q, case.k_pool, case.v_pool, case.block_table, d_len, case.softmax_scale,
                              max_seq_len=case.max_seq_len, out=d_out, workspace=ws)
@@ -393,9 +401,7 @@ def measure_decode_e2e(pa, case, steps, warmup):
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_len))
-    d2h = h_out.numel() * h_out.element_size()
-    return ms, h2d, d2h
+    return ms, h_pack.numel(), h_out.numel() * h_out.element_size()
 
 
 def _flush_l2(buf):
