@@ -287,8 +287,8 @@ int attn_decode_paged_fp8(void* out, float* lse, const void* q, const void* k_po
  * which every GPU that loads the library holds until the process exits.
  * Problems whose workspace (pa_decode_workspace_bytes) exceeds 8 MiB are
  * rejected with PA_ERR_SCRATCH_LIMIT before anything is enqueued; roughly,
- * (batch * num_kv_heads * ceil(group / 64) + twice the SM count) * rows must
- * stay below about 16,000 at head_dim 128 (about 32,000 at head_dim 64),
+ * (batch * num_kv_heads * ceil(group / 64) + three times the SM count) * rows
+ * must stay below about 16,000 at head_dim 128 (about 32,000 at head_dim 64),
  * where group = num_q_heads / num_kv_heads and rows = 16 for group <= 16,
  * 32 for group <= 32 and 64 above.
  *

@@ -58,20 +58,19 @@ constexpr int UNIT = 16;       // tokens per unit
 constexpr int RB = 16;         // rows per row block (mma M)
 constexpr int SBR = 64;        // rows per segment (at most W row blocks)
 constexpr int MIN_CHUNK = 16;  // minimum units per CTA
-#ifndef PA_DEC_CTAS_PER_SM
-#define PA_DEC_CTAS_PER_SM 2
-#endif
-#ifndef PA_DEC_DEPTH_BF16
-#define PA_DEC_DEPTH_BF16 3
-#endif
-#ifndef PA_DEC_DEPTH_FP8
-#define PA_DEC_DEPTH_FP8 6
-#endif
-constexpr int CTAS_PER_SM = PA_DEC_CTAS_PER_SM;  // CTAs (of 4 warps) per SM: they hide each other's latency
+// CTAs (of 4 warps) per SM: they hide each other's latency.  The swapped-operand
+// FP8 variant is bound by its own instruction latency and runs three per SM (in
+// 168 registers, with shallower staging so the shared memory fits); the others
+// run two (the bf16 decode loses more to the register cap than it gains).
+template <bool FP8, bool SWAP>
+constexpr int ctas_per_sm() { return (FP8 && SWAP) ? 3 : 2; }
+constexpr int kMaxCtasPerSM = 3;  // sizes the workspace slots for either grid
 
-template <int D, bool FP8 = false>
+// Per-warp copy pipeline depth (units in flight); the three-per-SM variant gets
+// the shallower pipeline.
+template <int D, bool FP8 = false, bool SWAP = false>
 struct Cfg {
-    static constexpr int DEPTH = FP8 ? PA_DEC_DEPTH_FP8 : ((D == 128) ? PA_DEC_DEPTH_BF16 : 2 * PA_DEC_DEPTH_BF16);
+    static constexpr int DEPTH = FP8 ? (SWAP ? 3 : 6) : (D == 128 ? 3 : 6);
     static constexpr int BOXES = D / 64;             // 128-byte-wide column blocks per row (bf16)
     static constexpr int BOX_BYTES = UNIT * 128;     // 16 rows x 128 bytes
     static constexpr int UNIT_BYTES = UNIT * D * (FP8 ? 1 : 2);  // one K or V unit
@@ -222,10 +221,10 @@ struct UnitIter {
 // Rows past the sequence end are not copied; their V rows are zeroed (their
 // slots may hold anything and 0 * NaN = NaN), their K rows are masked later.
 // Every call commits exactly one cp.async group (possibly empty).
-template <int D, bool FP8>
+template <int D, bool FP8, bool SWAP>
 __device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, uint8_t* stage, int* phys_slot,
                                            int lane, uint64_t policy) {
-    using C = Cfg<D, FP8>;
+    using C = Cfg<D, FP8, SWAP>;
     constexpr int CH = D / 8;  // 16-byte chunks per row (bf16)
     const int j = (it.u - it.seg.start) >> it.seg.sh.nrb_shift;  // key block within the sequence
     const int tok0 = j * UNIT;
@@ -328,9 +327,9 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 // and k-index 8 + (lane & 3) * 2 + j reads that + 2, so each lane's K bytes
 // and Q values are one contiguous run of D/4 dimensions.
 template <int D, bool FP8, bool SWAP>
-__global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
+__global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
     decode_kernel(const Params p) {
-    using C = Cfg<D, FP8>;
+    using C = Cfg<D, FP8, SWAP>;
     constexpr int DEPTH = C::DEPTH;
     constexpr int KSTEPS = D / 16;
     constexpr int NT = D / 8;  // n-tiles of O
@@ -431,7 +430,7 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
     // prologue: one cp.async group per stage (empty groups once the warp runs out of units)
     for (int i = 0; i < DEPTH; ++i) {
         if (!it.done) {
-            issue_unit<D, FP8>(p, it, my_stages + i * C::STAGE_BYTES, &s_phys[warp][i], lane, policy);
+            issue_unit<D, FP8, SWAP>(p, it, my_stages + i * C::STAGE_BYTES, &s_phys[warp][i], lane, policy);
             it.u += W;
             it.norm(p, warp);
         } else {
@@ -770,7 +769,7 @@ __global__ void __launch_bounds__(W * 32, CTAS_PER_SM)
             __syncwarp();  // every lane is done reading this stage
             ++consumed;
             if (!it.done) {
-                issue_unit<D, FP8>(p, it, my_stages + st * C::STAGE_BYTES, &s_phys[warp][st], lane, policy);
+                issue_unit<D, FP8, SWAP>(p, it, my_stages + st * C::STAGE_BYTES, &s_phys[warp][st], lane, policy);
                 it.u += W;
                 it.norm(p, warp);
             } else {
@@ -978,7 +977,7 @@ inline Bounds bounds(int group, int qmax) {
 inline size_t ws_bytes(int sm_count, int batch, int num_q_heads, int num_kv_heads, int head_dim, int qmax) {
     const Bounds bd = bounds(num_q_heads / num_kv_heads, qmax);
     const int segs = batch * num_kv_heads * bd.SBmax;
-    const int slots = sm_count * CTAS_PER_SM + segs;
+    const int slots = sm_count * kMaxCtasPerSM + segs;
     return ws_layout(slots, segs, bd.RS, head_dim).total;
 }
 
@@ -1038,15 +1037,16 @@ static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_
     const long long units_upper = segs * nrb_max * ((max_seq_len + UNIT - 1) / UNIT);
     // every unit index and grid * chunk must fit in int32
     if (segs * nrb_max * ((max_pages_per_seq * (long long)page_size + UNIT - 1) / UNIT) +
-            (long long)dev.sm_count * CTAS_PER_SM * MIN_CHUNK >=
+            (long long)dev.sm_count * kMaxCtasPerSM * MIN_CHUNK >=
         (1ll << 31))
         return PA_ERR_SHAPE;
-    const int gmax = dev.sm_count * CTAS_PER_SM;
+    const bool swap = group * qmax <= 8;  // at most 8 rows per segment: the swapped-operand variant
+    const int gmax = dev.sm_count * ((fp8 && swap) ? ctas_per_sm<true, true>() : ctas_per_sm<false, false>());
     long long g = (units_upper + MIN_CHUNK - 1) / MIN_CHUNK;
     if (g < 1) g = 1;
     const int grid = (int)(g < gmax ? g : gmax);
 
-    const int slots = gmax + (int)segs;
+    const int slots = dev.sm_count * kMaxCtasPerSM + (int)segs;  // as pa_decode_*_workspace_bytes
     const WsLayout wl = ws_layout(slots, (int)segs, bd.RS, head_dim);
     if (workspace == nullptr) return PA_ERR_WORKSPACE;
     if (workspace_bytes < wl.total) return PA_ERR_WORKSPACE;
@@ -1093,22 +1093,20 @@ static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_
         kernel<<<grid, W * 32, smem, st>>>(prm);
         return PA_OK;
     };
-    // at most 8 rows per segment: the swapped-operand variant (half the mma work)
-    const bool swap = group * qmax <= 8;
     if (head_dim == 128) {
         if (fp8)
-            rc = swap ? go(decode_kernel<128, true, true>, Cfg<128, true>::SMEM_BYTES, 7)
-                      : go(decode_kernel<128, true, false>, Cfg<128, true>::SMEM_BYTES, 5);
+            rc = swap ? go(decode_kernel<128, true, true>, Cfg<128, true, true>::SMEM_BYTES, 7)
+                      : go(decode_kernel<128, true, false>, Cfg<128, true, false>::SMEM_BYTES, 5);
         else
-            rc = swap ? go(decode_kernel<128, false, true>, Cfg<128, false>::SMEM_BYTES, 8)
-                      : go(decode_kernel<128, false, false>, Cfg<128, false>::SMEM_BYTES, 0);
+            rc = swap ? go(decode_kernel<128, false, true>, Cfg<128, false, true>::SMEM_BYTES, 8)
+                      : go(decode_kernel<128, false, false>, Cfg<128, false, false>::SMEM_BYTES, 0);
     } else {
         if (fp8)
-            rc = swap ? go(decode_kernel<64, true, true>, Cfg<64, true>::SMEM_BYTES, 9)
-                      : go(decode_kernel<64, true, false>, Cfg<64, true>::SMEM_BYTES, 6);
+            rc = swap ? go(decode_kernel<64, true, true>, Cfg<64, true, true>::SMEM_BYTES, 9)
+                      : go(decode_kernel<64, true, false>, Cfg<64, true, false>::SMEM_BYTES, 6);
         else
-            rc = swap ? go(decode_kernel<64, false, true>, Cfg<64, false>::SMEM_BYTES, 10)
-                      : go(decode_kernel<64, false, false>, Cfg<64, false>::SMEM_BYTES, 1);
+            rc = swap ? go(decode_kernel<64, false, true>, Cfg<64, false, true>::SMEM_BYTES, 10)
+                      : go(decode_kernel<64, false, false>, Cfg<64, false, false>::SMEM_BYTES, 1);
     }
     if (rc != PA_OK) return rc;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
