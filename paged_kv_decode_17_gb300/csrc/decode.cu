@@ -345,6 +345,9 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    // launched while the previous kernel of the stream (typically the writeback of the
+    // newest K/V rows) may still run: wait for it before reading any input
+    pdl_wait();
 
     // ---- plan: total units T, this CTA's range, and the segment holding U0
     if (warp == 0) {
@@ -1090,8 +1093,19 @@ static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto go = [&](auto kernel, int smem, int slot) {
         if (set_smem_limit_once((const void*)kernel, smem, dev.device, slot) != PA_OK) return PA_ERR_CUDA;
-        kernel<<<grid, W * 32, smem, st>>>(prm);
-        return PA_OK;
+        // programmatic dependent launch: the CTAs may start (and set up) while the previous
+        // kernel finishes; they wait for it in the kernel before touching any input
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid, 1, 1);
+        cfg.blockDim = dim3(W * 32, 1, 1);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kernel, prm) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     };
     if (head_dim == 128) {
         if (fp8)

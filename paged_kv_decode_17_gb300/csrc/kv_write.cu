@@ -1,8 +1,9 @@
 // Eager K/V writeback into pages ("Inside Ion", section "IonAttention in One
 // Paragraph": KV pages are written back eagerly as they are produced).
 //
-// One warp per new token: it finds the token's sequence by binary search
-// over cu_seqlens_new, resolves (page, slot) through the block table, and
+// One warp per new token: it finds the token's sequence by counting the
+// cu_seqlens_new entries at or below it (one coalesced load per 32 sequences),
+// resolves (page, slot) through the block table, and
 // copies the token's [Hkv][D] K and V rows with 16-byte vector loads and
 // stores.  A bit-exact copy; nothing else in the pools is written.
 //
@@ -35,28 +36,52 @@ namespace kvw {
 
 constexpr int kWarps = 8;
 
+// Sequence of new row t: the last b with cu_new[b] <= t, which is the number of
+// entries <= t minus one (cu_new is non-decreasing, so they form a prefix; the
+// last of several equal entries is the non-empty sequence holding t).  The warp
+// counts them 32 at a time with coalesced loads: one memory round trip for up to
+// 31 sequences, instead of a chain of dependent binary-search loads.
+__device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu_new, int batch, int t) {
+    const int lane = threadIdx.x & 31;
+    int cnt = 0;
+    for (int c = 0; c <= batch; c += 32) {
+        const int idx = c + lane;
+        const int v = idx <= batch ? __ldg(cu_new + idx) : 0x7fffffff;
+        cnt += __popc(__ballot_sync(0xffffffffu, v <= t));
+    }
+    return cnt - 1;
+}
+
 __global__ void __launch_bounds__(kWarps * 32) kv_write_kernel(
     __nv_bfloat16* __restrict__ k_pool, __nv_bfloat16* __restrict__ v_pool, const __nv_bfloat16* __restrict__ k_new,
     const __nv_bfloat16* __restrict__ v_new, const int32_t* __restrict__ cu_new, const int32_t* __restrict__ seq_lens,
     const int32_t* __restrict__ block_table, int num_pages, int max_pages, int batch, int total_new, int page_size,
     int num_kv_heads, int head_dim, int32_t* status) {
+    pdl_launch_dependents();  // the next kernel (e.g. the decode) may start; it waits for our writes
     const int lane = threadIdx.x & 31;
     const int vec_per_head = head_dim / 8;  // 16-byte vectors per row
     const int vec_per_tok = num_kv_heads * vec_per_head;
     const int nwarps = gridDim.x * kWarps;
     for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < total_new; t += nwarps) {
-        // sequence of token t: largest b with cu_new[b] <= t (skipping empty ones)
-        int lo = 0, hi = batch - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(cu_new + mid) <= t) lo = mid; else hi = mid - 1;
+        const uint4* ks = reinterpret_cast<const uint4*>(k_new + (size_t)t * num_kv_heads * head_dim);
+        const uint4* vs = reinterpret_cast<const uint4*>(v_new + (size_t)t * num_kv_heads * head_dim);
+        // the row's first vectors depend only on t: load them while the sequence is looked up
+        uint4 k0 = make_uint4(0, 0, 0, 0), v0 = k0, k1 = k0, v1 = k0;
+        if (lane < vec_per_tok) {
+            k0 = __ldg(ks + lane);
+            v0 = __ldg(vs + lane);
         }
-        const int b = lo;
-        const int n_b = __ldg(cu_new + b + 1) - __ldg(cu_new + b);
-        const int i = t - __ldg(cu_new + b);
+        if (lane + 32 < vec_per_tok) {
+            k1 = __ldg(ks + lane + 32);
+            v1 = __ldg(vs + lane + 32);
+        }
+        const int b = find_seq(cu_new, batch, t);
+        const int c0 = __ldg(cu_new + b);
+        const int n_b = __ldg(cu_new + b + 1) - c0;
+        const int i = t - c0;
         const int L = __ldg(seq_lens + b);
         const int pos = L - n_b + i;
-        if (n_b <= 0 || i >= n_b || pos < 0 || pos >= max_pages * page_size) {
+        if (b < 0 || b >= batch || n_b <= 0 || i >= n_b || pos < 0 || pos >= max_pages * page_size) {
             if (lane == 0) report(status, PA_ERR_BAD_LEN);
             continue;
         }
@@ -66,14 +91,12 @@ __global__ void __launch_bounds__(kWarps * 32) kv_write_kernel(
             continue;
         }
         const int slot = pos % page_size;
-        const uint4* ks = reinterpret_cast<const uint4*>(k_new + (size_t)t * num_kv_heads * head_dim);
-        const uint4* vs = reinterpret_cast<const uint4*>(v_new + (size_t)t * num_kv_heads * head_dim);
         for (int v = lane; v < vec_per_tok; v += 32) {
             const int g = v / vec_per_head;
             const int c = v - g * vec_per_head;
             const size_t dst = (((size_t)phys * num_kv_heads + g) * page_size + slot) * head_dim / 8 + c;
-            const uint4 kv = __ldg(ks + v);
-            const uint4 vv = __ldg(vs + v);
+            const uint4 kv = v == lane ? k0 : (v == lane + 32 ? k1 : __ldg(ks + v));
+            const uint4 vv = v == lane ? v0 : (v == lane + 32 ? v1 : __ldg(vs + v));
             reinterpret_cast<uint4*>(k_pool)[dst] = kv;
             reinterpret_cast<uint4*>(v_pool)[dst] = vv;
         }
@@ -168,15 +191,15 @@ __device__ __forceinline__ void rope_rows(const __nv_bfloat16* src, size_t src_s
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32) kv_write_rope_kernel(const __grid_constant__ RopeParams p) {
     constexpr int PPL = D / 64;
+    pdl_launch_dependents();  // the next kernel (e.g. the decode) may start; it waits for our writes
     const int lane = threadIdx.x & 31;
     const int nwarps = gridDim.x * kWarps;
     for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < p.total_new; t += nwarps) {
-        int lo = 0, hi = p.batch - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(p.cu_new + mid) <= t) lo = mid; else hi = mid - 1;
+        const int b = find_seq(p.cu_new, p.batch, t);
+        if (b < 0 || b >= p.batch) {
+            if (lane == 0) report(p.status, PA_ERR_BAD_LEN);
+            continue;
         }
-        const int b = lo;
         const int n_b = __ldg(p.cu_new + b + 1) - __ldg(p.cu_new + b);
         const int i = t - __ldg(p.cu_new + b);
         const int L = __ldg(p.seq_lens + b);
@@ -243,15 +266,15 @@ __global__ void __launch_bounds__(kWarps * 32) kv_write_fp8_kernel(
     const int32_t* __restrict__ cu_new, const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
     int num_pages, int max_pages, int batch, int total_new, int page_size, int num_kv_heads, int32_t* status) {
     constexpr int EPL = D / 32;  // elements per lane (2 or 4)
+    pdl_launch_dependents();  // the next kernel (e.g. the decode) may start; it waits for our writes
     const int lane = threadIdx.x & 31;
     const int nwarps = gridDim.x * kWarps;
     for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < total_new; t += nwarps) {
-        int lo = 0, hi = batch - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(cu_new + mid) <= t) lo = mid; else hi = mid - 1;
+        const int b = find_seq(cu_new, batch, t);
+        if (b < 0 || b >= batch) {
+            if (lane == 0) report(status, PA_ERR_BAD_LEN);
+            continue;
         }
-        const int b = lo;
         const int n_b = __ldg(cu_new + b + 1) - __ldg(cu_new + b);
         const int i = t - __ldg(cu_new + b);
         const int pos = __ldg(seq_lens + b) - n_b + i;

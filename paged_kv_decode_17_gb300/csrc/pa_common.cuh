@@ -73,6 +73,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 
 // Order this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA) accesses to the same memory.
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream still runs;
+// pdl_wait() blocks until that kernel has finished and its writes are visible
+// (it returns at once when there is no such dependency).  A kernel calls
+// pdl_launch_dependents() to let the next one start early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
