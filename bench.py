@@ -312,7 +312,10 @@ def _events(stream, n):
 
 
 def measure_decode(pa, case, steps, warmup, pg):
-    """Decode step = writeback of the newest K/V row + split-K decode."""
+    """Decode step = writeback of the newest K/V row + split-K decode (decode
+    and merge kernels).  The K timed steps run back to back (each launch a
+    programmatic dependent of the one before); a second pass with events
+    between the calls splits the time into writeback and decode."""
     dev = case.q.device
     stream = torch.cuda.current_stream()
     B, Hq, D = case.q.shape
@@ -330,28 +333,30 @@ def measure_decode(pa, case, steps, warmup, pg):
     torch.cuda.synchronize()
     barrier(pg)
     torch.cuda.synchronize()
-    ev = _events(stream, 4 * steps)
     sampler = ClockSampler()
     with sampler:
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         for i in range(steps):
-            ev[4 * i].record(stream)
-            pa.kv_write_paged(case.k_pool, case.v_pool, case.k_new, case.v_new, ones, case.seq_lens,
-                              case.block_table)
-            ev[4 * i + 1].record(stream)
-            pa.attn_decode_paged(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
-                                 case.softmax_scale, max_seq_len=case.max_seq_len, out=out, workspace=ws)
-            ev[4 * i + 2].record(stream)
+            step()
         t_end.record(stream)
         torch.cuda.synchronize()
     barrier(pg)
     torch.cuda.synchronize()
     total_ms = t_start.elapsed_time(t_end)
-    dec_ms = [ev[4 * i + 1].elapsed_time(ev[4 * i + 2]) for i in range(steps)]
-    kvw_ms = [ev[4 * i].elapsed_time(ev[4 * i + 1]) for i in range(steps)]
-    return total_ms, dec_ms, kvw_ms, sampler.summary(), 2 * steps
+    ev = _events(stream, 3 * steps)
+    for i in range(steps):
+        ev[3 * i].record(stream)
+        pa.kv_write_paged(case.k_pool, case.v_pool, case.k_new, case.v_new, ones, case.seq_lens, case.block_table)
+        ev[3 * i + 1].record(stream)
+        pa.attn_decode_paged(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
+                             case.softmax_scale, max_seq_len=case.max_seq_len, out=out, workspace=ws)
+        ev[3 * i + 2].record(stream)
+    torch.cuda.synchronize()
+    dec_ms = [ev[3 * i + 1].elapsed_time(ev[3 * i + 2]) for i in range(steps)]
+    kvw_ms = [ev[3 * i].elapsed_time(ev[3 * i + 1]) for i in range(steps)]
+    return total_ms, dec_ms, kvw_ms, sampler.summary(), 3 * steps
 
 
 def measure_decode_e2e(pa, case, steps, warmup):
@@ -460,7 +465,7 @@ def measure_prefill(pa, steps, warmup, peaks):
            "kv_write": {"ms": w, "bytes": wbytes, "gbs": wbytes / (w * 1e-3) / 1e9,
                         "frac_hbm": wbytes / (w * 1e-3) / 1e9 / peaks["hbm_gbs"]},
            "l2": "flushed (256 MiB write) between iterations", "steps": steps,
-           "launches_per_step": 4}  # writeback, split-K decode (no entry to serve here), plan, prefill
+           "launches_per_step": 5}  # writeback, split-K decode + merge (no entry to serve here), plan, prefill
     del case, flush
     torch.cuda.empty_cache()
     return res
@@ -603,7 +608,7 @@ def measure_mixed(pa, steps, warmup, peaks):
            "step_ms": t, "decode_kv_bytes": dbytes, "prefill_flops": flops,
            "t_roofline_ms": 1e3 * max(t_bytes, t_flops), "t_serial_roofline_ms": 1e3 * (t_bytes + t_flops),
            "frac_of_roofline": max(t_bytes, t_flops) / (t * 1e-3),
-           "tokens_per_s": case.total_q / (t * 1e-3), "launches_per_step": 3, "steps": steps,
+           "tokens_per_s": case.total_q / (t * 1e-3), "launches_per_step": 4, "steps": steps,
            "l2": "inputs larger than L2 (about 9 GB of KV)"}
     del case
     torch.cuda.empty_cache()
@@ -712,7 +717,7 @@ def main(argv=None):
                    "l2": "inputs larger than L2: 512 MiB of KV read per step vs 129 MB L2, no flush"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "kernel": "attn_decode_paged (decode_kernel<128>)",
+                     "kernel": "attn_decode_paged (decode_kernel<128> + merge_kernel<128>)",
                      "algorithmic_bytes_per_launch": kv_bytes, "launch_ms": dec_avg,
                      "peak_source": peaks["source"]},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -728,7 +733,7 @@ def main(argv=None):
         line["multiquery"] = measure_multiquery(pa, psteps, 3, peaks)
         line["rope_writeback"] = measure_rope_writeback(pa, psteps, 3, peaks)
         line["fp8_decode"] = measure_fp8_decode(pa, psteps, 3, peaks)
-        line["gpu_launches"] += world * psteps * (4 + 3 + 1 + 1 + 1)
+        line["gpu_launches"] += world * psteps * (5 + 4 + 2 + 1 + 2)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_subprocess()
     if rank == 0:

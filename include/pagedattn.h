@@ -97,16 +97,11 @@ const char* pa_status_string(int status);
 
 /*
  * Workspace bytes attn_decode_paged needs for these sizes on the current
- * device.  The workspace holds the split partials (normalised partial
- * outputs and their log-sum-exps) and one arrival counter per
- * (sequence, KV head, segment of query rows) at its start.  The caller must
- * ZERO it once after allocating it; every successful call leaves the
- * counters zero again.  A workspace may serve calls of different sizes: the
- * library remembers, per workspace address, the size of the last call's
- * counter region and clears the counters (one small asynchronous memset on
- * `stream`) when it changes.  If a call reports a device error, zero it
- * again before reuse.  Two calls that may run concurrently need separate
- * workspaces.
+ * device.  The workspace holds each sequence's first work unit (batch + 1
+ * int32) and the split partials (normalised partial outputs and their
+ * log-sum-exps).  A call writes every part before reading it, so the
+ * workspace needs no initialisation and may serve calls of any size that
+ * fits.  Two calls that may run concurrently need separate workspaces.
  */
 size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim);
 
@@ -128,8 +123,8 @@ int attn_decode_paged(void* out, float* lse, const void* q, const void* k_pool, 
 
 /*
  * Workspace bytes attn_decode_multiquery_paged needs when no entry has more
- * than max_q_len (1..8) query rows; same zeroing rules as the decode
- * workspace.  Returns 0 for unsupported sizes.
+ * than max_q_len (1..8) query rows; like the decode workspace it needs no
+ * initialisation.  Returns 0 for unsupported sizes.
  */
 size_t pa_decode_multiquery_workspace_bytes(int batch, int max_q_len, int num_q_heads, int num_kv_heads,
                                             int head_dim);
@@ -163,7 +158,7 @@ int attn_decode_multiquery_paged(void* out, float* lse, const void* q, const voi
                                  size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
- * Workspace bytes attn_prefill_varlen_causal needs (same zeroing rules as
+ * Workspace bytes attn_prefill_varlen_causal needs (no initialisation, as
  * the decode workspace; it also holds the split partials of the entries
  * with at most 8 query rows, which the call serves on the split-K decode
  * path).
@@ -295,9 +290,8 @@ int attn_decode_paged_fp8(void* out, float* lse, const void* q, const void* k_po
  * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  Every call clears the arrival counters in the
- * array (an asynchronous memset on `stream`) before it launches.  All calls
- * on a device share the one array and it keeps the last call's contents:
+ * before any stream capture.  All calls on a device share the one array and
+ * it keeps the last call's contents:
  * calls whose execution may overlap on the GPU (different streams, or
  * concurrent graph branches) race on it and give wrong results.
  */

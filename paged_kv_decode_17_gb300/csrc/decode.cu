@@ -37,10 +37,14 @@
 //   registers.
 // * At the end of the CTA's part of a segment the states of the warps that
 //   hold the same row block are merged in shared memory in a fixed order.  A
-//   segment covered by one CTA is normalised and stored directly; otherwise
-//   the partial (o_c, lse_c) goes to the workspace and the last CTA to arrive
-//   (atomic ticket, no waiting) merges all partials of that segment in a
-//   fixed order, so results are bit-identical run to run.
+//   segment covered by one chunk is normalised and stored directly; otherwise
+//   the partial (o_c, lse_c) goes to the workspace slot of its chunk, and a
+//   second, small kernel (launched as a programmatic dependent of the first)
+//   merges each split segment's partials in chunk order, one thread per
+//   (row, 4 dimensions), so results are bit-identical run to run.  (Merging
+//   in the decode kernel, by the last CTA to finish a segment, held that CTA
+//   up for several L2 round trips at the very end of its range: the CTAs that
+//   merged set the length of the whole launch.)
 #include "pa_common.cuh"
 #include "pa_host.h"
 
@@ -92,7 +96,8 @@ struct Params {
     const int32_t* block_table;
     const int32_t* seq_lens;
     const int32_t* cu_q;  // null: one query row per sequence (row b); else rows cu_q[b] .. cu_q[b+1]
-    int32_t* counters;
+    int32_t* seg_base;  // [batch + 1]: first unit of each sequence, then the total (written by CTA 0)
+    int G;              // CTAs of the decode grid
     float* ws_lse;  // [slots][RS], log2 domain
     float* ws_o;    // [slots][RS][D], normalised
     int32_t* status;
@@ -201,6 +206,8 @@ struct UnitIter {
     Seg seg;
     int pe, u, U1;
     bool done;
+    int pc_base;  // page cache: unit whose page lane 0 holds (-1: empty)
+    int pc_phys;  // this lane's entry: the page of unit pc_base + lane * W (-1 past the piece)
     __device__ __forceinline__ void norm(const Params& p, int w) {
         while (!done && u >= pe) {
             if (pe >= U1) {
@@ -210,9 +217,30 @@ struct UnitIter {
             seg_next(seg, p);
             pe = min(U1, seg.end);
             u = seg.start + w;
+            pc_base = -1;
         }
     }
 };
+
+// Physical page of unit it.u.  The warp keeps the pages of its next 32 units,
+// one per lane, and reloads all 32 at once (one block_table load per lane, in
+// parallel) when it runs past them or enters a new segment, so issuing a unit
+// does not wait for a block_table round trip.
+__device__ __forceinline__ int unit_page(const Params& p, UnitIter& it, int lane) {
+    int k = (it.u - it.pc_base) / W;
+    if (it.pc_base < 0 || k >= 32) {
+        it.pc_base = it.u;
+        const int ul = it.u + lane * W;
+        int v = -1;
+        if (ul < it.pe) {
+            const int j = (ul - it.seg.start) >> it.seg.sh.nrb_shift;  // key block
+            v = __ldg(p.block_table + (size_t)it.seg.b * p.max_pages + ((j * UNIT) >> p.ps_shift));
+        }
+        it.pc_phys = v;
+        k = 0;
+    }
+    return __shfl_sync(0xffffffffu, it.pc_phys, k);
+}
 
 // Stage one unit (16 keys of K and of V) with 16-byte cp.async copies, written
 // in the 128-byte-swizzled layout the ldmatrix reads expect: 16-byte chunk c of
@@ -222,15 +250,14 @@ struct UnitIter {
 // slots may hold anything and 0 * NaN = NaN), their K rows are masked later.
 // Every call commits exactly one cp.async group (possibly empty).
 template <int D, bool FP8, bool SWAP>
-__device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, uint8_t* stage, int* phys_slot,
-                                           int lane, uint64_t policy) {
+__device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, int phys, uint8_t* stage,
+                                           int* phys_slot, int lane, uint64_t policy) {
     using C = Cfg<D, FP8, SWAP>;
     constexpr int CH = D / 8;  // 16-byte chunks per row (bf16)
     const int j = (it.u - it.seg.start) >> it.seg.sh.nrb_shift;  // key block within the sequence
     const int tok0 = j * UNIT;
     const int page = tok0 >> p.ps_shift;
     const int sub = (tok0 - (page << p.ps_shift)) / UNIT;
-    const int phys = __ldg(p.block_table + (size_t)it.seg.b * p.max_pages + page);
     if (phys < 0 || phys >= p.num_pages) {
         if (lane == 0) {
             report(p.status, PA_ERR_BAD_PAGE);
@@ -326,6 +353,18 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 // (lane & 3) * 2 + j of k-step kk reads dimension (lane & 3) * D/4 + 4 kk + j,
 // and k-index 8 + (lane & 3) * 2 + j reads that + 2, so each lane's K bytes
 // and Q values are one contiguous run of D/4 dimensions.
+// How the units [0, T) of a launch are cut into chunks, one per CTA of a grid
+// of G; the decode and the merge kernel derive it from the same T and G.
+// Chunk c owns workspace slots c + (segment index).  (Cutting the last part
+// into small chunks that idle CTAs take from a counter was measured: the
+// CTAs' finishing spread is about 10 %, and the extra partials cost the merge
+// more than the balance gained.)
+struct Split {
+    int T, S;
+    __device__ __forceinline__ Split(int T_, int G) : T(T_), S(max(MIN_CHUNK, (T_ + G - 1) / G)) {}
+    __device__ __forceinline__ int chunk_of(int u) const { return u / S; }
+};
+
 template <int D, bool FP8, bool SWAP>
 __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
     decode_kernel(const Params p) {
@@ -341,15 +380,15 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
     __shared__ int s_phys[W][DEPTH];
     __shared__ float s_m[W][RB], s_l[W][RB], s_M[RB], s_L[RB];
     __shared__ int s_plan[8];
-    __shared__ int s_last;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     // launched while the previous kernel of the stream (typically the writeback of the
     // newest K/V rows) may still run: wait for it before reading any input
     pdl_wait();
+    pdl_launch_dependents();  // the merge kernel may be scheduled (it waits for this grid)
 
-    // ---- plan: total units T, this CTA's range, and the segment holding U0
+    // ---- plan: total units T (and the defined result of empty sequences)
     if (warp == 0) {
         int T = 0;
         for (int b0 = 0; b0 < p.batch; b0 += 32) {
@@ -370,44 +409,57 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
                         }
                 }
             }
-            T += warp_sum_int(n);
-        }
-        int chunk = (T + gridDim.x - 1) / gridDim.x;
-        chunk = max(chunk, MIN_CHUNK);
-        const int U0 = blockIdx.x * chunk;  // grid * chunk < 2^31 is checked on the host
-        const int U1 = min(T, U0 + chunk);
-        int sb = -1, sP = 0;
-        if (U0 < U1) {
-            int P = 0;
-            for (int b0 = 0; b0 < p.batch && sb < 0; b0 += 32) {
-                const int b = b0 + lane;
-                const int n = (b < p.batch) ? seq_units(p, seq_shape(p, b)) : 0;
-                const int incl = warp_incl_scan(n);
-                const int tot = __shfl_sync(0xffffffffu, incl, 31);
-                if (U0 < P + tot) {
-                    const unsigned hit = __ballot_sync(0xffffffffu, P + incl > U0);
-                    const int l = __ffs(hit) - 1;
-                    sb = b0 + l;
-                    sP = P + __shfl_sync(0xffffffffu, incl - n, l);
-                }
-                P += tot;
-            }
+            const int incl = warp_incl_scan(n);
+            if (blockIdx.x == 0 && b < p.batch) p.seg_base[b] = T + incl - n;
+            T += __shfl_sync(0xffffffffu, incl, 31);
         }
         if (lane == 0) {
             s_plan[0] = T;
-            s_plan[1] = chunk;
-            s_plan[2] = U0;
-            s_plan[3] = U1;
+            if (blockIdx.x == 0) p.seg_base[p.batch] = T;
+        }
+    }
+    __syncthreads();
+    // ---- split: CTA c owns the equal range [c S, (c + 1) S) of the units
+    const Split sp(s_plan[0], gridDim.x);
+    const int U0 = blockIdx.x * sp.S;  // grid * chunk < 2^31 is checked on the host
+    const int U1 = min(sp.T, U0 + sp.S);
+    if (U0 >= U1) return;
+
+    const uint64_t policy = policy_evict_first();
+    uint8_t* my_stages = stages + warp * DEPTH * C::STAGE_BYTES;
+
+    // per-lane ldmatrix geometry (see the fragment layouts of mma.m16n8k16)
+    const int mi = lane >> 3, ri = lane & 7;
+    const int k_key = ((mi >> 1) << 3) + ri;  // K: matrices (keys 0-7|8-15) x (d lo|hi)
+    const int k_dsel = mi & 1;
+    const int v_key = ((mi & 1) << 3) + ri;   // V (trans): matrices (keys lo|hi) x (d lo|hi)
+    const int v_dsel = mi >> 1;
+    const int qr = lane >> 2;       // row group of this lane in mma fragments
+    const int qc = (lane & 3) * 2;  // column pair of this lane
+
+    const int cidx = blockIdx.x;  // this range's chunk
+    // segment holding U0
+    if (warp == 0) {
+        int sb = -1, sP = 0, P = 0;
+        for (int b0 = 0; b0 < p.batch && sb < 0; b0 += 32) {
+            const int b = b0 + lane;
+            const int n = (b < p.batch) ? seq_units(p, seq_shape(p, b)) : 0;
+            const int incl = warp_incl_scan(n);
+            const int tot = __shfl_sync(0xffffffffu, incl, 31);
+            if (U0 < P + tot) {
+                const unsigned hit = __ballot_sync(0xffffffffu, P + incl > U0);
+                const int l = __ffs(hit) - 1;
+                sb = b0 + l;
+                sP = P + __shfl_sync(0xffffffffu, incl - n, l);
+            }
+            P += tot;
+        }
+        if (lane == 0) {
             s_plan[4] = sb;
             s_plan[5] = sP;
         }
     }
     __syncthreads();
-    const int chunk = s_plan[1];
-    const int U0 = s_plan[2], U1 = s_plan[3];
-    if (U0 >= U1) return;
-
-    // segment holding U0
     Seg seg0;
     {
         seg_set_seq(seg0, p, s_plan[4]);
@@ -418,37 +470,28 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
         seg0.end = seg0.start + seg0.n;
     }
 
-    const uint64_t policy = policy_evict_first();
-    uint8_t* my_stages = stages + warp * DEPTH * C::STAGE_BYTES;
-
-    // ---- prologue: fill this warp's pipeline
+    // ---- prologue: fill this warp's pipeline, one cp.async group per stage (empty
+    // groups once the warp runs out of units)
     UnitIter it;
     it.seg = seg0;
     it.U1 = U1;
     it.pe = min(U1, seg0.end);
     it.u = U0 + warp;
     it.done = false;
+    it.pc_base = -1;
+    it.pc_phys = -1;
     it.norm(p, warp);
     uint32_t consumed = 0;
-    // prologue: one cp.async group per stage (empty groups once the warp runs out of units)
     for (int i = 0; i < DEPTH; ++i) {
         if (!it.done) {
-            issue_unit<D, FP8, SWAP>(p, it, my_stages + i * C::STAGE_BYTES, &s_phys[warp][i], lane, policy);
+            const int phys = unit_page(p, it, lane);
+            issue_unit<D, FP8, SWAP>(p, it, phys, my_stages + i * C::STAGE_BYTES, &s_phys[warp][i], lane, policy);
             it.u += W;
             it.norm(p, warp);
         } else {
             cp_async_commit();
         }
     }
-
-    // per-lane ldmatrix geometry (see the fragment layouts of mma.m16n8k16)
-    const int mi = lane >> 3, ri = lane & 7;
-    const int k_key = ((mi >> 1) << 3) + ri;  // K: matrices (keys 0-7|8-15) x (d lo|hi)
-    const int k_dsel = mi & 1;
-    const int v_key = ((mi & 1) << 3) + ri;   // V (trans): matrices (keys lo|hi) x (d lo|hi)
-    const int v_dsel = mi >> 1;
-    const int qr = lane >> 2;       // row group of this lane in mma fragments
-    const int qc = (lane & 3) * 2;  // column pair of this lane
 
     Seg cs = seg0;
     int pa_ = U0;
@@ -772,7 +815,9 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
             __syncwarp();  // every lane is done reading this stage
             ++consumed;
             if (!it.done) {
-                issue_unit<D, FP8, SWAP>(p, it, my_stages + st * C::STAGE_BYTES, &s_phys[warp][st], lane, policy);
+                const int phys_next = unit_page(p, it, lane);
+                issue_unit<D, FP8, SWAP>(p, it, phys_next, my_stages + st * C::STAGE_BYTES, &s_phys[warp][st], lane,
+                                         policy);
                 it.u += W;
                 it.norm(p, warp);
             } else {
@@ -795,7 +840,7 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
             s_l[warp][rB] = l1;
         }
         __syncthreads();
-        const int c0 = cs.start / chunk, c1 = (cs.end - 1) / chunk;
+        const int c0 = sp.chunk_of(cs.start), c1 = sp.chunk_of(cs.end - 1);
         const int sid = (cs.b * p.Hkv + cs.g) * p.SBmax + cs.sb;
         const bool single = (c0 == c1);
         const size_t orow = q_row(p, cs.b);
@@ -883,61 +928,13 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
                     *reinterpret_cast<uint2*>(p.out + orr * D + d4 * 4) = ob;
                     if (p.lse != nullptr && d4 == 0) p.lse[orr] = L > 0.f ? (s_M[rr] + lg2(L)) * kLn2 : -INFINITY;
                 } else {
-                    const size_t srow = ((size_t)blockIdx.x + sid) * p.RS + r * RB + rr;
+                    const size_t srow = ((size_t)cidx + sid) * p.RS + r * RB + rr;
                     *reinterpret_cast<float4*>(p.ws_o + srow * D + d4 * 4) =
                         make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
                     if (d4 == 0) p.ws_lse[srow] = L > 0.f ? s_M[rr] + lg2(L) : -INFINITY;
                 }
             }
             __syncthreads();  // the merge buffer and s_M / s_L are reused by the next row block
-        }
-        if (!single) {
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) {
-                const int prev = atomicAdd(p.counters + sid, 1);
-                s_last = (prev == c1 - c0);
-            }
-            __syncthreads();
-            if (s_last) {
-                // last CTA of this segment: merge all partials in slot order
-                __threadfence();
-                for (int idx = tid; idx < nrb * RB * (D / 4); idx += W * 32) {
-                    const int rw = idx / (D / 4);
-                    const int d4 = idx - rw * (D / 4);
-                    const int r = rw / RB, rr = rw - r * RB;
-                    if (rr >= min(cs.sh.R, rows_sb - r * cs.sh.R)) continue;
-                    float M = -INFINITY;
-                    for (int c = c0; c <= c1; ++c)
-                        M = fmaxf(M, __ldcg(p.ws_lse + ((size_t)c + sid) * p.RS + rw));
-                    float L = 0.f;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (M != -INFINITY) {
-                        for (int c = c0; c <= c1; ++c) {
-                            const size_t srow = ((size_t)c + sid) * p.RS + rw;
-                            const float lc = __ldcg(p.ws_lse + srow);
-                            if (lc == -INFINITY) continue;
-                            const float wgt = ex2(lc - M);
-                            const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws_o + srow * D) + d4);
-                            L += wgt;
-                            acc.x += wgt * v.x;
-                            acc.y += wgt * v.y;
-                            acc.z += wgt * v.z;
-                            acc.w += wgt * v.w;
-                        }
-                    }
-                    const float inv = L > 0.f ? 1.f / L : 0.f;
-                    const int f = row_sb + r * cs.sh.R + rr;
-                    const int i = f / p.group;
-                    const size_t orr = (orow + i) * p.Hq + cs.g * p.group + (f - i * p.group);
-                    uint2 ob;
-                    ob.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-                    ob.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-                    *reinterpret_cast<uint2*>(p.out + orr * D + d4 * 4) = ob;
-                    if (p.lse != nullptr && d4 == 0) p.lse[orr] = L > 0.f ? (M + lg2(L)) * kLn2 : -INFINITY;
-                }
-                if (tid == 0) p.counters[sid] = 0;  // leave the workspace ready for the next call
-            }
         }
         __syncthreads();  // merge buffers are reused by the next piece
         if (pe >= U1) break;
@@ -948,15 +945,75 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
     cp_async_wait_group<0>();  // never exit with a copy still landing in shared memory
 }
 
-// Workspace layout: [counters: segs int32][ws_lse: slots x RS f32][ws_o: slots x RS x D f32]
+// Merge of the split segments (the reduction step of Flash-Decoding):
+//     lse = log sum_c exp(lse_c),   o = sum_c exp(lse_c - lse) o_c
+// over the chunks c0 .. c1 of a segment, in chunk order.  Block (segment,
+// row block), one thread per (row, 4 dimensions); each thread loads its
+// row's partials eight chunks at a time and merges them with a running max.  Launched right after the decode
+// kernel as its programmatic dependent, it waits for that grid to finish.
+template <int D>
+__global__ void __launch_bounds__(RB * D / 4) merge_kernel(const Params p) {
+    pdl_wait();
+    const int sid = blockIdx.x;
+    const int per_b = p.Hkv * p.SBmax;
+    const int b = sid / per_b;
+    const int g = (sid - b * per_b) / p.SBmax;
+    const int sb = sid - b * per_b - g * p.SBmax;
+    Seg s;
+    seg_set_seq(s, p, b);
+    if (s.n == 0 || sb >= s.sh.SB) return;
+    const int r = blockIdx.y;
+    if (r >= (1 << s.sh.nrb_shift)) return;
+    const int rr = threadIdx.x / (D / 4), d4 = threadIdx.x - rr * (D / 4);
+    const int row_sb = sb * s.sh.RSB;
+    const int rows_sb = min(s.sh.RSB, s.sh.qlen * p.group - row_sb);
+    if (rr >= min(s.sh.R, rows_sb - r * s.sh.R)) return;
+    const int start = p.seg_base[b] + (g * s.sh.SB + sb) * s.n;
+    const Split sp(p.seg_base[p.batch], p.G);
+    const int c0 = sp.chunk_of(start), c1 = sp.chunk_of(start + s.n - 1);
+    if (c0 == c1) return;  // one chunk held the whole segment and stored its rows
+    const int rw = r * RB + rr;
+    // one pass with a running max (rescaling when it grows), so that each partial's
+    // lse and O loads are issued together
+    float M = -INFINITY, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int c = c0; c <= c1; ++c) {
+        const size_t srow = ((size_t)c + sid) * p.RS + rw;
+        const float lc = __ldcg(p.ws_lse + srow);
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws_o + srow * D) + d4);
+        const float mn = fmaxf(M, lc);
+        const float sc = M == -INFINITY ? 0.f : ex2(M - mn);  // the state is all zero while M = -inf
+        // a partial with no visible key has lse = -inf and O = 0
+        const float wgt = lc == -INFINITY ? 0.f : ex2(lc - mn);
+        L = L * sc + wgt;
+        acc.x = acc.x * sc + wgt * v.x;
+        acc.y = acc.y * sc + wgt * v.y;
+        acc.z = acc.z * sc + wgt * v.z;
+        acc.w = acc.w * sc + wgt * v.w;
+        M = mn;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int f = row_sb + r * s.sh.R + rr;
+    const int i = f / p.group;
+    const size_t orr = (q_row(p, b) + i) * p.Hq + g * p.group + (f - i * p.group);
+    uint2 ob;
+    ob.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    ob.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(p.out + orr * D + d4 * 4) = ob;
+    if (p.lse != nullptr && d4 == 0) p.lse[orr] = L > 0.f ? (M + lg2(L)) * kLn2 : -INFINITY;
+}
+
+// Workspace layout: [seg_base: batch + 1 int32][ws_lse: slots x RS f32][ws_o: slots x RS x D f32].
+// Every part is written before it is read in a call: the workspace needs no initialisation.
 struct WsLayout {
-    size_t counters, lse, o, total;
+    size_t hdr, lse, o, total;
 };
 
-inline WsLayout ws_layout(int slots, int segs, int RS, int D) {
+inline WsLayout ws_layout(int slots, int batch, int RS, int D) {
     WsLayout w;
-    w.counters = 0;
-    w.lse = align_up((size_t)segs * 4, 256);
+    w.hdr = 0;
+    w.lse = align_up((size_t)(batch + 1) * 4, 256);
     w.o = w.lse + align_up((size_t)slots * RS * 4, 256);
     w.total = w.o + (size_t)slots * RS * D * 4;
     return w;
@@ -977,11 +1034,13 @@ inline Bounds bounds(int group, int qmax) {
     return bd;
 }
 
+// Workspace slots: one per chunk (at most the largest grid), offset by the segment index.
+inline int ws_slots(int sm_count, int segs) { return sm_count * kMaxCtasPerSM + segs; }
+
 inline size_t ws_bytes(int sm_count, int batch, int num_q_heads, int num_kv_heads, int head_dim, int qmax) {
     const Bounds bd = bounds(num_q_heads / num_kv_heads, qmax);
     const int segs = batch * num_kv_heads * bd.SBmax;
-    const int slots = sm_count * kMaxCtasPerSM + segs;
-    return ws_layout(slots, segs, bd.RS, head_dim).total;
+    return ws_layout(ws_slots(sm_count, segs), batch, bd.RS, head_dim).total;
 }
 
 }  // namespace dec
@@ -1049,16 +1108,10 @@ static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_
     if (g < 1) g = 1;
     const int grid = (int)(g < gmax ? g : gmax);
 
-    const int slots = dev.sm_count * kMaxCtasPerSM + (int)segs;  // as pa_decode_*_workspace_bytes
-    const WsLayout wl = ws_layout(slots, (int)segs, bd.RS, head_dim);
+    const WsLayout wl = ws_layout(ws_slots(dev.sm_count, (int)segs), batch, bd.RS, head_dim);  // as *_workspace_bytes
     if (workspace == nullptr) return PA_ERR_WORKSPACE;
     if (workspace_bytes < wl.total) return PA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_WORKSPACE;
-    // the counter region [0, wl.lse) is what must be zero; partials start right after it, so two calls
-    // with the same region size never write each other's counters
-    rc = prepare_counters(workspace, wl.lse, (uint64_t)wl.lse, stream);
-    if (rc != PA_OK) return rc;
-
     dec::Params prm;
     prm.out = static_cast<__nv_bfloat16*>(out);
     prm.lse = lse;
@@ -1076,7 +1129,8 @@ static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_
     prm.SBmax = bd.SBmax;
     prm.RS = bd.RS;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    prm.counters = reinterpret_cast<int32_t*>(ws + wl.counters);
+    prm.seg_base = reinterpret_cast<int32_t*>(ws + wl.hdr);
+    prm.G = grid;
     prm.ws_lse = reinterpret_cast<float*>(ws + wl.lse);
     prm.ws_o = reinterpret_cast<float*>(ws + wl.o);
     prm.status = status;
@@ -1123,6 +1177,22 @@ static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_
                       : go(decode_kernel<64, false, false>, Cfg<64, false, false>::SMEM_BYTES, 1);
     }
     if (rc != PA_OK) return rc;
+    // the merge of split segments, a programmatic dependent of the decode grid
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)segs, (unsigned)nrb_max, 1);
+        cfg.blockDim = dim3(RB * head_dim / 4, 1, 1);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = head_dim == 128 ? cudaLaunchKernelEx(&cfg, merge_kernel<128>, prm)
+                                              : cudaLaunchKernelEx(&cfg, merge_kernel<64>, prm);
+        if (e != cudaSuccess) return PA_ERR_CUDA;
+    }
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -1184,9 +1254,9 @@ extern "C" int attn_decode_multiquery_paged(void* out, float* lse, const void* q
 // Some callers cannot call cudaMalloc: code running inside an allocator or
 // memory-pool callback, a plugin loaded into a host framework that owns all
 // device memory, or a latency-critical path that must not enter the driver's
-// allocator.  For them this file keeps the split-K scratch (arrival counters
-// and partial outputs) in a fixed device array, so the only buffers they
-// pass are inputs and outputs.
+// allocator.  For them this file keeps the split-K scratch (the partial
+// outputs) in a fixed device array, so the only buffers they pass are
+// inputs and outputs.
 // ---------------------------------------------------------------------------
 namespace pa {
 namespace dec {
@@ -1236,12 +1306,6 @@ extern "C" int attn_decode_paged_noalloc(void* out, float* lse, const void* q, c
     void* scratch = nullptr;
     rc = dec::static_scratch_ptr(dev.device, &scratch);
     if (rc != PA_OK) return rc;
-    // The arrival counters must start at zero; an earlier call that stopped
-    // on a device error may have left them dirty, so clear them every call.
-    const int segs = batch * num_kv_heads * dec::bounds(num_q_heads / num_kv_heads, 1).SBmax;
-    const size_t counter_bytes = align_up((size_t)segs * 4, 256);
-    if (cudaMemsetAsync(scratch, 0, counter_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return PA_ERR_CUDA;
     return attn_decode_paged(out, lse, q, k_pool, v_pool, num_pages, block_table, max_pages_per_seq, seq_lens, batch,
                              max_seq_len, page_size, num_q_heads, num_kv_heads, head_dim, softmax_scale, scratch,
                              dec::kStaticScratchBytes, status, stream);

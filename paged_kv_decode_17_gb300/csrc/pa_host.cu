@@ -5,7 +5,6 @@
 
 #include <atomic>
 #include <mutex>
-#include <unordered_map>
 
 #include "pa_host.h"
 
@@ -99,28 +98,6 @@ int set_smem_limit_once(const void* kernel, int bytes, int device, int slot) {
         return PA_ERR_CUDA;
     g_smem_set[device][slot] = true;
     return PA_OK;
-}
-
-}  // namespace pa
-
-namespace pa {
-namespace {
-std::mutex g_layout_mu;
-std::unordered_map<uintptr_t, uint64_t> g_layout;  // workspace address -> layout of its last call
-}  // namespace
-
-int prepare_counters(void* workspace, size_t counter_bytes, uint64_t layout, void* stream) {
-    {
-        std::lock_guard<std::mutex> lk(g_layout_mu);
-        const uintptr_t key = reinterpret_cast<uintptr_t>(workspace);
-        auto it = g_layout.find(key);
-        if (it != g_layout.end() && it->second == layout) return PA_OK;
-        if (g_layout.size() >= 4096) g_layout.clear();  // bounded; a forgotten entry only costs a memset
-        g_layout[key] = layout;
-    }
-    return cudaMemsetAsync(workspace, 0, counter_bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? PA_OK
-               : PA_ERR_CUDA;
 }
 
 }  // namespace pa

@@ -64,15 +64,6 @@ int launch_decode(void* out, float* lse, const void* q, const void* k_pool, cons
                   size_t workspace_bytes, int32_t* status, void* stream);
 }  // namespace dec
 
-// The split-K arrival counters at the start of a workspace must be zero when
-// a call starts.  Every successful call leaves its own counters zero, but a
-// workspace whose last call had a different layout may hold that call's
-// partial outputs where this call's counters are.  The library remembers the
-// last layout (the size of the counter region) per workspace address and,
-// when it changes (or on first use), clears `counter_bytes` with one
-// asynchronous memset on `stream`.
-int prepare_counters(void* workspace, size_t counter_bytes, uint64_t layout, void* stream);
-
 // Set the dynamic shared-memory limit of a kernel once per device.
 int set_smem_limit_once(const void* kernel, int bytes, int device, int slot);
 

@@ -42,17 +42,14 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int) -> None:
 
 
 class Workspace:
-    """Zero-initialised device scratch for the split partials and arrival
-    counters.  The kernels leave the counters zero after each successful call;
-    after a device error call ``reset()``.  One workspace per stream that may
-    run a call concurrently."""
+    """Device scratch for the split partials (and each sequence's first work
+    unit).  Every call writes what it reads, so it needs no initialisation
+    and may serve calls of any size that fits.  One workspace per stream that
+    may run a call concurrently."""
 
     def __init__(self, nbytes: int, device):
         self.nbytes = int(max(nbytes, 256))
-        self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device)
-
-    def reset(self) -> None:
-        self.buf.zero_()
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
 
     @property
     def ptr(self) -> int:
