@@ -38,6 +38,15 @@
  * perform no host synchronisation and allocate nothing, so they may be
  * captured in a CUDA graph.
  *
+ * Back-to-back launches: the writeback kernels let the kernel after them
+ * start at once (programmatic dependent launch), and the decode kernels are
+ * launched so that they may start early.  A decode call's kernel then reads
+ * seq_lens, cu_seqlens_q and block_table while the kernel before it still
+ * runs, and reads q and the pools only after that kernel has finished.  So
+ * seq_lens, cu_seqlens_q and block_table must be final before a kernel that
+ * lets its dependents start early (only the writebacks of this library do,
+ * unless the caller's own kernels use programmatic dependent launch).
+ *
  * Element types: K/V pools, q, out, k_new, v_new are bf16 (IEEE binary16
  * "brain float", 2 bytes); lse is float32; integer arrays are int32.
  *

@@ -383,47 +383,28 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    // launched while the previous kernel of the stream (typically the writeback of the
-    // newest K/V rows) may still run: wait for it before reading any input
-    pdl_wait();
     pdl_launch_dependents();  // the merge kernel may be scheduled (it waits for this grid)
+    // Launched as a programmatic dependent: until pdl_wait() below, the previous kernel
+    // of the stream may still run (the writeback of the newest K/V rows lets its
+    // dependents start at once).  Before the wait the kernel reads only seq_lens, cu_q
+    // and block_table, which that kernel does not write, and writes nothing, so the
+    // plan and the first block-table lookups overlap it.
 
-    // ---- plan: total units T (and the defined result of empty sequences)
+    // ---- plan: total units T
     if (warp == 0) {
         int T = 0;
         for (int b0 = 0; b0 < p.batch; b0 += 32) {
             const int b = b0 + lane;
-            int n = 0;
-            if (b < p.batch) {
-                const SeqShape sh = seq_shape(p, b);
-                n = seq_units(p, sh);
-                if (sh.qlen > 0 && sh.len == 0 && (b % gridDim.x) == blockIdx.x) {
-                    // empty sequence: defined result, out = 0, lse = -inf
-                    const size_t row0 = q_row(p, b);
-                    for (int i = 0; i < sh.qlen; ++i)
-                        for (int h = 0; h < p.Hq; ++h) {
-                            const size_t row = (row0 + i) * p.Hq + h;
-                            uint4* o = reinterpret_cast<uint4*>(p.out + row * D);
-                            for (int c = 0; c < D / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
-                            if (p.lse) p.lse[row] = -INFINITY;
-                        }
-                }
-            }
-            const int incl = warp_incl_scan(n);
-            if (blockIdx.x == 0 && b < p.batch) p.seg_base[b] = T + incl - n;
-            T += __shfl_sync(0xffffffffu, incl, 31);
+            T += warp_sum_int(b < p.batch ? seq_units(p, seq_shape(p, b)) : 0);
         }
-        if (lane == 0) {
-            s_plan[0] = T;
-            if (blockIdx.x == 0) p.seg_base[p.batch] = T;
-        }
+        if (lane == 0) s_plan[0] = T;
     }
     __syncthreads();
     // ---- split: CTA c owns the equal range [c S, (c + 1) S) of the units
     const Split sp(s_plan[0], gridDim.x);
     const int U0 = blockIdx.x * sp.S;  // grid * chunk < 2^31 is checked on the host
     const int U1 = min(sp.T, U0 + sp.S);
-    if (U0 >= U1) return;
+    const bool has_work = U0 < U1;
 
     const uint64_t policy = policy_evict_first();
     uint8_t* my_stages = stages + warp * DEPTH * C::STAGE_BYTES;
@@ -438,53 +419,86 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
     const int qc = (lane & 3) * 2;  // column pair of this lane
 
     const int cidx = blockIdx.x;  // this range's chunk
-    // segment holding U0
-    if (warp == 0) {
-        int sb = -1, sP = 0, P = 0;
-        for (int b0 = 0; b0 < p.batch && sb < 0; b0 += 32) {
-            const int b = b0 + lane;
-            const int n = (b < p.batch) ? seq_units(p, seq_shape(p, b)) : 0;
-            const int incl = warp_incl_scan(n);
-            const int tot = __shfl_sync(0xffffffffu, incl, 31);
-            if (U0 < P + tot) {
-                const unsigned hit = __ballot_sync(0xffffffffu, P + incl > U0);
-                const int l = __ffs(hit) - 1;
-                sb = b0 + l;
-                sP = P + __shfl_sync(0xffffffffu, incl - n, l);
-            }
-            P += tot;
-        }
-        if (lane == 0) {
-            s_plan[4] = sb;
-            s_plan[5] = sP;
-        }
-    }
-    __syncthreads();
     Seg seg0;
-    {
+    UnitIter it;
+    int phys0 = -1;  // page of this warp's first unit
+    if (has_work) {
+        // segment holding U0
+        if (warp == 0) {
+            int sb = -1, sP = 0, P = 0;
+            for (int b0 = 0; b0 < p.batch && sb < 0; b0 += 32) {
+                const int b = b0 + lane;
+                const int n = (b < p.batch) ? seq_units(p, seq_shape(p, b)) : 0;
+                const int incl = warp_incl_scan(n);
+                const int tot = __shfl_sync(0xffffffffu, incl, 31);
+                if (U0 < P + tot) {
+                    const unsigned hit = __ballot_sync(0xffffffffu, P + incl > U0);
+                    const int l = __ffs(hit) - 1;
+                    sb = b0 + l;
+                    sP = P + __shfl_sync(0xffffffffu, incl - n, l);
+                }
+                P += tot;
+            }
+            if (lane == 0) {
+                s_plan[4] = sb;
+                s_plan[5] = sP;
+            }
+        }
+        __syncthreads();
         seg_set_seq(seg0, p, s_plan[4]);
         const int idx = (U0 - s_plan[5]) / seg0.n;  // (g, sb) index within sequence b
         seg0.g = idx / seg0.sh.SB;
         seg0.sb = idx - seg0.g * seg0.sh.SB;
         seg0.start = s_plan[5] + idx * seg0.n;
         seg0.end = seg0.start + seg0.n;
+
+        it.seg = seg0;
+        it.U1 = U1;
+        it.pe = min(U1, seg0.end);
+        it.u = U0 + warp;
+        it.done = false;
+        it.pc_base = -1;
+        it.pc_phys = -1;
+        it.norm(p, warp);
+        if (!it.done) phys0 = unit_page(p, it, lane);
     }
+
+    // the previous kernel's writes (K/V rows, possibly q) are visible from here on
+    pdl_wait();
+
+    if (warp == 0) {
+        // first unit of each sequence, for the merge kernel
+        if (blockIdx.x == 0) {
+            int T = 0;
+            for (int b0 = 0; b0 < p.batch; b0 += 32) {
+                const int b = b0 + lane;
+                const int n = b < p.batch ? seq_units(p, seq_shape(p, b)) : 0;
+                const int incl = warp_incl_scan(n);
+                if (b < p.batch) p.seg_base[b] = T + incl - n;
+                T += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) p.seg_base[p.batch] = T;
+        }
+        // empty sequences have a defined result: out = 0, lse = -inf
+        for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
+            const SeqShape sh = seq_shape(p, b);
+            if (sh.qlen > 0 && sh.len == 0) {
+                const size_t row0 = q_row(p, b) * p.Hq;
+                for (int i = lane; i < sh.qlen * p.Hq * (D / 8); i += 32)
+                    reinterpret_cast<uint4*>(p.out + row0 * D)[i] = make_uint4(0, 0, 0, 0);
+                if (p.lse)
+                    for (int i = lane; i < sh.qlen * p.Hq; i += 32) p.lse[row0 + i] = -INFINITY;
+            }
+        }
+    }
+    if (!has_work) return;
 
     // ---- prologue: fill this warp's pipeline, one cp.async group per stage (empty
     // groups once the warp runs out of units)
-    UnitIter it;
-    it.seg = seg0;
-    it.U1 = U1;
-    it.pe = min(U1, seg0.end);
-    it.u = U0 + warp;
-    it.done = false;
-    it.pc_base = -1;
-    it.pc_phys = -1;
-    it.norm(p, warp);
     uint32_t consumed = 0;
     for (int i = 0; i < DEPTH; ++i) {
         if (!it.done) {
-            const int phys = unit_page(p, it, lane);
+            const int phys = i == 0 ? phys0 : unit_page(p, it, lane);
             issue_unit<D, FP8, SWAP>(p, it, phys, my_stages + i * C::STAGE_BYTES, &s_phys[warp][i], lane, policy);
             it.u += W;
             it.norm(p, warp);
