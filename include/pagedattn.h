@@ -47,8 +47,18 @@
  * lets its dependents start early (only the writebacks of this library do,
  * unless the caller's own kernels use programmatic dependent launch).
  *
- * Element types: K/V pools, q, out, k_new, v_new are bf16 (IEEE binary16
- * "brain float", 2 bytes); lse is float32; integer arrays are int32.
+ * Memory: the K/V pools, block_table, the workspace and every argument of
+ * attn_prefill_varlen_causal must be device memory.  The small per-step
+ * arguments of the decode and writeback calls (q, out, lse, k_new, v_new,
+ * seq_lens, cu_seqlens_q, cu_seqlens_new) may instead be page-locked host
+ * memory (cudaHostAlloc / cudaHostRegister): the kernels read and write it
+ * in place over the CPU-GPU link (NVLink-C2C on GB300), which for a decode
+ * step's few hundred kilobytes costs less than staging copies on the copy
+ * engine.
+ *
+ * Element types: K/V pools, q, out, k_new, v_new are bf16 (bfloat16: sign,
+ * 8 exponent and 7 mantissa bits, 2 bytes); lse is float32; integer arrays
+ * are int32.
  *
  * Layouts (row-major, contiguous):
  *   k_pool, v_pool : [num_pages][num_kv_heads][page_size][head_dim]

@@ -1,9 +1,11 @@
 """Torch-facing wrappers of the C ABI: argument marshalling only.
 
-Every function takes CUDA tensors, checks dtypes/shapes/contiguity, passes
-raw device pointers and the current CUDA stream to libpagedattn.so, and
-raises ``PagedAttnError`` on a non-zero status.  No arithmetic of the method
-happens here and there is no CPU path.
+Every function takes CUDA tensors (the decode and writeback calls also take
+pinned host tensors for their small per-step arguments: q, out, lse, the new
+K/V rows, seq_lens, cu_seqlens), checks dtypes/shapes/contiguity, passes raw
+pointers and the current CUDA stream to libpagedattn.so, and raises
+``PagedAttnError`` on a non-zero status.  No arithmetic of the method happens
+here and there is no CPU path.
 """
 
 from __future__ import annotations
@@ -28,11 +30,16 @@ def _stream_handle(stream) -> int:
     return stream.cuda_stream
 
 
-def _need(t: torch.Tensor, name: str, dtype, ndim: int) -> None:
+def _need(t: torch.Tensor, name: str, dtype, ndim: int, host_ok: bool = False) -> None:
+    """Check a tensor argument.  ``host_ok``: a pinned (page-locked) host
+    tensor is accepted too; the kernels read or write it in place over the
+    CPU-GPU link (NVLink-C2C on GB300), which for a decode step's small
+    per-step tensors is cheaper than staging copies."""
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
-    if not t.is_cuda:
-        raise ValueError("%s must be a CUDA tensor (there is no CPU path)" % name)
+    if not (t.is_cuda or (host_ok and t.is_pinned())):
+        raise ValueError("%s must be a CUDA tensor%s (there is no CPU path)"
+                         % (name, " or a pinned host tensor" if host_ok else ""))
     if t.dtype != dtype:
         raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
     if t.dim() != ndim:
@@ -98,10 +105,10 @@ def kv_write_paged(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch.Tens
     lib = _lib.load()
     _need(k_pool, "k_pool", torch.bfloat16, 4)
     _need(v_pool, "v_pool", torch.bfloat16, 4)
-    _need(k_new, "k_new", torch.bfloat16, 3)
-    _need(v_new, "v_new", torch.bfloat16, 3)
-    _need(cu_seqlens_new, "cu_seqlens_new", torch.int32, 1)
-    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(k_new, "k_new", torch.bfloat16, 3, host_ok=True)
+    _need(v_new, "v_new", torch.bfloat16, 3, host_ok=True)
+    _need(cu_seqlens_new, "cu_seqlens_new", torch.int32, 1, host_ok=True)
+    _need(seq_lens, "seq_lens", torch.int32, 1, host_ok=True)
     _need(block_table, "block_table", torch.int32, 2)
     P, Hkv, ps, D = k_pool.shape
     if v_pool.shape != k_pool.shape or k_new.shape != v_new.shape or k_new.shape[1:] != (Hkv, D):
@@ -129,17 +136,17 @@ def kv_write_paged_rope(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch
     lib = _lib.load()
     _need(k_pool, "k_pool", torch.bfloat16, 4)
     _need(v_pool, "v_pool", torch.bfloat16, 4)
-    _need(k_new, "k_new", torch.bfloat16, 3)
-    _need(v_new, "v_new", torch.bfloat16, 3)
-    _need(cu_seqlens_new, "cu_seqlens_new", torch.int32, 1)
-    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(k_new, "k_new", torch.bfloat16, 3, host_ok=True)
+    _need(v_new, "v_new", torch.bfloat16, 3, host_ok=True)
+    _need(cu_seqlens_new, "cu_seqlens_new", torch.int32, 1, host_ok=True)
+    _need(seq_lens, "seq_lens", torch.int32, 1, host_ok=True)
     _need(block_table, "block_table", torch.int32, 2)
     P, Hkv, ps, D = k_pool.shape
     if v_pool.shape != k_pool.shape or k_new.shape != v_new.shape or k_new.shape[1:] != (Hkv, D):
         raise ValueError("inconsistent K/V shapes")
     Hq = 0
     if q is not None:
-        _need(q, "q", torch.bfloat16, 3)
+        _need(q, "q", torch.bfloat16, 3, host_ok=True)
         if q.shape[0] != k_new.shape[0] or q.shape[2] != D:
             raise ValueError("q must be [total_new][Hq][head_dim]")
         Hq = q.shape[1]
@@ -179,10 +186,10 @@ def kv_write_paged_fp8(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch.
     saturating) and write them into the FP8 pools (V transposed per page block)."""
     lib = _lib.load()
     P, Hkv, ps, D = _need_fp8_pools(k_pool, v_pool, k_scale, v_scale)
-    _need(k_new, "k_new", torch.bfloat16, 3)
-    _need(v_new, "v_new", torch.bfloat16, 3)
-    _need(cu_seqlens_new, "cu_seqlens_new", torch.int32, 1)
-    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(k_new, "k_new", torch.bfloat16, 3, host_ok=True)
+    _need(v_new, "v_new", torch.bfloat16, 3, host_ok=True)
+    _need(cu_seqlens_new, "cu_seqlens_new", torch.int32, 1, host_ok=True)
+    _need(seq_lens, "seq_lens", torch.int32, 1, host_ok=True)
     _need(block_table, "block_table", torch.int32, 2)
     if k_new.shape != v_new.shape or k_new.shape[1:] != (Hkv, D):
         raise ValueError("k_new / v_new must be [total_new][Hkv][head_dim]")
@@ -204,10 +211,10 @@ def attn_decode_paged_fp8(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.T
                           status: Optional[torch.Tensor] = None, stream=None):
     """Split-K paged decode over an FP8 (e4m3) cache with per-KV-head scales."""
     lib = _lib.load()
-    _need(q, "q", torch.bfloat16, 3)
+    _need(q, "q", torch.bfloat16, 3, host_ok=True)
     P, Hkv, ps, D = _need_fp8_pools(k_pool, v_pool, k_scale, v_scale)
     _need(block_table, "block_table", torch.int32, 2)
-    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(seq_lens, "seq_lens", torch.int32, 1, host_ok=True)
     B, Hq, Dq = q.shape
     if Dq != D:
         raise ValueError("inconsistent head_dim")
@@ -218,16 +225,16 @@ def attn_decode_paged_fp8(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.T
     if max_seq_len is None:
         max_seq_len = block_table.shape[1] * ps
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=q.dtype, device=k_pool.device)
     else:
-        _need(out, "out", torch.bfloat16, 3)
+        _need(out, "out", torch.bfloat16, 3, host_ok=True)
     if return_lse and lse is None:
-        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=k_pool.device)
     if lse is not None:
-        _need(lse, "lse", torch.float32, 2)
+        _need(lse, "lse", torch.float32, 2, host_ok=True)
     need = int(lib.pa_decode_workspace_bytes(B, Hq, Hkv, D)) if B > 0 else 0
     if workspace is None:
-        workspace = _cached_ws("decode", need, q.device)
+        workspace = _cached_ws("decode", need, k_pool.device)
     rc = lib.attn_decode_paged_fp8(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
                                    _ptr(v_scale), P, _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B,
                                    int(max_seq_len), ps, Hq, Hkv, D, float(softmax_scale), workspace.ptr,
@@ -250,11 +257,11 @@ def attn_decode_paged(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tenso
     table's capacity).  Returns out (and lse if requested).
     """
     lib = _lib.load()
-    _need(q, "q", torch.bfloat16, 3)
+    _need(q, "q", torch.bfloat16, 3, host_ok=True)
     _need(k_pool, "k_pool", torch.bfloat16, 4)
     _need(v_pool, "v_pool", torch.bfloat16, 4)
     _need(block_table, "block_table", torch.int32, 2)
-    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(seq_lens, "seq_lens", torch.int32, 1, host_ok=True)
     B, Hq, D = q.shape
     P, Hkv, ps, D2 = k_pool.shape
     if D2 != D or v_pool.shape != k_pool.shape:
@@ -266,16 +273,16 @@ def attn_decode_paged(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tenso
     if max_seq_len is None:
         max_seq_len = block_table.shape[1] * ps
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=q.dtype, device=k_pool.device)
     else:
-        _need(out, "out", torch.bfloat16, 3)
+        _need(out, "out", torch.bfloat16, 3, host_ok=True)
     if return_lse and lse is None:
-        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=k_pool.device)
     if lse is not None:
-        _need(lse, "lse", torch.float32, 2)
+        _need(lse, "lse", torch.float32, 2, host_ok=True)
     need = int(lib.pa_decode_workspace_bytes(B, Hq, Hkv, D)) if B > 0 else 0
     if workspace is None:
-        workspace = _cached_ws("decode", need, q.device)
+        workspace = _cached_ws("decode", need, k_pool.device)
     rc = lib.attn_decode_paged(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_pool), _ptr(v_pool), P, _ptr(block_table),
                                block_table.shape[1], _ptr(seq_lens), B, int(max_seq_len), ps, Hq, Hkv, D,
                                float(softmax_scale), workspace.ptr, workspace.nbytes, _ptr(status),
@@ -299,12 +306,12 @@ def attn_decode_multiquery_paged(q: torch.Tensor, k_pool: torch.Tensor, v_pool: 
     row counts; it sizes the workspace and the launch.
     """
     lib = _lib.load()
-    _need(q, "q", torch.bfloat16, 3)
+    _need(q, "q", torch.bfloat16, 3, host_ok=True)
     _need(k_pool, "k_pool", torch.bfloat16, 4)
     _need(v_pool, "v_pool", torch.bfloat16, 4)
     _need(block_table, "block_table", torch.int32, 2)
-    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
-    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1, host_ok=True)
+    _need(seq_lens, "seq_lens", torch.int32, 1, host_ok=True)
     Tq, Hq, D = q.shape
     P, Hkv, ps, D2 = k_pool.shape
     B = seq_lens.shape[0]
@@ -319,16 +326,16 @@ def attn_decode_multiquery_paged(q: torch.Tensor, k_pool: torch.Tensor, v_pool: 
     if max_q_len is None:
         max_q_len = max(1, min(8, Tq))
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=q.dtype, device=k_pool.device)
     else:
-        _need(out, "out", torch.bfloat16, 3)
+        _need(out, "out", torch.bfloat16, 3, host_ok=True)
     if return_lse and lse is None:
-        lse = torch.empty((Tq, Hq), dtype=torch.float32, device=q.device)
+        lse = torch.empty((Tq, Hq), dtype=torch.float32, device=k_pool.device)
     if lse is not None:
-        _need(lse, "lse", torch.float32, 2)
+        _need(lse, "lse", torch.float32, 2, host_ok=True)
     need = int(lib.pa_decode_multiquery_workspace_bytes(B, int(max_q_len), Hq, Hkv, D)) if B > 0 else 0
     if workspace is None:
-        workspace = _cached_ws("decode", need, q.device)
+        workspace = _cached_ws("decode", need, k_pool.device)
     rc = lib.attn_decode_multiquery_paged(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_pool), _ptr(v_pool), P,
                                           _ptr(block_table), block_table.shape[1], _ptr(cu_seqlens_q),
                                           _ptr(seq_lens), B, Tq, int(max_q_len), int(max_seq_len), ps, Hq, Hkv, D,

@@ -156,3 +156,46 @@ def test_llama8b_ragged_decode_full_size_sampled(cuda_device):
     order = sorted(range(len(lens)), key=lambda b: lens[b])
     seqs = [order[0], order[len(order) // 2], order[-1]]  # shortest, median, longest
     _sampled_full_size(case, seqs, cuda_device)
+
+
+def test_pinned_host_arguments_match_device(cuda_device):
+    """q, out, lse, the new K/V rows, seq_lens and cu_seqlens in pinned host
+    memory (read and written in place by the kernels) give the same bits as
+    device copies: writeback, decode and multi-query decode."""
+    pa = _pa()
+    dev = cuda_device
+    case = workloads.make_paged_case("pinned", [700, 33, 4096, 1], [1, 1, 1, 1], 28, 4, 128, seed=81,
+                                     prewritten=False, device=dev)
+    pools = (case.k_pool.clone(), case.v_pool.clone())
+    ones = torch.arange(case.batch + 1, dtype=torch.int32, device=dev)
+    # device path
+    pa.kv_write_paged(case.k_pool, case.v_pool, case.k_new, case.v_new, ones, case.seq_lens, case.block_table)
+    out_d, lse_d = pa.attn_decode_paged(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
+                                        case.softmax_scale, max_seq_len=case.max_seq_len, return_lse=True)
+    # pinned host path on fresh pools
+    k2, v2 = pools
+    h = {n: getattr(case, n).cpu().pin_memory() for n in ("q", "k_new", "v_new", "seq_lens")}
+    h_ones = ones.cpu().pin_memory()
+    out_h = torch.full(case.q.shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.full((case.batch, case.num_q_heads), float("nan"), dtype=torch.float32).pin_memory()
+    status = pa.new_status(dev)
+    pa.kv_write_paged(k2, v2, h["k_new"], h["v_new"], h_ones, h["seq_lens"], case.block_table, status=status)
+    pa.attn_decode_paged(h["q"], k2, v2, case.block_table, h["seq_lens"], case.softmax_scale,
+                         max_seq_len=case.max_seq_len, out=out_h, lse=lse_h, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(k2.view(torch.int16), case.k_pool.view(torch.int16))
+    assert torch.equal(v2.view(torch.int16), case.v_pool.view(torch.int16))
+    assert torch.equal(out_h.view(torch.int16), out_d.cpu().view(torch.int16))
+    assert torch.equal(lse_h, lse_d.cpu())
+    # multi-query decode (2 rows per sequence) with host q / out / cu_seqlens_q / seq_lens
+    mq = workloads.make_paged_case("pinned_mq", [300, 64, 2000], [2, 2, 2], 28, 4, 128, seed=82, device=dev)
+    ref = pa.attn_decode_multiquery_paged(mq.q, mq.k_pool, mq.v_pool, mq.block_table, mq.cu_seqlens_q, mq.seq_lens,
+                                          mq.softmax_scale, max_q_len=2, max_seq_len=mq.max_seq_len)
+    hq = mq.q.cpu().pin_memory()
+    hout = torch.empty(mq.q.shape, dtype=torch.bfloat16).pin_memory()
+    pa.attn_decode_multiquery_paged(hq, mq.k_pool, mq.v_pool, mq.block_table, mq.cu_seqlens_q.cpu().pin_memory(),
+                                    mq.seq_lens.cpu().pin_memory(), mq.softmax_scale, max_q_len=2,
+                                    max_seq_len=mq.max_seq_len, out=hout)
+    torch.cuda.synchronize()
+    assert torch.equal(hout.view(torch.int16), ref.cpu().view(torch.int16))
