@@ -503,7 +503,7 @@ def measure_fp8_decode(pa, steps, warmup, peaks):
            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]},
            "tokens_per_s": B / (t * 1e-3), "l2": "flushed (256 MiB write) between iterations", "steps": steps,
-           "launches_per_step": 1}
+           "launches_per_step": 2}  # decode + merge
     del case, kc, vc, flush
     torch.cuda.empty_cache()
     return res
@@ -633,7 +633,7 @@ def measure_multiquery(pa, steps, warmup, peaks, q_len=4):
            "q_len": q_len, "ms": t, "kv_bytes": kv,
            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]},
-           "tokens_per_s": B * q_len / (t * 1e-3), "steps": steps, "launches_per_step": 1,
+           "tokens_per_s": B * q_len / (t * 1e-3), "steps": steps, "launches_per_step": 2,
            "l2": "inputs larger than L2 (512 MiB of KV), no flush"}
     del case
     torch.cuda.empty_cache()
