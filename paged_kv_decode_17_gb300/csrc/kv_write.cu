@@ -245,7 +245,14 @@ __global__ void __launch_bounds__(kWarps * 32) kv_write_rope_kernel(const __grid
         }
         if (p.q != nullptr) {
             __nv_bfloat16* qrow = p.q + (size_t)t * p.Hq * D;
+            // eight head rows per batch of loads: one warp keeps 2 KB in flight
             int h = 0;
+            for (; h + 8 <= p.Hq; h += 8) {
+                __nv_bfloat16* qd[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) qd[k] = qrow + (h + k) * D;
+                rope_rows<D, 8>(qrow + h * D, D, qd, p.q_norm_w, p.eps, lane, c, s);
+            }
             for (; h + 4 <= p.Hq; h += 4) {
                 __nv_bfloat16* qd[4] = {qrow + h * D, qrow + (h + 1) * D, qrow + (h + 2) * D, qrow + (h + 3) * D};
                 rope_rows<D, 4>(qrow + h * D, D, qd, p.q_norm_w, p.eps, lane, c, s);
