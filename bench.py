@@ -312,21 +312,21 @@ def _events(stream, n):
 
 
 def measure_decode(pa, case, steps, warmup, pg):
-    """Decode step = writeback of the newest K/V row + split-K decode (decode
-    and merge kernels).  The K timed steps run back to back (each launch a
-    programmatic dependent of the one before); a second pass with events
-    between the calls splits the time into writeback and decode."""
+    """Decode step = split-K decode with each sequence's newest K/V row written
+    back by the same kernel (attn_decode_paged_append: decode + merge
+    kernels).  The K timed steps run back to back (each launch a programmatic
+    dependent of the one before); a second pass with events around each call
+    gives the per-call time for the roofline."""
     dev = case.q.device
     stream = torch.cuda.current_stream()
     B, Hq, D = case.q.shape
     ws = pa.Workspace(pa.decode_workspace_bytes(B, Hq, case.num_kv_heads, D), dev)
     out = torch.empty_like(case.q)
-    ones = torch.arange(B + 1, dtype=torch.int32, device=dev)  # one new row per sequence
 
     def step():
-        pa.kv_write_paged(case.k_pool, case.v_pool, case.k_new, case.v_new, ones, case.seq_lens, case.block_table)
         pa.attn_decode_paged(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
-                             case.softmax_scale, max_seq_len=case.max_seq_len, out=out, workspace=ws)
+                             case.softmax_scale, max_seq_len=case.max_seq_len, out=out, workspace=ws,
+                             k_new=case.k_new, v_new=case.v_new)
 
     for _ in range(warmup):
         step()
@@ -345,38 +345,32 @@ def measure_decode(pa, case, steps, warmup, pg):
     barrier(pg)
     torch.cuda.synchronize()
     total_ms = t_start.elapsed_time(t_end)
-    ev = _events(stream, 3 * steps)
+    ev = _events(stream, 2 * steps)
     for i in range(steps):
-        ev[3 * i].record(stream)
-        pa.kv_write_paged(case.k_pool, case.v_pool, case.k_new, case.v_new, ones, case.seq_lens, case.block_table)
-        ev[3 * i + 1].record(stream)
-        pa.attn_decode_paged(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
-                             case.softmax_scale, max_seq_len=case.max_seq_len, out=out, workspace=ws)
-        ev[3 * i + 2].record(stream)
+        ev[2 * i].record(stream)
+        step()
+        ev[2 * i + 1].record(stream)
     torch.cuda.synchronize()
-    dec_ms = [ev[3 * i + 1].elapsed_time(ev[3 * i + 2]) for i in range(steps)]
-    kvw_ms = [ev[3 * i].elapsed_time(ev[3 * i + 1]) for i in range(steps)]
-    return total_ms, dec_ms, kvw_ms, sampler.summary(), 3 * steps
+    dec_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(steps)]
+    return total_ms, dec_ms, sampler.summary(), 2 * steps
 
 
 def measure_decode_e2e(pa, case, steps, warmup):
     """Same step through the public API with the step's inputs and result in
-    pinned host memory: the writeback and decode kernels read q, the new K/V
-    rows and seq_lens, and write the attention output, in place over the
-    CPU-GPU link (NVLink-C2C on GB300), as a serving loop on this machine
-    would pass them; no copy-engine copies."""
+    pinned host memory: the kernels read q, the new K/V rows and seq_lens,
+    and write the attention output, in place over the CPU-GPU link
+    (NVLink-C2C on GB300), as a serving loop on this machine would pass them;
+    no copy-engine copies."""
     dev = case.q.device
     B, Hq, D = case.q.shape
     ws = pa.Workspace(pa.decode_workspace_bytes(B, Hq, case.num_kv_heads, D), dev)
     h_q, h_k, h_v, h_len = (t.cpu().pin_memory() for t in (case.q, case.k_new, case.v_new, case.seq_lens))
     h_out = torch.empty(case.q.shape, dtype=case.q.dtype).pin_memory()
-    ones = torch.arange(B + 1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
 
     def step():
-        pa.kv_write_paged(case.k_pool, case.v_pool, h_k, h_v, ones, h_len, case.block_table)
         pa.attn_decode_paged(h_q, case.k_pool, case.v_pool, case.block_table, h_len, case.softmax_scale,
-                             max_seq_len=case.max_seq_len, out=h_out, workspace=ws)
+                             max_seq_len=case.max_seq_len, out=h_out, workspace=ws, k_new=h_k, v_new=h_v)
 
     for _ in range(warmup):
         step()
@@ -673,7 +667,7 @@ def main(argv=None):
 
     case = workloads.qwen7b_decode(device=dev, seed=1 + rank)
     kv_bytes = roofline.decode_kv_bytes(case.seq_lens_host, case.num_kv_heads, case.head_dim)
-    total_ms, dec_ms, kvw_ms, clocks, launches = measure_decode(pa, case, args.steps, args.warmup, pg)
+    total_ms, dec_ms, clocks, launches = measure_decode(pa, case, args.steps, args.warmup, pg)
     total_ms = max_over_ranks(pg, total_ms)
     ms_per_step = total_ms / args.steps
     all_bytes = sum_over_ranks(pg, kv_bytes * args.steps)
@@ -694,14 +688,15 @@ def main(argv=None):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "qwen7b_decode: batch 32 x 8192-token contexts, Hq=28, Hkv=4, head_dim 128, "
-                               "16-token pages, 16384-page pool (seeded permutation); step = KV writeback of the "
-                               "newest row + split-K decode",
+                               "16-token pages, 16384-page pool (seeded permutation); step = split-K decode with "
+                               "the KV writeback of each sequence's newest row in the same kernel "
+                               "(attn_decode_paged_append)",
                    "batch": 32, "ctx": 8192, "Hq": 28, "Hkv": 4, "head_dim": 128, "page_size": 16,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2: 512 MiB of KV read per step vs 129 MB L2, no flush"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "kernel": "attn_decode_paged (decode_kernel<128> + merge_kernel<128>)",
+                     "kernel": "attn_decode_paged_append (decode_kernel<128> + merge_kernel<128>)",
                      "algorithmic_bytes_per_launch": kv_bytes, "launch_ms": dec_avg,
                      "peak_source": peaks["source"]},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -710,7 +705,6 @@ def main(argv=None):
                             "kernels over NVLink-C2C (no copy-engine copies)"},
         "gpu_launches": launches * world,
         "clocks": clocks,
-        "kv_write_ms": statistics.mean(kvw_ms),
     }
     if not args.decode_only:
         psteps = max(3, min(args.steps, 20))

@@ -18,6 +18,8 @@
  *                                and merged with the log-sum-exp identity
  *                                ("The Stack Below the Stack, Part 2",
  *                                section 2.2 Flash-Decoding, steps 1-3).
+ *   attn_decode_paged_append     writeback of each sequence's newest row and
+ *                                the decode, in one kernel.
  *   attn_decode_multiquery_paged the same for a short block (2-8) of query
  *                                rows per sequence, causal inside the block
  *                                (speculative-decode verification).
@@ -32,8 +34,9 @@
  * Common conventions
  * ------------------
  * Pointers named *_pool, q, out, k_new, v_new, block_table, seq_lens,
- * cu_seqlens_*, lse, workspace and status are DEVICE pointers; the caller
- * owns every buffer (nothing is allocated by the library).  All calls are
+ * cu_seqlens_*, lse, workspace and status are pointers the GPU accesses:
+ * device memory, or page-locked host memory where "Memory" below allows it;
+ * the caller owns every buffer (nothing is allocated by the library).  All calls are
  * asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream),
  * perform no host synchronisation and allocate nothing, so they may be
  * captured in a CUDA graph.
@@ -50,7 +53,8 @@
  * Memory: the K/V pools, block_table, the workspace and every argument of
  * attn_prefill_varlen_causal must be device memory.  The small per-step
  * arguments of the decode and writeback calls (q, out, lse, k_new, v_new,
- * seq_lens, cu_seqlens_q, cu_seqlens_new) may instead be page-locked host
+ * seq_lens, cu_seqlens_q, cu_seqlens_new; also k_new and v_new of
+ * attn_decode_paged_append) may instead be page-locked host
  * memory (cudaHostAlloc / cudaHostRegister): the kernels read and write it
  * in place over the CPU-GPU link (NVLink-C2C on GB300), which for a decode
  * step's few hundred kilobytes costs less than staging copies on the copy
@@ -139,6 +143,26 @@ int attn_decode_paged(void* out, float* lse, const void* q, const void* k_pool, 
                       const int32_t* seq_lens, int batch, int max_seq_len, int page_size,
                       int num_q_heads, int num_kv_heads, int head_dim, float softmax_scale,
                       void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * Decode with the writeback of the newest rows in the same kernel ("Inside
+ * Ion", section "IonAttention in One Paragraph": KV pages are written back
+ * eagerly as they are produced): the result of kv_write_paged (one new row
+ * per sequence, at position seq_lens[b] - 1) followed by attn_decode_paged,
+ * in one call.  The decode stages each sequence's newest K/V row from
+ * k_new / v_new instead of its pool slot, and one warp per (sequence, KV
+ * head) writes the row into that slot (bit-exact copy).
+ *   k_pool, v_pool  written at the new rows' slots (block_table must map
+ *                   position seq_lens[b] - 1 to an allocated page)
+ *   k_new, v_new    bf16 [batch][num_kv_heads][head_dim]
+ * Other arguments, workspace and results as attn_decode_paged.  bf16 pools
+ * only (the FP8 cache keeps kv_write_paged_fp8 + attn_decode_paged_fp8).
+ */
+int attn_decode_paged_append(void* out, float* lse, const void* q, void* k_pool, void* v_pool,
+                             const void* k_new, const void* v_new, int num_pages, const int32_t* block_table,
+                             int max_pages_per_seq, const int32_t* seq_lens, int batch, int max_seq_len,
+                             int page_size, int num_q_heads, int num_kv_heads, int head_dim, float softmax_scale,
+                             void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
  * Workspace bytes attn_decode_multiquery_paged needs when no entry has more

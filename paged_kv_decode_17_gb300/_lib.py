@@ -32,6 +32,14 @@ SIGNATURES = {
         c_int, c_int, c_int, c_float,  # Hq, Hkv, D, scale
         c_void_p, c_size_t, c_void_p, c_void_p,  # workspace, bytes, status, stream
     ]),
+    "attn_decode_paged_append": (c_int, [
+        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,  # out, lse, q, k_pool, v_pool
+        c_void_p, c_void_p,  # k_new, v_new
+        c_int, c_void_p, c_int,  # num_pages, block_table, max_pages_per_seq
+        c_void_p, c_int, c_int, c_int,  # seq_lens, batch, max_seq_len, page_size
+        c_int, c_int, c_int, c_float,  # Hq, Hkv, D, scale
+        c_void_p, c_size_t, c_void_p, c_void_p,  # workspace, bytes, status, stream
+    ]),
     "attn_decode_paged_noalloc": (c_int, [
         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,  # out, lse, q, k_pool, v_pool
         c_int, c_void_p, c_int,  # num_pages, block_table, max_pages_per_seq

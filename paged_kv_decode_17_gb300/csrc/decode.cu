@@ -91,6 +91,10 @@ struct Params {
     const __nv_bfloat16* q;
     const __nv_bfloat16* k_pool;  // FP8 variant: e4m3 codes, [page][Hkv][page_size][D]
     const __nv_bfloat16* v_pool;  // FP8 variant: e4m3 codes, [page][Hkv][D][page_size] (transposed)
+    const __nv_bfloat16* k_new;   // append (bf16 only): K/V rows of the query tokens, [rows][Hkv][D],
+    const __nv_bfloat16* v_new;   // read in place of their pool slots and written there; null: none
+    __nv_bfloat16* k_pool_w;      // append: the pools, writable
+    __nv_bfloat16* v_pool_w;
     const float* k_scale;         // FP8 variant: [Hkv], K = code * k_scale[g]
     const float* v_scale;         // FP8 variant: [Hkv], V = code * v_scale[g]
     const int32_t* block_table;
@@ -249,7 +253,7 @@ __device__ __forceinline__ int unit_page(const Params& p, UnitIter& it, int lane
 // Rows past the sequence end are not copied; their V rows are zeroed (their
 // slots may hold anything and 0 * NaN = NaN), their K rows are masked later.
 // Every call commits exactly one cp.async group (possibly empty).
-template <int D, bool FP8, bool SWAP>
+template <int D, bool FP8, bool SWAP, bool APPEND>
 __device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, int phys, uint8_t* stage,
                                            int* phys_slot, int lane, uint64_t policy) {
     using C = Cfg<D, FP8, SWAP>;
@@ -291,19 +295,46 @@ __device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, 
         } else {
             const char* ksrc = reinterpret_cast<const char*>(p.k_pool + row * D);
             const char* vsrc = reinterpret_cast<const char*>(p.v_pool + row * D);
+            // append: rows r >= nf of the unit are the query tokens' own K/V (new token r - nf of
+            // the sequence), not yet in the pool; that unit (one per sequence and head) is staged
+            // by a second copy loop that takes them from k_new / v_new
+            const int nf = APPEND ? it.seg.sh.len - it.seg.sh.qlen - tok0 : UNIT;
+            if (APPEND && nf < UNIT) {
+                const size_t nrow = q_row(p, it.seg.b) * p.Hkv + it.seg.g;  // new token 0, head g
+                const char* knew = reinterpret_cast<const char*>(p.k_new + nrow * D);
+                const char* vnew = reinterpret_cast<const char*>(p.v_new + nrow * D);
 #pragma unroll
-            for (int i = 0; i < CH; ++i) {
-                const int q = i * 32 + lane;
-                const int t = q / (UNIT * CH);  // 0 = K, 1 = V
-                const int qq = q - t * UNIT * CH;
-                const int r = qq / CH;
-                const int cc = qq - r * CH;
-                const uint32_t dst = sbase + t * C::UNIT_BYTES + (cc >> 3) * C::BOX_BYTES + r * 128 +
-                                     (((cc & 7) ^ (r & 7)) << 4);
-                if (r < valid) {
-                    cp_async_16(dst, (t ? vsrc : ksrc) + r * D * 2 + cc * 16, policy);
-                } else if (t == 1) {
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+                for (int i = 0; i < CH; ++i) {
+                    const int q = i * 32 + lane;
+                    const int t = q / (UNIT * CH);  // 0 = K, 1 = V
+                    const int qq = q - t * UNIT * CH;
+                    const int r = qq / CH;
+                    const int cc = qq - r * CH;
+                    const uint32_t dst = sbase + t * C::UNIT_BYTES + (cc >> 3) * C::BOX_BYTES + r * 128 +
+                                         (((cc & 7) ^ (r & 7)) << 4);
+                    if (r < valid) {
+                        const char* src = r >= nf ? (t ? vnew : knew) + (size_t)(r - nf) * p.Hkv * D * 2 + cc * 16
+                                                  : (t ? vsrc : ksrc) + r * D * 2 + cc * 16;
+                        cp_async_16(dst, src, policy);
+                    } else if (t == 1) {
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < CH; ++i) {
+                    const int q = i * 32 + lane;
+                    const int t = q / (UNIT * CH);  // 0 = K, 1 = V
+                    const int qq = q - t * UNIT * CH;
+                    const int r = qq / CH;
+                    const int cc = qq - r * CH;
+                    const uint32_t dst = sbase + t * C::UNIT_BYTES + (cc >> 3) * C::BOX_BYTES + r * 128 +
+                                         (((cc & 7) ^ (r & 7)) << 4);
+                    if (r < valid) {
+                        cp_async_16(dst, (t ? vsrc : ksrc) + r * D * 2 + cc * 16, policy);
+                    } else if (t == 1) {
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+                    }
                 }
             }
         }
@@ -365,7 +396,7 @@ struct Split {
     __device__ __forceinline__ int chunk_of(int u) const { return u / S; }
 };
 
-template <int D, bool FP8, bool SWAP>
+template <int D, bool FP8, bool SWAP, bool APPEND>
 __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
     decode_kernel(const Params p) {
     using C = Cfg<D, FP8, SWAP>;
@@ -499,7 +530,7 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
     for (int i = 0; i < DEPTH; ++i) {
         if (!it.done) {
             const int phys = i == 0 ? phys0 : unit_page(p, it, lane);
-            issue_unit<D, FP8, SWAP>(p, it, phys, my_stages + i * C::STAGE_BYTES, &s_phys[warp][i], lane, policy);
+            issue_unit<D, FP8, SWAP, APPEND>(p, it, phys, my_stages + i * C::STAGE_BYTES, &s_phys[warp][i], lane, policy);
             it.u += W;
             it.norm(p, warp);
         } else {
@@ -826,12 +857,35 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
                 }
                 }
             }
+            if constexpr (APPEND) {
+                // append: the warp that staged this unit for segment 0 and row block 0 (exactly one
+                // per key block and KV head) writes its new rows from shared memory to their slots
+                if (phys >= 0 && cs.sb == 0 && wrb == 0 &&
+                    ((u - cs.start) >> cs.sh.nrb_shift) * UNIT + UNIT > cs.sh.len - cs.sh.qlen) {
+                    constexpr int CH = D / 8;  // 16-byte chunks per row
+                    const int tok0 = ((u - cs.start) >> cs.sh.nrb_shift) * UNIT;
+                    const int r1 = min(UNIT, cs.sh.len - tok0);
+                    if (lane < 2 * CH) {
+                        const int cc = lane % CH;
+                        const bool isv = lane >= CH;
+                        const size_t row0 = ((size_t)phys * p.Hkv + cs.g) * p.page_size + (tok0 & (p.page_size - 1));
+                        for (int r = max(0, cs.sh.len - cs.sh.qlen - tok0); r < r1; ++r) {
+                            uint4 v;
+                            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                                         : "r"(smem_u32(isv ? sv : sk) + (cc >> 3) * C::BOX_BYTES + r * 128 +
+                                               (((cc & 7) ^ (r & 7)) << 4)));
+                            *reinterpret_cast<uint4*>((isv ? p.v_pool_w : p.k_pool_w) + (row0 + r) * D + cc * 8) = v;
+                        }
+                    }
+                }
+            }
             __syncwarp();  // every lane is done reading this stage
             ++consumed;
             if (!it.done) {
                 const int phys_next = unit_page(p, it, lane);
-                issue_unit<D, FP8, SWAP>(p, it, phys_next, my_stages + st * C::STAGE_BYTES, &s_phys[warp][st], lane,
-                                         policy);
+                issue_unit<D, FP8, SWAP, APPEND>(p, it, phys_next, my_stages + st * C::STAGE_BYTES,
+                                                 &s_phys[warp][st], lane, policy);
                 it.u += W;
                 it.norm(p, warp);
             } else {
@@ -1084,7 +1138,8 @@ namespace dec {
 // longer entries are left to the prefill kernel.
 // k_scale / v_scale non-null: the pools hold e4m3 codes (V transposed per page block).
 static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool,
-                            const float* k_scale, const float* v_scale, int num_pages, const int32_t* block_table,
+                            const float* k_scale, const float* v_scale, const void* k_new, const void* v_new,
+                            int num_pages, const int32_t* block_table,
                             int max_pages_per_seq, const int32_t* seq_lens, const int32_t* cu_q, int total_q,
                             int qmax, int qcap, int batch, int max_seq_len, int page_size, int num_q_heads,
                             int num_kv_heads, int head_dim, float softmax_scale, void* workspace,
@@ -1099,6 +1154,8 @@ static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_
     if (num_pages < 1 || max_pages_per_seq < 1) return PA_ERR_SHAPE;
     if ((long long)max_seq_len > (long long)max_pages_per_seq * page_size) return PA_ERR_SHAPE;
     if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(q) || !aligned16(out)) return PA_ERR_SHAPE;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PA_ERR_NULL;
+    if (k_new != nullptr && (fp8 || !aligned16(k_new) || !aligned16(v_new))) return PA_ERR_SHAPE;
     const long long pool_rows = (long long)num_pages * num_kv_heads * page_size;
     if (pool_rows >= (1ll << 31)) return PA_ERR_SHAPE;
 
@@ -1134,6 +1191,10 @@ static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_
     prm.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
     prm.k_scale = k_scale;
     prm.v_scale = v_scale;
+    prm.k_new = static_cast<const __nv_bfloat16*>(k_new);
+    prm.v_new = static_cast<const __nv_bfloat16*>(v_new);
+    prm.k_pool_w = k_new != nullptr ? static_cast<__nv_bfloat16*>(const_cast<void*>(k_pool)) : nullptr;
+    prm.v_pool_w = k_new != nullptr ? static_cast<__nv_bfloat16*>(const_cast<void*>(v_pool)) : nullptr;
     prm.block_table = block_table;
     prm.seq_lens = seq_lens;
     prm.cu_q = cu_q;
@@ -1175,20 +1236,27 @@ static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_
         cfg.numAttrs = 1;
         return cudaLaunchKernelEx(&cfg, kernel, prm) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     };
+    const bool app = k_new != nullptr;
     if (head_dim == 128) {
         if (fp8)
-            rc = swap ? go(decode_kernel<128, true, true>, Cfg<128, true, true>::SMEM_BYTES, 7)
-                      : go(decode_kernel<128, true, false>, Cfg<128, true, false>::SMEM_BYTES, 5);
+            rc = swap ? go(decode_kernel<128, true, true, false>, Cfg<128, true, true>::SMEM_BYTES, 7)
+                      : go(decode_kernel<128, true, false, false>, Cfg<128, true, false>::SMEM_BYTES, 5);
+        else if (app)
+            rc = swap ? go(decode_kernel<128, false, true, true>, Cfg<128, false, true>::SMEM_BYTES, 11)
+                      : go(decode_kernel<128, false, false, true>, Cfg<128, false, false>::SMEM_BYTES, 12);
         else
-            rc = swap ? go(decode_kernel<128, false, true>, Cfg<128, false, true>::SMEM_BYTES, 8)
-                      : go(decode_kernel<128, false, false>, Cfg<128, false, false>::SMEM_BYTES, 0);
+            rc = swap ? go(decode_kernel<128, false, true, false>, Cfg<128, false, true>::SMEM_BYTES, 8)
+                      : go(decode_kernel<128, false, false, false>, Cfg<128, false, false>::SMEM_BYTES, 0);
     } else {
         if (fp8)
-            rc = swap ? go(decode_kernel<64, true, true>, Cfg<64, true, true>::SMEM_BYTES, 9)
-                      : go(decode_kernel<64, true, false>, Cfg<64, true, false>::SMEM_BYTES, 6);
+            rc = swap ? go(decode_kernel<64, true, true, false>, Cfg<64, true, true>::SMEM_BYTES, 9)
+                      : go(decode_kernel<64, true, false, false>, Cfg<64, true, false>::SMEM_BYTES, 6);
+        else if (app)
+            rc = swap ? go(decode_kernel<64, false, true, true>, Cfg<64, false, true>::SMEM_BYTES, 13)
+                      : go(decode_kernel<64, false, false, true>, Cfg<64, false, false>::SMEM_BYTES, 14);
         else
-            rc = swap ? go(decode_kernel<64, false, true>, Cfg<64, false, true>::SMEM_BYTES, 10)
-                      : go(decode_kernel<64, false, false>, Cfg<64, false, false>::SMEM_BYTES, 1);
+            rc = swap ? go(decode_kernel<64, false, true, false>, Cfg<64, false, true>::SMEM_BYTES, 10)
+                      : go(decode_kernel<64, false, false, false>, Cfg<64, false, false>::SMEM_BYTES, 1);
     }
     if (rc != PA_OK) return rc;
     // the merge of split segments, a programmatic dependent of the decode grid
@@ -1215,7 +1283,7 @@ int launch_decode(void* out, float* lse, const void* q, const void* k_pool, cons
                   const int32_t* cu_q, int total_q, int qmax, int qcap, int batch, int max_seq_len, int page_size,
                   int num_q_heads, int num_kv_heads, int head_dim, float softmax_scale, void* workspace,
                   size_t workspace_bytes, int32_t* status, void* stream) {
-    return launch_decode_kv(out, lse, q, k_pool, v_pool, nullptr, nullptr, num_pages, block_table,
+    return launch_decode_kv(out, lse, q, k_pool, v_pool, nullptr, nullptr, nullptr, nullptr, num_pages, block_table,
                             max_pages_per_seq, seq_lens, cu_q, total_q, qmax, qcap, batch, max_seq_len, page_size,
                             num_q_heads, num_kv_heads, head_dim, softmax_scale, workspace, workspace_bytes, status,
                             stream);
@@ -1231,10 +1299,10 @@ extern "C" int attn_decode_paged_fp8(void* out, float* lse, const void* q, const
                                      int head_dim, float softmax_scale, void* workspace, size_t workspace_bytes,
                                      int32_t* status, void* stream) {
     if (batch > 0 && (k_scale == nullptr || v_scale == nullptr)) return PA_ERR_NULL;
-    return dec::launch_decode_kv(out, lse, q, k_pool, v_pool, k_scale, v_scale, num_pages, block_table,
-                                 max_pages_per_seq, seq_lens, nullptr, batch, 1, 1, batch, max_seq_len, page_size,
-                                 num_q_heads, num_kv_heads, head_dim, softmax_scale, workspace, workspace_bytes,
-                                 status, stream);
+    return dec::launch_decode_kv(out, lse, q, k_pool, v_pool, k_scale, v_scale, nullptr, nullptr, num_pages,
+                                 block_table, max_pages_per_seq, seq_lens, nullptr, batch, 1, 1, batch, max_seq_len,
+                                 page_size, num_q_heads, num_kv_heads, head_dim, softmax_scale, workspace,
+                                 workspace_bytes, status, stream);
 }
 
 extern "C" int attn_decode_paged(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool,
@@ -1245,6 +1313,19 @@ extern "C" int attn_decode_paged(void* out, float* lse, const void* q, const voi
     return dec::launch_decode(out, lse, q, k_pool, v_pool, num_pages, block_table, max_pages_per_seq, seq_lens,
                               nullptr, batch, 1, 1, batch, max_seq_len, page_size, num_q_heads, num_kv_heads,
                               head_dim, softmax_scale, workspace, workspace_bytes, status, stream);
+}
+
+extern "C" int attn_decode_paged_append(void* out, float* lse, const void* q, void* k_pool, void* v_pool,
+                                        const void* k_new, const void* v_new, int num_pages,
+                                        const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
+                                        int batch, int max_seq_len, int page_size, int num_q_heads, int num_kv_heads,
+                                        int head_dim, float softmax_scale, void* workspace, size_t workspace_bytes,
+                                        int32_t* status, void* stream) {
+    if (batch > 0 && (k_new == nullptr || v_new == nullptr)) return PA_ERR_NULL;
+    return dec::launch_decode_kv(out, lse, q, k_pool, v_pool, nullptr, nullptr, k_new, v_new, num_pages, block_table,
+                                 max_pages_per_seq, seq_lens, nullptr, batch, 1, 1, batch, max_seq_len, page_size,
+                                 num_q_heads, num_kv_heads, head_dim, softmax_scale, workspace, workspace_bytes,
+                                 status, stream);
 }
 
 extern "C" int attn_decode_multiquery_paged(void* out, float* lse, const void* q, const void* k_pool,

@@ -248,13 +248,18 @@ def attn_decode_paged(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tenso
                       max_seq_len: Optional[int] = None, out: Optional[torch.Tensor] = None,
                       lse: Optional[torch.Tensor] = None, return_lse: bool = False,
                       workspace: Optional[Workspace] = None, status: Optional[torch.Tensor] = None,
+                      k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None,
                       stream=None):
     """Split-K paged decode, one query row per sequence.
 
     q [B][Hq][D] bf16; pools [P][Hkv][page_size][D] bf16; block_table
     [B][max_pages] int32; seq_lens [B] int32 (device).  ``max_seq_len`` is a
     host upper bound of seq_lens used only to size the launch (default: the
-    table's capacity).  Returns out (and lse if requested).
+    table's capacity).  With ``k_new``/``v_new`` ([B][Hkv][D] bf16: each
+    sequence's newest row, at position seq_lens[b] - 1) the rows are written
+    into their pool slots by the same kernel (attn_decode_paged_append)
+    instead of needing a kv_write_paged call first.  Returns out (and lse if
+    requested).
     """
     lib = _lib.load()
     _need(q, "q", torch.bfloat16, 3, host_ok=True)
@@ -283,11 +288,24 @@ def attn_decode_paged(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tenso
     need = int(lib.pa_decode_workspace_bytes(B, Hq, Hkv, D)) if B > 0 else 0
     if workspace is None:
         workspace = _cached_ws("decode", need, k_pool.device)
-    rc = lib.attn_decode_paged(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_pool), _ptr(v_pool), P, _ptr(block_table),
-                               block_table.shape[1], _ptr(seq_lens), B, int(max_seq_len), ps, Hq, Hkv, D,
-                               float(softmax_scale), workspace.ptr, workspace.nbytes, _ptr(status),
-                               _stream_handle(stream))
-    _lib.check(rc, "attn_decode_paged")
+    if (k_new is None) != (v_new is None):
+        raise ValueError("pass both k_new and v_new, or neither")
+    if k_new is not None:
+        _need(k_new, "k_new", torch.bfloat16, 3, host_ok=True)
+        _need(v_new, "v_new", torch.bfloat16, 3, host_ok=True)
+        if k_new.shape != (B, Hkv, D) or v_new.shape != k_new.shape:
+            raise ValueError("k_new / v_new must be [batch][Hkv][head_dim]")
+        rc = lib.attn_decode_paged_append(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_new),
+                                          _ptr(v_new), P, _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                          B, int(max_seq_len), ps, Hq, Hkv, D, float(softmax_scale), workspace.ptr,
+                                          workspace.nbytes, _ptr(status), _stream_handle(stream))
+        _lib.check(rc, "attn_decode_paged_append")
+    else:
+        rc = lib.attn_decode_paged(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_pool), _ptr(v_pool), P, _ptr(block_table),
+                                   block_table.shape[1], _ptr(seq_lens), B, int(max_seq_len), ps, Hq, Hkv, D,
+                                   float(softmax_scale), workspace.ptr, workspace.nbytes, _ptr(status),
+                                   _stream_handle(stream))
+        _lib.check(rc, "attn_decode_paged")
     return (out, lse) if return_lse else out
 
 

@@ -199,3 +199,53 @@ def test_pinned_host_arguments_match_device(cuda_device):
                                     max_seq_len=mq.max_seq_len, out=hout)
     torch.cuda.synchronize()
     assert torch.equal(hout.view(torch.int16), ref.cpu().view(torch.int16))
+
+
+@pytest.mark.parametrize("lens,hq,hkv,d,ps", [
+    ([1, 16, 17, 31, 32, 500], 28, 4, 128, 16),   # group 7: swapped variant; page-boundary positions
+    ([1, 64, 65, 1000], 16, 2, 64, 64),           # group 8, head_dim 64, 64-token pages
+    ([5, 300, 4097], 32, 2, 128, 16),             # group 16: unswapped
+    ([3, 129, 2048], 64, 2, 128, 32),             # group 32: two row blocks, one writer per key block
+])
+def test_append_matches_writeback_then_decode(cuda_device, lens, hq, hkv, d, ps):
+    """attn_decode_paged_append = kv_write_paged + attn_decode_paged, bit for
+    bit (output, lse and the pools), and matches the oracle."""
+    pa = _pa()
+    dev = cuda_device
+    case = workloads.make_paged_case("append", lens, [1] * len(lens), hq, hkv, d, page_size=ps, seed=91,
+                                     prewritten=False, device=dev)
+    k2, v2 = case.k_pool.clone(), case.v_pool.clone()
+    ones = torch.arange(case.batch + 1, dtype=torch.int32, device=dev)
+    pa.kv_write_paged(case.k_pool, case.v_pool, case.k_new, case.v_new, ones, case.seq_lens, case.block_table)
+    out1, lse1 = pa.attn_decode_paged(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
+                                      case.softmax_scale, max_seq_len=case.max_seq_len, return_lse=True)
+    status = pa.new_status(dev)
+    out2, lse2 = pa.attn_decode_paged(case.q, k2, v2, case.block_table, case.seq_lens, case.softmax_scale,
+                                      max_seq_len=case.max_seq_len, return_lse=True, status=status,
+                                      k_new=case.k_new, v_new=case.v_new)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+    assert torch.equal(k2.view(torch.int16), case.k_pool.view(torch.int16))
+    assert torch.equal(v2.view(torch.int16), case.v_pool.view(torch.int16))
+    ref_out, ref_lse = oracle.paged_attention(**oracle_args(case))
+    assert_attention_close(out2, ref_out, lse2, ref_lse, what="append")
+
+
+def test_append_with_pinned_host_rows(cuda_device):
+    """The appended rows (and q / out) may be pinned host tensors."""
+    pa = _pa()
+    dev = cuda_device
+    case = workloads.make_paged_case("append_host", [40, 7, 900], [1, 1, 1], 28, 4, 128, seed=92,
+                                     prewritten=False, device=dev)
+    k2, v2 = case.k_pool.clone(), case.v_pool.clone()
+    ref = pa.attn_decode_paged(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
+                               case.softmax_scale, max_seq_len=case.max_seq_len, k_new=case.k_new, v_new=case.v_new)
+    hout = torch.empty(case.q.shape, dtype=torch.bfloat16).pin_memory()
+    pa.attn_decode_paged(case.q.cpu().pin_memory(), k2, v2, case.block_table, case.seq_lens, case.softmax_scale,
+                         max_seq_len=case.max_seq_len, out=hout, k_new=case.k_new.cpu().pin_memory(),
+                         v_new=case.v_new.cpu().pin_memory())
+    torch.cuda.synchronize()
+    assert torch.equal(hout.view(torch.int16), ref.cpu().view(torch.int16))
+    assert torch.equal(k2.view(torch.int16), case.k_pool.view(torch.int16))
