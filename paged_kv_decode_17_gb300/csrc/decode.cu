@@ -1017,11 +1017,14 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
 //     lse = log sum_c exp(lse_c),   o = sum_c exp(lse_c - lse) o_c
 // over the chunks c0 .. c1 of a segment, in chunk order.  Block (segment,
 // row block), one thread per (row, 4 dimensions); each thread loads its
-// row's partials eight chunks at a time and merges them with a running max.  Launched right after the decode
-// kernel as its programmatic dependent, it waits for that grid to finish.
+// row's partials eight chunks at a time and merges them with a running max.
+// Launched right after the decode kernel as its programmatic dependent: the
+// row geometry (from seq_lens / cu_q, which the decode does not write) is
+// worked out while the decode finishes, then it waits for that grid, and
+// lets the next kernel of the stream (the next step's decode, which reads
+// only its unwritten inputs before its own wait) start its plan.
 template <int D>
 __global__ void __launch_bounds__(RB * D / 4) merge_kernel(const Params p) {
-    pdl_wait();
     const int sid = blockIdx.x;
     const int per_b = p.Hkv * p.SBmax;
     const int b = sid / per_b;
@@ -1036,6 +1039,8 @@ __global__ void __launch_bounds__(RB * D / 4) merge_kernel(const Params p) {
     const int row_sb = sb * s.sh.RSB;
     const int rows_sb = min(s.sh.RSB, s.sh.qlen * p.group - row_sb);
     if (rr >= min(s.sh.R, rows_sb - r * s.sh.R)) return;
+    pdl_wait();
+    pdl_launch_dependents();
     const int start = p.seg_base[b] + (g * s.sh.SB + sb) * s.n;
     const Split sp(p.seg_base[p.batch], p.G);
     const int c0 = sp.chunk_of(start), c1 = sp.chunk_of(start + s.n - 1);
