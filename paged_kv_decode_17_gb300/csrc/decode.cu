@@ -369,6 +369,18 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     return y;
 }
 
+// How the units [0, T) of a launch are cut into chunks, one per CTA of a grid
+// of G; the decode and the merge kernel derive it from the same T and G.
+// Chunk c owns workspace slots c + (segment index).  (Cutting the last part
+// into small chunks that idle CTAs take from a counter was measured: the
+// CTAs' finishing spread is about 10 %, and the extra partials cost the merge
+// more than the balance gained.)
+struct Split {
+    int T, S;
+    __device__ __forceinline__ Split(int T_, int G) : T(T_), S(max(MIN_CHUNK, (T_ + G - 1) / G)) {}
+    __device__ __forceinline__ int chunk_of(int u) const { return u / S; }
+};
+
 // Swapped-operand variant (SWAP, for at most 8 query rows per segment, e.g.
 // decode with a GQA group of up to 8): the scores are computed transposed,
 // S^T = K Q^T with the 16 keys of a unit as the mma's M and the 8 rows as its
@@ -384,18 +396,10 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 // (lane & 3) * 2 + j of k-step kk reads dimension (lane & 3) * D/4 + 4 kk + j,
 // and k-index 8 + (lane & 3) * 2 + j reads that + 2, so each lane's K bytes
 // and Q values are one contiguous run of D/4 dimensions.
-// How the units [0, T) of a launch are cut into chunks, one per CTA of a grid
-// of G; the decode and the merge kernel derive it from the same T and G.
-// Chunk c owns workspace slots c + (segment index).  (Cutting the last part
-// into small chunks that idle CTAs take from a counter was measured: the
-// CTAs' finishing spread is about 10 %, and the extra partials cost the merge
-// more than the balance gained.)
-struct Split {
-    int T, S;
-    __device__ __forceinline__ Split(int T_, int G) : T(T_), S(max(MIN_CHUNK, (T_ + G - 1) / G)) {}
-    __device__ __forceinline__ int chunk_of(int u) const { return u / S; }
-};
-
+//
+// APPEND (bf16 pools): the query tokens' own K/V rows are not in the pool yet;
+// the unit holding them stages them from k_new / v_new, and one warp per
+// (sequence, KV head) writes them into their pool slots after using them.
 template <int D, bool FP8, bool SWAP, bool APPEND>
 __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
     decode_kernel(const Params p) {
