@@ -73,6 +73,26 @@ def test_decode_host_validation(lib, over, code):
     assert lib.attn_decode_paged(*_decode_args(**over)) == code
 
 
+def _append_args(k_new=1 << 20, v_new=1 << 20, **over):
+    a = _decode_args(**over)
+    return a[:5] + [k_new, v_new] + a[5:]
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(k_new=None), -1),           # the new rows are required
+    (dict(v_new=None), -1),
+    (dict(k_new=(1 << 20) + 8), -2),  # 16-byte alignment
+    (dict(hq=3), -2),
+    (dict(q=None), -1),
+])
+def test_append_host_validation(lib, kw, code):
+    assert lib.attn_decode_paged_append(*_append_args(**kw)) == code
+
+
+def test_append_empty_batch_is_a_noop(lib):
+    assert lib.attn_decode_paged_append(*_append_args(k_new=None, v_new=None, batch=0, q=None, out=None)) == 0
+
+
 def test_decode_empty_batch_is_a_noop(lib):
     assert lib.attn_decode_paged(*_decode_args(batch=0, q=None, out=None)) == 0
 
