@@ -612,14 +612,14 @@ def measure_multiquery(pa, steps, warmup, peaks, q_len=4):
     for _ in range(warmup):
         attn()
     torch.cuda.synchronize()
-    ev = _events(stream, 2 * steps)
-    for i in range(steps):
-        ev[2 * i].record(stream)
+    # K calls back to back, as the decode step: average duration over the timed region
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
         attn()
-        ev[2 * i + 1].record(stream)
+    e1.record(stream)
     torch.cuda.synchronize()
-    ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(steps)]
-    t = statistics.mean(ms)
+    t = e0.elapsed_time(e1) / steps
     kv = roofline.decode_kv_bytes(case.seq_lens_host, case.num_kv_heads, D)
     gbs = kv / (t * 1e-3) / 1e9
     res = {"workload": "qwen7b_multiquery: batch 32 x 8192-token contexts, %d query rows per sequence (causal "

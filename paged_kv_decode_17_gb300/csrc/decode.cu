@@ -362,6 +362,30 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// FP8 variant: in the unit holding a sequence's last key (fewer than 16 valid
+// keys), clear the staged value codes of the keys past the end: their slots
+// may hold any code, NaN included, and 0 * NaN = NaN.  The transposed value
+// block is D rows of 16 key bytes; word w of a row holds keys 4w .. 4w + 3.
+// Other units are left alone (valid >= 16: nothing to clear).
+template <int D>
+__device__ __forceinline__ void clear_codes_past_end(uint32_t vb, int valid, int lane) {
+    if (valid >= UNIT) return;
+    for (int i = lane; i < D * 4; i += 32) {
+        const int w = i & 3;
+        uint32_t keep = 0u;
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            if (w * 4 + b < valid) keep |= 0xFFu << (8 * b);
+        if (keep != 0xFFFFFFFFu) {
+            const uint32_t addr = vb + (i >> 2) * 16 + w * 4;
+            uint32_t x;
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x) : "r"(addr));
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(x & keep) : "memory");
+        }
+    }
+    __syncwarp();
+}
+
 // 8x8 b16 transpose across the warp (lane holds row lane/4, columns 2 (lane%4) + {0,1})
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     uint32_t y;
@@ -697,11 +721,7 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
                 const uint32_t b1 = movmatrix_trans(FP8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
                 // O^T += V^T P^T, 16 value dimensions per mma
                 if constexpr (FP8) {
-                    const int valid = min(UNIT, cs.sh.len - tok0);
-                    uint32_t keep = 0u;
-#pragma unroll
-                    for (int b = 0; b < 4; ++b)
-                        if ((lane & 3) * 4 + b < valid) keep |= 0xFFu << (8 * b);
+                    clear_codes_past_end<D>(vb, cs.sh.len - tok0, lane);
 #pragma unroll
                     for (int n = 0; n < D / 16; ++n) {
                         uint32_t wl, wh;
@@ -709,8 +729,6 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
                         asm volatile("ld.shared.u32 %0, [%1];"
                                      : "=r"(wh)
                                      : "r"(vb + (n * 16 + 8 + qr) * 16 + (lane & 3) * 4));
-                        wl &= keep;
-                        wh &= keep;
                         const uint32_t a[4] = {e4m3x2_to_f16x2(wl), e4m3x2_to_f16x2(wh), e4m3x2_to_f16x2(wl >> 16),
                                                e4m3x2_to_f16x2(wh >> 16)};
                         mma_16816_f16(o[n], a, b0, b1);
@@ -829,18 +847,12 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
                     pa[2] = pack_f16x2(pr[1][0], pr[1][1]);
                     pa[3] = pack_f16x2(pr[1][2], pr[1][3]);
                     // O += P V: value row d of the transposed unit holds the 16 keys' codes;
-                    // this lane's keys (lane & 3) * 4 .. + 3 are one word.  Keys past the
-                    // sequence end may hold any code (0 * NaN = NaN), so they are cleared.
-                    const int valid = min(UNIT, cs.sh.len - tok0);
-                    uint32_t keep = 0u;
-#pragma unroll
-                    for (int b = 0; b < 4; ++b)
-                        if ((lane & 3) * 4 + b < valid) keep |= 0xFFu << (8 * b);
+                    // this lane's keys (lane & 3) * 4 .. + 3 are one word.
+                    clear_codes_past_end<D>(vb, cs.sh.len - tok0, lane);
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         uint32_t w;
                         asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(vb + (n * 8 + qr) * 16 + (lane & 3) * 4));
-                        w &= keep;
                         mma_16816_f16(o[n], pa, e4m3x2_to_f16x2(w), e4m3x2_to_f16x2(w >> 16));
                     }
                 } else {
