@@ -19,7 +19,9 @@
  *                                ("The Stack Below the Stack, Part 2",
  *                                section 2.2 Flash-Decoding, steps 1-3).
  *   attn_decode_paged_append     writeback of each sequence's newest row and
- *                                the decode, in one kernel.
+ *                                the decode, in one kernel (and
+ *                                attn_decode_multiquery_paged_append for
+ *                                a block of new rows).
  *   attn_decode_multiquery_paged the same for a short block (2-8) of query
  *                                rows per sequence, causal inside the block
  *                                (speculative-decode verification).
@@ -53,8 +55,8 @@
  * Memory: the K/V pools, block_table, the workspace and every argument of
  * attn_prefill_varlen_causal must be device memory.  The small per-step
  * arguments of the decode and writeback calls (q, out, lse, k_new, v_new,
- * seq_lens, cu_seqlens_q, cu_seqlens_new; also k_new and v_new of
- * attn_decode_paged_append) may instead be page-locked host
+ * seq_lens, cu_seqlens_q, cu_seqlens_new; also k_new and v_new of the
+ * *_append calls) may instead be page-locked host
  * memory (cudaHostAlloc / cudaHostRegister): the kernels read and write it
  * in place over the CPU-GPU link (NVLink-C2C on GB300), which for a decode
  * step's few hundred kilobytes costs less than staging copies on the copy
@@ -199,6 +201,24 @@ int attn_decode_multiquery_paged(void* out, float* lse, const void* q, const voi
                                  int max_seq_len, int page_size, int num_q_heads, int num_kv_heads,
                                  int head_dim, float softmax_scale, void* workspace,
                                  size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * attn_decode_multiquery_paged with the query tokens' own K/V rows written
+ * back by the same kernel, as attn_decode_paged_append does for one row:
+ * the result of kv_write_paged (cu_seqlens_new = cu_seqlens_q) followed by
+ * attn_decode_multiquery_paged, in one call.
+ *   k_new, v_new  bf16 [total_q][num_kv_heads][head_dim]: row cu_seqlens_q[b] + i
+ *                 is token seq_lens[b] - q_len + i of sequence b
+ * bf16 pools only.
+ */
+int attn_decode_multiquery_paged_append(void* out, float* lse, const void* q, void* k_pool, void* v_pool,
+                                        const void* k_new, const void* v_new, int num_pages,
+                                        const int32_t* block_table, int max_pages_per_seq,
+                                        const int32_t* cu_seqlens_q, const int32_t* seq_lens, int batch,
+                                        int total_q, int max_q_len, int max_seq_len, int page_size,
+                                        int num_q_heads, int num_kv_heads, int head_dim, float softmax_scale,
+                                        void* workspace, size_t workspace_bytes, int32_t* status,
+                                        void* stream);
 
 /*
  * Workspace bytes attn_prefill_varlen_causal needs (no initialisation, as

@@ -56,6 +56,15 @@ SIGNATURES = {
         c_int, c_int, c_int, c_int, c_float,  # page_size, Hq, Hkv, D, scale
         c_void_p, c_size_t, c_void_p, c_void_p,  # workspace, bytes, status, stream
     ]),
+    "attn_decode_multiquery_paged_append": (c_int, [
+        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,  # out, lse, q, k_pool, v_pool
+        c_void_p, c_void_p,  # k_new, v_new
+        c_int, c_void_p, c_int,  # num_pages, block_table, max_pages_per_seq
+        c_void_p, c_void_p,  # cu_seqlens_q, seq_lens
+        c_int, c_int, c_int, c_int,  # batch, total_q, max_q_len, max_seq_len
+        c_int, c_int, c_int, c_int, c_float,  # page_size, Hq, Hkv, D, scale
+        c_void_p, c_size_t, c_void_p, c_void_p,  # workspace, bytes, status, stream
+    ]),
     "pa_prefill_workspace_bytes": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
     "attn_prefill_varlen_causal": (c_int, [
         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,  # out, lse, q, k_pool, v_pool

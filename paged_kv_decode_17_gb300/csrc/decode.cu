@@ -1349,6 +1349,22 @@ extern "C" int attn_decode_paged_append(void* out, float* lse, const void* q, vo
                                  status, stream);
 }
 
+extern "C" int attn_decode_multiquery_paged_append(void* out, float* lse, const void* q, void* k_pool, void* v_pool,
+                                                   const void* k_new, const void* v_new, int num_pages,
+                                                   const int32_t* block_table, int max_pages_per_seq,
+                                                   const int32_t* cu_seqlens_q, const int32_t* seq_lens, int batch,
+                                                   int total_q, int max_q_len, int max_seq_len, int page_size,
+                                                   int num_q_heads, int num_kv_heads, int head_dim,
+                                                   float softmax_scale, void* workspace, size_t workspace_bytes,
+                                                   int32_t* status, void* stream) {
+    if (max_q_len < 1 || max_q_len > kDecodeMaxQ) return PA_ERR_SHAPE;
+    if (batch > 0 && (cu_seqlens_q == nullptr || k_new == nullptr || v_new == nullptr)) return PA_ERR_NULL;
+    return dec::launch_decode_kv(out, lse, q, k_pool, v_pool, nullptr, nullptr, k_new, v_new, num_pages, block_table,
+                                 max_pages_per_seq, seq_lens, cu_seqlens_q, total_q, max_q_len, INT_MAX, batch,
+                                 max_seq_len, page_size, num_q_heads, num_kv_heads, head_dim, softmax_scale,
+                                 workspace, workspace_bytes, status, stream);
+}
+
 extern "C" int attn_decode_multiquery_paged(void* out, float* lse, const void* q, const void* k_pool,
                                             const void* v_pool, int num_pages, const int32_t* block_table,
                                             int max_pages_per_seq, const int32_t* cu_seqlens_q,

@@ -315,13 +315,18 @@ def attn_decode_multiquery_paged(q: torch.Tensor, k_pool: torch.Tensor, v_pool: 
                                  max_seq_len: Optional[int] = None, out: Optional[torch.Tensor] = None,
                                  lse: Optional[torch.Tensor] = None, return_lse: bool = False,
                                  workspace: Optional[Workspace] = None, status: Optional[torch.Tensor] = None,
+                                 k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None,
                                  stream=None):
     """Multi-query decode: 1..8 query rows per sequence, causal inside the block.
 
     q [total_q][Hq][D] bf16; cu_seqlens_q [B+1] int32; seq_lens [B] int32
     (total keys, the query rows' own K/V already written).  ``max_q_len``
     (1..8, default min(8, total_q)) is a host upper bound of the per-entry
-    row counts; it sizes the workspace and the launch.
+    row counts; it sizes the workspace and the launch.  With ``k_new`` /
+    ``v_new`` ([total_q][Hkv][D] bf16, the query tokens' own K/V rows) the
+    rows are written into their pool slots by the same kernel
+    (attn_decode_multiquery_paged_append) instead of needing kv_write_paged
+    first.
     """
     lib = _lib.load()
     _need(q, "q", torch.bfloat16, 3, host_ok=True)
@@ -354,12 +359,26 @@ def attn_decode_multiquery_paged(q: torch.Tensor, k_pool: torch.Tensor, v_pool: 
     need = int(lib.pa_decode_multiquery_workspace_bytes(B, int(max_q_len), Hq, Hkv, D)) if B > 0 else 0
     if workspace is None:
         workspace = _cached_ws("decode", need, k_pool.device)
-    rc = lib.attn_decode_multiquery_paged(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_pool), _ptr(v_pool), P,
-                                          _ptr(block_table), block_table.shape[1], _ptr(cu_seqlens_q),
-                                          _ptr(seq_lens), B, Tq, int(max_q_len), int(max_seq_len), ps, Hq, Hkv, D,
-                                          float(softmax_scale), workspace.ptr, workspace.nbytes, _ptr(status),
-                                          _stream_handle(stream))
-    _lib.check(rc, "attn_decode_multiquery_paged")
+    if (k_new is None) != (v_new is None):
+        raise ValueError("pass both k_new and v_new, or neither")
+    if k_new is not None:
+        _need(k_new, "k_new", torch.bfloat16, 3, host_ok=True)
+        _need(v_new, "v_new", torch.bfloat16, 3, host_ok=True)
+        if k_new.shape != (Tq, Hkv, D) or v_new.shape != k_new.shape:
+            raise ValueError("k_new / v_new must be [total_q][Hkv][head_dim]")
+        rc = lib.attn_decode_multiquery_paged_append(
+            _ptr(out), _ptr(lse), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_new), _ptr(v_new), P,
+            _ptr(block_table), block_table.shape[1], _ptr(cu_seqlens_q), _ptr(seq_lens), B, Tq, int(max_q_len),
+            int(max_seq_len), ps, Hq, Hkv, D, float(softmax_scale), workspace.ptr, workspace.nbytes, _ptr(status),
+            _stream_handle(stream))
+        _lib.check(rc, "attn_decode_multiquery_paged_append")
+    else:
+        rc = lib.attn_decode_multiquery_paged(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_pool), _ptr(v_pool), P,
+                                              _ptr(block_table), block_table.shape[1], _ptr(cu_seqlens_q),
+                                              _ptr(seq_lens), B, Tq, int(max_q_len), int(max_seq_len), ps, Hq, Hkv,
+                                              D, float(softmax_scale), workspace.ptr, workspace.nbytes, _ptr(status),
+                                              _stream_handle(stream))
+        _lib.check(rc, "attn_decode_multiquery_paged")
     return (out, lse) if return_lse else out
 
 

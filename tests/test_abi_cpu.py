@@ -89,6 +89,24 @@ def test_append_host_validation(lib, kw, code):
     assert lib.attn_decode_paged_append(*_append_args(**kw)) == code
 
 
+def test_multiquery_append_host_validation(lib):
+    f = lib.attn_decode_multiquery_paged_append
+    P = 1 << 20
+    # out, lse, q, k, v, k_new, v_new, num_pages, bt, maxp, cu_q, lens, batch, total_q, max_q_len, max_seq_len,
+    # ps, hq, hkv, d, scale, ws, wsb, status, stream
+    args = [P, None, P, P, P, P, P, 16, P, 8, P, P, 2, 4, 2, 100, 16, 4, 2, 64, 0.125, None, 0, None, None]
+    for i, code in ((5, -1), (6, -1), (10, -1)):  # k_new, v_new, cu_seqlens_q missing
+        bad = list(args)
+        bad[i] = None
+        assert f(*bad) == code
+    bad = list(args)
+    bad[14] = 9  # more than 8 query rows
+    assert f(*bad) == -2
+    bad = list(args)
+    bad[17] = 3  # Hq not a multiple of Hkv
+    assert f(*bad) == -2
+
+
 def test_append_empty_batch_is_a_noop(lib):
     assert lib.attn_decode_paged_append(*_append_args(k_new=None, v_new=None, batch=0, q=None, out=None)) == 0
 

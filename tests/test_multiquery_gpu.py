@@ -169,3 +169,35 @@ def test_qwen7b_multiquery_full_size_sampled(cuda_device):
     ref_out, ref_lse = oracle.paged_attention(**args, heads=heads)
     assert_attention_close(out[rows][:, heads], ref_out[:, heads], lse[rows][:, heads], ref_lse[:, heads],
                            what="qwen7b_multiquery sampled")
+
+
+@pytest.mark.parametrize("lens,qlens,hq,hkv,d,ps", [
+    ([900, 2, 37, 18], [2, 2, 3, 3], 28, 4, 128, 16),      # 21 rows: two row blocks; new rows 15-17 span two units
+    ([16, 300, 65], [8, 4, 1], 32, 4, 64, 16),             # 64 rows: four row blocks; head_dim 64
+    ([40, 1000], [4, 2], 16, 8, 128, 32),                  # group 2 x 4 rows = 8: swapped variant, 32-token pages
+])
+def test_multiquery_append_matches_writeback_then_decode(cuda_device, lens, qlens, hq, hkv, d, ps):
+    """attn_decode_multiquery_paged_append = kv_write_paged (cu_seqlens_new =
+    cu_seqlens_q) + attn_decode_multiquery_paged, bit for bit (output, lse and
+    the pools), and matches the oracle."""
+    pa = _pa()
+    dev = cuda_device
+    case = workloads.make_paged_case("mq_append", lens, qlens, hq, hkv, d, page_size=ps, seed=93,
+                                     prewritten=False, device=dev)
+    k2, v2 = case.k_pool.clone(), case.v_pool.clone()
+    pa.kv_write_paged(case.k_pool, case.v_pool, case.k_new, case.v_new, case.cu_seqlens_q, case.seq_lens,
+                      case.block_table)
+    out1, lse1 = _mq(case, dev)
+    status = pa.new_status(dev)
+    out2, lse2 = pa.attn_decode_multiquery_paged(case.q, k2, v2, case.block_table, case.cu_seqlens_q, case.seq_lens,
+                                                 case.softmax_scale, max_q_len=max(qlens),
+                                                 max_seq_len=case.max_seq_len, return_lse=True, status=status,
+                                                 k_new=case.k_new, v_new=case.v_new)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+    assert torch.equal(k2.view(torch.int16), case.k_pool.view(torch.int16))
+    assert torch.equal(v2.view(torch.int16), case.v_pool.view(torch.int16))
+    ref_out, ref_lse = oracle.paged_attention(**oracle_args(case))
+    assert_attention_close(out2, ref_out, lse2, ref_lse, what="mq_append")
