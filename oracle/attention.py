@@ -17,7 +17,7 @@ Sources
   through a per-sequence table of page ids; new K/V rows are written into
   their pages eagerly.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 
 * pools are ``[num_pages][Hkv][page_size][D]``; query head ``h`` reads KV
   head ``h // (Hq // Hkv)``;

@@ -21,7 +21,7 @@ Sources
 * attention then runs on the dequantised K/V exactly as in
   ``attention.paged_attention`` (float64, whole score row).
 
-Readings (also listed in the design doc): one float32 scale per KV head for K and
+Readings where the pages are silent: one float32 scale per KV head for K and
 one for V (a page is filled one token at a time by the eager writeback, so a
 per-page scale would be fixed by its first token), and V stored transposed
 inside each page block, ``[D][page_size]`` per (page, KV head), so that the

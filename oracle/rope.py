@@ -19,7 +19,7 @@ Sources
   * weight``, applied per head before the rotation (as in models with
   per-head Q/K norms).
 
-Readings where the pages are silent (each also listed in the design doc): the
+Readings where the pages are silent: the
 rotate-half pairing, the frequency base as a parameter, normalisation before
 rotation, and the row position ``seq_len - n_new + i`` (the slot the row is
 written to) as the rotation position.
