@@ -231,8 +231,8 @@ def _compact_numpy(case, seqs):
                 num_kv_heads=case.num_kv_heads, page_size=ps, scale=case.softmax_scale)
 
 
-def oracle_decode_rate(case, budget_s=12.0, max_seqs=None):
-    """Time the fp64 CPU oracle on whole sequences of `case` until `budget_s`
+def oracle_decode_rate(case, time_limit_s=12.0, max_seqs=None):
+    """Time the fp64 CPU oracle on whole sequences of `case` until `time_limit_s`
     of CPU work; returns (GB/s of KV, seconds, sequences done)."""
     import oracle  # test infrastructure: only the CPU-baseline legs use it
     done, t_total, nbytes = 0, 0.0, 0
@@ -244,12 +244,12 @@ def oracle_decode_rate(case, budget_s=12.0, max_seqs=None):
         t_total += time.perf_counter() - t0
         nbytes += roofline.decode_kv_bytes([case.seq_lens_host[b]], case.num_kv_heads, case.head_dim)
         done += 1
-        if t_total >= budget_s:
+        if t_total >= time_limit_s:
             break
     return nbytes / t_total / 1e9, t_total, done
 
 
-def cpu_baseline_subprocess(budget_s=12.0):
+def cpu_baseline_subprocess(time_limit_s=12.0):
     """Run the oracle in a fresh single-threaded process (BLAS pinned to one
     thread, so `cores` is exact)."""
     env = dict(os.environ)
@@ -258,7 +258,7 @@ def cpu_baseline_subprocess(budget_s=12.0):
     env["CUDA_VISIBLE_DEVICES"] = ""
     code = ("import sys, json; sys.path.insert(0, %r); import bench, workloads; "
             "c = workloads.qwen7b_decode(device='cpu'); "
-            "r = bench.oracle_decode_rate(c, %r); print('CPU_BASELINE', json.dumps(r))" % (ROOT, budget_s))
+            "r = bench.oracle_decode_rate(c, %r); print('CPU_BASELINE', json.dumps(r))" % (ROOT, time_limit_s))
     try:
         out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
         for line in out.stdout.splitlines():

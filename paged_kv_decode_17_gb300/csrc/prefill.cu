@@ -97,7 +97,7 @@ struct Cfg {
     static constexpr int TM_O0 = 2 * BN;
     static constexpr int TM_USED = 2 * BN + 2 * D;
     static constexpr int TM_COLS = TM_USED <= 256 ? 256 : 512;
-    static_assert(TM_USED <= 512, "TMEM budget");
+    static_assert(TM_USED <= 512, "more than the 512 TMEM columns");
     static constexpr uint32_t IDESC_S = tc::idesc_bf16(BM, BN, 0, 0);   // Q K-major, K K-major
     static constexpr uint32_t IDESC_PV = tc::idesc_bf16(BM, D, 0, 1);   // P K-major, V MN-major
 };
