@@ -593,6 +593,58 @@ def measure_mixed(pa, steps, warmup, peaks):
     return res
 
 
+def measure_ragged_decode(pa, steps, warmup, peaks):
+    """Ragged Llama-3-8B-shaped decode step: batch 64, contexts uniform on
+    [1, 32768] (seeded), Hq=32, Hkv=8, D=128, 16-token pages scattered over a
+    131,072-page pool; the same call as the headline step (split-K decode with
+    each sequence's newest row written back in the kernel).  About 4.3 GB of
+    KV per step, far above L2, so no flush; K calls back to back, then K calls
+    with an event on each side."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = workloads.llama8b_ragged_decode(device=dev)
+    stream = torch.cuda.current_stream()
+    B, Hq, D = case.q.shape
+    ws = pa.Workspace(pa.decode_workspace_bytes(B, Hq, case.num_kv_heads, D), dev)
+    out = torch.empty_like(case.q)
+
+    def step():
+        pa.attn_decode_paged(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
+                             case.softmax_scale, max_seq_len=case.max_seq_len, out=out, workspace=ws,
+                             k_new=case.k_new, v_new=case.v_new)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / steps
+    ev = _events(stream, 2 * steps)
+    for i in range(steps):
+        ev[2 * i].record(stream)
+        step()
+        ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    t_iso = statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(steps))
+    kv = roofline.decode_kv_bytes(case.seq_lens_host, case.num_kv_heads, D)
+    gbs = kv / (t * 1e-3) / 1e9
+    res = {"workload": "llama8b_ragged_decode: batch 64, contexts uniform on [1, 32768] (seeded), Hq=32, Hkv=8, "
+                       "head_dim 128, 16-token pages in a 131072-page pool; step = split-K decode with the newest "
+                       "row of each sequence written back in the same kernel (attn_decode_paged_append)",
+           "tokens_in_context": int(sum(case.seq_lens_host)), "ms": t, "ms_isolated": t_iso, "kv_bytes": kv,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / peaks["hbm_gbs"], "frac_isolated": kv / (t_iso * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                        "peak_source": peaks["source"]},
+           "tokens_per_s": B / (t * 1e-3), "steps": steps, "launches_per_step": 2,
+           "l2": "inputs larger than L2 (about 4.3 GB of KV), no flush"}
+    del case
+    torch.cuda.empty_cache()
+    return res
+
+
 def measure_multiquery(pa, steps, warmup, peaks, q_len=4):
     """Multi-query decode (speculative-decode verification): the qwen7b_decode
     shape with q_len query rows per sequence, causal inside the block; the
@@ -642,7 +694,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-only", action="store_true", help="skip the prefill and mixed-step measurements")
-    ap.add_argument("--only", choices=["prefill", "mixed", "multiquery", "rope_writeback", "fp8_decode"],
+    ap.add_argument("--only", choices=["prefill", "mixed", "multiquery", "rope_writeback", "fp8_decode",
+                                       "llama8b_ragged"],
                     default=None,
                     help="run just this extra measurement (for profiling); prints its object only")
     args = ap.parse_args(argv)
@@ -659,7 +712,8 @@ def main(argv=None):
     dev = torch.device("cuda", torch.cuda.current_device())
     if args.only is not None:
         fn = {"prefill": measure_prefill, "mixed": measure_mixed, "multiquery": measure_multiquery,
-              "rope_writeback": measure_rope_writeback, "fp8_decode": measure_fp8_decode}[args.only]
+              "rope_writeback": measure_rope_writeback, "fp8_decode": measure_fp8_decode,
+              "llama8b_ragged": measure_ragged_decode}[args.only]
         res = fn(pa, args.steps, args.warmup, peaks)
         if rank == 0:
             print(json.dumps({"only": args.only, args.only: res}), flush=True)
@@ -713,12 +767,13 @@ def main(argv=None):
     }
     if not args.decode_only:
         psteps = max(3, min(args.steps, 20))
+        line["llama8b_ragged"] = measure_ragged_decode(pa, psteps, 3, peaks)
         line["prefill"] = measure_prefill(pa, psteps, 3, peaks)
         line["mixed"] = measure_mixed(pa, psteps, 3, peaks)
         line["multiquery"] = measure_multiquery(pa, psteps, 3, peaks)
         line["rope_writeback"] = measure_rope_writeback(pa, psteps, 3, peaks)
         line["fp8_decode"] = measure_fp8_decode(pa, psteps, 3, peaks)
-        line["gpu_launches"] += world * psteps * (5 + 4 + 2 + 1 + 2)
+        line["gpu_launches"] += world * psteps * (2 * 2 + 5 + 4 + 2 + 1 + 2)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_subprocess()
     if rank == 0:

@@ -86,7 +86,9 @@
  * Errors: a negative return value is a pa_status detected on the host
  * before anything is launched (nothing was enqueued).  Errors found on the
  * device (a block_table entry outside [0, num_pages), an inconsistent
- * length, a wait that timed out) are written, first one wins, to the
+ * length, or -- in the prefill kernel of attn_prefill_varlen_causal, the only
+ * kernel that waits on mbarriers -- a wait on a TMA copy or a tensor-core
+ * operation that ran past its time limit) are written, first one wins, to the
  * optional device word `status` (int32, caller-zeroed); the kernels skip
  * the offending access instead of faulting, and the affected outputs are
  * unspecified.  Read `status` after synchronising the stream.
@@ -107,7 +109,7 @@ typedef enum {
     PA_ERR_SHAPE = -2,      /* unsupported or inconsistent sizes                   */
     PA_ERR_WORKSPACE = -3,  /* workspace missing or smaller than required          */
     PA_ERR_CUDA = -4,       /* a CUDA runtime/driver call or the launch failed     */
-    PA_ERR_TIMEOUT = -5,    /* device: a wait on an asynchronous copy timed out    */
+    PA_ERR_TIMEOUT = -5,    /* device: a prefill-kernel wait ran past its limit    */
     PA_ERR_BAD_PAGE = -6,   /* device: block_table entry outside [0, num_pages)    */
     PA_ERR_BAD_LEN = -7,    /* device: seq_len / row count inconsistent            */
     PA_ERR_ARCH = -8,       /* the current device is not an sm_103 GPU             */
@@ -350,10 +352,16 @@ int attn_decode_paged_fp8(void* out, float* lse, const void* q, const void* k_po
  * where group = num_q_heads / num_kv_heads and rows = 16 for group <= 16,
  * 32 for group <= 32 and 64 above.
  *
- * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls on a device share the one array and
+ * No call allocates: no cudaMalloc, cudaFree or allocating library call.
+ * The first call on each device (and the first after the device's context
+ * was destroyed and created again, e.g. by cudaDeviceReset) looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current.
+ * Because CUDA loads modules lazily, that first lookup (or the first launch of
+ * any kernel of this library) is also where the driver loads the library's
+ * device code and reserves the 8 MiB array, i.e. where the driver itself
+ * allocates.  Make that first call -- or a warm-up call -- where driver
+ * allocation is allowed and before any stream capture; later calls touch no
+ * allocator.  All calls on a device share the one array and
  * it keeps the last call's contents:
  * calls whose execution may overlap on the GPU (different streams, or
  * concurrent graph branches) race on it and give wrong results.

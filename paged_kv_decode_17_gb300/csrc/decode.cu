@@ -47,6 +47,7 @@
 //   merged set the length of the whole launch.)
 #include "pa_common.cuh"
 #include "pa_host.h"
+#include "pa_trace.h"
 
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -112,6 +113,7 @@ struct Params {
     int Hq, Hkv, group;
     int SBmax;    // segments per (sequence, KV head) at q_len = qmax
     int RS;       // rows per workspace slot (16 x the largest row-block count)
+    int min_chunk;  // smallest chunk, in units (MIN_CHUNK unless overridden for tests)
     float scale_log2;
 };
 
@@ -401,7 +403,7 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 // more than the balance gained.)
 struct Split {
     int T, S;
-    __device__ __forceinline__ Split(int T_, int G) : T(T_), S(max(MIN_CHUNK, (T_ + G - 1) / G)) {}
+    __device__ __forceinline__ Split(int T_, int G, int min_chunk) : T(T_), S(max(min_chunk, (T_ + G - 1) / G)) {}
     __device__ __forceinline__ int chunk_of(int u) const { return u / S; }
 };
 
@@ -424,9 +426,16 @@ struct Split {
 // APPEND (bf16 pools): the query tokens' own K/V rows are not in the pool yet;
 // the unit holding them stages them from k_new / v_new, and one warp per
 // (sequence, KV head) writes them into their pool slots after using them.
-template <int D, bool FP8, bool SWAP, bool APPEND>
-__global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
+//
+// SW selects the operand order: 0 = plain (query rows as M), 1 = swapped for
+// every segment, 2 = chosen per segment (swapped when the segment has at most
+// 8 rows), for a call that mixes one-row entries with longer query blocks
+// (the decode rows of a mixed serving step).
+template <int D, bool FP8, int SW, bool APPEND>
+__global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SW == 1>())
     decode_kernel(const Params p) {
+    constexpr bool SWAP = SW == 1;
+    static_assert(SW >= 0 && SW <= 2 && !(FP8 && SW == 2), "operand order");
     using C = Cfg<D, FP8, SWAP>;
     constexpr int DEPTH = C::DEPTH;
     constexpr int KSTEPS = D / 16;
@@ -460,7 +469,7 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
     }
     __syncthreads();
     // ---- split: CTA c owns the equal range [c S, (c + 1) S) of the units
-    const Split sp(s_plan[0], gridDim.x);
+    const Split sp(s_plan[0], gridDim.x, p.min_chunk);
     const int U0 = blockIdx.x * sp.S;  // grid * chunk < 2^31 is checked on the host
     const int U1 = min(sp.T, U0 + sp.S);
     const bool has_work = U0 < U1;
@@ -577,17 +586,19 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
         const int rows_sb = min(cs.sh.RSB, cs.sh.qlen * p.group - row_sb);
         const int my_rows = max(0, min(cs.sh.R, rows_sb - wrb * cs.sh.R));
         const int qlast = cs.sh.len - cs.sh.qlen;  // position of query token 0
+        // operand order of this piece (uniform over the CTA: every warp works on this segment)
+        const bool swp = SW == 2 ? cs.sh.qlen * p.group <= 8 : SWAP;
 
         // Q fragments of this warp's rows (rows >= my_rows are zero) and the
         // number of keys each of the lane's two rows may see
         uint32_t qa[KSTEPS][4];
         int lim0 = cs.sh.len, lim1 = cs.sh.len;
         // this lane's two softmax rows
-        const int rA = SWAP ? (lane & 3) * 2 : qr, rB = SWAP ? rA + 1 : qr + 8;
+        const int rA = swp ? (lane & 3) * 2 : qr, rB = swp ? rA + 1 : qr + 8;
         {
             const size_t qrow = q_row(p, cs.b);
             // rows whose q this lane loads: qr and qr + 8 (SWAP: only qr, as a column of Q^T)
-            const bool r0ok = qr < my_rows, r8ok = !SWAP && qr + 8 < my_rows;
+            const bool r0ok = qr < my_rows, r8ok = !swp && qr + 8 < my_rows;
             const int f0 = row_sb + wrb * cs.sh.R + qr, f8 = f0 + 8;
             const int i0 = f0 / p.group, i8 = f8 / p.group;
             const int h0 = cs.g * p.group + (f0 - i0 * p.group), h8 = cs.g * p.group + (f8 - i8 * p.group);
@@ -612,7 +623,7 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
                     const __nv_bfloat162 f = *reinterpret_cast<__nv_bfloat162*>(&v8.y);
                     qa[kk][0] = pack_f16x2(__low2float(a), __high2float(a));
                     qa[kk][SWAP ? 1 : 2] = pack_f16x2(__low2float(b), __high2float(b));
-                    if constexpr (!SWAP) {
+                    if constexpr (!SWAP) {  // (no per-segment order for FP8)
                         qa[kk][1] = pack_f16x2(__low2float(e), __high2float(e));
                         qa[kk][3] = pack_f16x2(__low2float(f), __high2float(f));
                     }
@@ -621,7 +632,7 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; ++kk) {
                     const int c = (kk * 16 + qc) >> 1;
-                    if constexpr (SWAP) {
+                    if (swp) {
                         qa[kk][0] = r0ok ? __ldg(q0 + c) : 0u;
                         qa[kk][1] = r0ok ? __ldg(q0 + c + 4) : 0u;
                     } else {
@@ -648,7 +659,7 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
             const int phys = s_phys[warp][st];
             uint8_t* sk = my_stages + st * C::STAGE_BYTES;
             uint8_t* sv = sk + C::UNIT_BYTES;
-            if (SWAP && phys >= 0) {
+            if (swp && phys >= 0) {
                 const int tok0 = ((u - cs.start) >> cs.sh.nrb_shift) * UNIT;
                 const int vis0 = lim0 - tok0, vis1 = lim1 - tok0;  // keys of this unit rows rA / rB see
                 const uint32_t kb = smem_u32(sk), vb = smem_u32(sv);
@@ -744,7 +755,7 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
                         mma_16816(o[n], a, b0, b1);
                     }
                 }
-            } else if (!SWAP && phys >= 0) {
+            } else if (!swp && phys >= 0) {
                 const int tok0 = ((u - cs.start) >> cs.sh.nrb_shift) * UNIT;
                 const int vis0 = lim0 - tok0, vis1 = lim1 - tok0;  // keys of this unit each row sees
                 const uint32_t kb = smem_u32(sk), vb = smem_u32(sv);
@@ -911,12 +922,20 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
 
         // ---- merge the states of the warps that hold the same row block (fixed order)
         // (a row's partial sums are spread over the lanes that hold its other keys)
+        if (swp) {
 #pragma unroll
-        for (int o_ = SWAP ? 4 : 1; o_ < (SWAP ? 32 : 4); o_ <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, o_);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, o_);
+            for (int o_ = 4; o_ < 32; o_ <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, o_);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, o_);
+            }
+        } else {
+#pragma unroll
+            for (int o_ = 1; o_ < 4; o_ <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, o_);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, o_);
+            }
         }
-        const bool row_owner = SWAP ? (lane >> 2) == 0 : (lane & 3) == 0;
+        const bool row_owner = swp ? (lane >> 2) == 0 : (lane & 3) == 0;
         if (row_owner) {
             s_m[warp][rA] = m0;
             s_l[warp][rA] = l0;
@@ -956,7 +975,7 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
             // warps add their rescaled O into one buffer in a fixed order
 #pragma unroll 1
             for (int w = wfirst; w < W; w += nrb) {
-                if (SWAP && warp == w) {
+                if (swp && warp == w) {
                     // O^T fragment: (d = 16 n + qr (+8), rows rA / rB)
 #pragma unroll
                     for (int n = 0; n < D / 16; ++n) {
@@ -974,7 +993,7 @@ __global__ void __launch_bounds__(W * 32, ctas_per_sm<FP8, SWAP>())
                             *pB = vB;
                         }
                     }
-                } else if (!SWAP && warp == w) {
+                } else if (!swp && warp == w) {
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         const int col = n * 8 + qc;
@@ -1058,7 +1077,7 @@ __global__ void __launch_bounds__(RB * D / 4) merge_kernel(const Params p) {
     pdl_wait();
     pdl_launch_dependents();
     const int start = p.seg_base[b] + (g * s.sh.SB + sb) * s.n;
-    const Split sp(p.seg_base[p.batch], p.G);
+    const Split sp(p.seg_base[p.batch], p.G, p.min_chunk);
     const int c0 = sp.chunk_of(start), c1 = sp.chunk_of(start + s.n - 1);
     if (c0 == c1) return;  // one chunk held the whole segment and stored its rows
     const int rw = r * RB + rr;
@@ -1158,13 +1177,15 @@ namespace dec {
 // cu_q[b] ..), q_len in (qmax, qcap] is reported as PA_ERR_BAD_LEN and
 // longer entries are left to the prefill kernel.
 // k_scale / v_scale non-null: the pools hold e4m3 codes (V transposed per page block).
+// per_segment: when not every segment fits the swapped-operand variant, choose the
+// operand order per segment (bf16, no append) instead of the plain order everywhere.
 static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool,
                             const float* k_scale, const float* v_scale, const void* k_new, const void* v_new,
                             int num_pages, const int32_t* block_table,
                             int max_pages_per_seq, const int32_t* seq_lens, const int32_t* cu_q, int total_q,
                             int qmax, int qcap, int batch, int max_seq_len, int page_size, int num_q_heads,
                             int num_kv_heads, int head_dim, float softmax_scale, void* workspace,
-                            size_t workspace_bytes, int32_t* status, void* stream) {
+                            size_t workspace_bytes, int32_t* status, void* stream, bool per_segment = false) {
     const bool fp8 = k_scale != nullptr;
     if (batch < 0 || max_seq_len < 0 || total_q < 0) return PA_ERR_SHAPE;
     if (qmax < 1 || qmax > kDecodeMaxQ || (cu_q == nullptr && qmax != 1)) return PA_ERR_SHAPE;
@@ -1189,14 +1210,17 @@ static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_
     const int nrb_max = bd.RS / RB;
     const long long segs = (long long)batch * num_kv_heads * bd.SBmax;
     const long long units_upper = segs * nrb_max * ((max_seq_len + UNIT - 1) / UNIT);
+    const int min_chunk = decode_min_chunk(MIN_CHUNK);
     // every unit index and grid * chunk must fit in int32
     if (segs * nrb_max * ((max_pages_per_seq * (long long)page_size + UNIT - 1) / UNIT) +
-            (long long)dev.sm_count * kMaxCtasPerSM * MIN_CHUNK >=
+            (long long)dev.sm_count * kMaxCtasPerSM * min_chunk >=
         (1ll << 31))
         return PA_ERR_SHAPE;
     const bool swap = group * qmax <= 8;  // at most 8 rows per segment: the swapped-operand variant
+    // some segments (the one-row entries) may fit it
+    const bool mixed_order = per_segment && !swap && group <= 8 && !fp8 && k_new == nullptr;
     const int gmax = dev.sm_count * ((fp8 && swap) ? ctas_per_sm<true, true>() : ctas_per_sm<false, false>());
-    long long g = (units_upper + MIN_CHUNK - 1) / MIN_CHUNK;
+    long long g = (units_upper + min_chunk - 1) / min_chunk;
     if (g < 1) g = 1;
     const int grid = (int)(g < gmax ? g : gmax);
 
@@ -1224,6 +1248,7 @@ static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_
     prm.qcap = qcap;
     prm.SBmax = bd.SBmax;
     prm.RS = bd.RS;
+    prm.min_chunk = min_chunk;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     prm.seg_base = reinterpret_cast<int32_t*>(ws + wl.hdr);
     prm.G = grid;
@@ -1258,6 +1283,13 @@ static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_
         return cudaLaunchKernelEx(&cfg, kernel, prm) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     };
     const bool app = k_new != nullptr;
+    log_config("split-K decode: head_dim %d, %s, operand order %s, %s, q_len <= %d, grid %d CTAs x %d warps "
+               "(%d per SM), min chunk %d units of %d keys, merge grid %lld x %d",
+               head_dim, fp8 ? "fp8 e4m3 pools" : "bf16 pools",
+               swap ? "swapped (keys as M)" : (mixed_order ? "per segment" : "plain (query rows as M)"),
+               app ? "newest rows appended in-kernel" : "no append", qmax, grid, W,
+               (fp8 && swap) ? ctas_per_sm<true, true>() : ctas_per_sm<false, false>(), min_chunk, UNIT, segs,
+               nrb_max);
     if (head_dim == 128) {
         if (fp8)
             rc = swap ? go(decode_kernel<128, true, true, false>, Cfg<128, true, true>::SMEM_BYTES, 7)
@@ -1265,6 +1297,8 @@ static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_
         else if (app)
             rc = swap ? go(decode_kernel<128, false, true, true>, Cfg<128, false, true>::SMEM_BYTES, 11)
                       : go(decode_kernel<128, false, false, true>, Cfg<128, false, false>::SMEM_BYTES, 12);
+        else if (mixed_order)
+            rc = go(decode_kernel<128, false, 2, false>, Cfg<128, false, false>::SMEM_BYTES, 15);
         else
             rc = swap ? go(decode_kernel<128, false, true, false>, Cfg<128, false, true>::SMEM_BYTES, 8)
                       : go(decode_kernel<128, false, false, false>, Cfg<128, false, false>::SMEM_BYTES, 0);
@@ -1275,6 +1309,8 @@ static int launch_decode_kv(void* out, float* lse, const void* q, const void* k_
         else if (app)
             rc = swap ? go(decode_kernel<64, false, true, true>, Cfg<64, false, true>::SMEM_BYTES, 13)
                       : go(decode_kernel<64, false, false, true>, Cfg<64, false, false>::SMEM_BYTES, 14);
+        else if (mixed_order)
+            rc = go(decode_kernel<64, false, 2, false>, Cfg<64, false, false>::SMEM_BYTES, 16);
         else
             rc = swap ? go(decode_kernel<64, false, true, false>, Cfg<64, false, true>::SMEM_BYTES, 10)
                       : go(decode_kernel<64, false, false, false>, Cfg<64, false, false>::SMEM_BYTES, 1);
@@ -1303,11 +1339,11 @@ int launch_decode(void* out, float* lse, const void* q, const void* k_pool, cons
                   const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
                   const int32_t* cu_q, int total_q, int qmax, int qcap, int batch, int max_seq_len, int page_size,
                   int num_q_heads, int num_kv_heads, int head_dim, float softmax_scale, void* workspace,
-                  size_t workspace_bytes, int32_t* status, void* stream) {
+                  size_t workspace_bytes, int32_t* status, void* stream, bool per_segment) {
     return launch_decode_kv(out, lse, q, k_pool, v_pool, nullptr, nullptr, nullptr, nullptr, num_pages, block_table,
                             max_pages_per_seq, seq_lens, cu_q, total_q, qmax, qcap, batch, max_seq_len, page_size,
                             num_q_heads, num_kv_heads, head_dim, softmax_scale, workspace, workspace_bytes, status,
-                            stream);
+                            stream, per_segment);
 }
 
 }  // namespace dec
@@ -1319,6 +1355,7 @@ extern "C" int attn_decode_paged_fp8(void* out, float* lse, const void* q, const
                                      int batch, int max_seq_len, int page_size, int num_q_heads, int num_kv_heads,
                                      int head_dim, float softmax_scale, void* workspace, size_t workspace_bytes,
                                      int32_t* status, void* stream) {
+    NvtxRange nvtx_("attn_decode_paged_fp8");
     if (batch > 0 && (k_scale == nullptr || v_scale == nullptr)) return PA_ERR_NULL;
     return dec::launch_decode_kv(out, lse, q, k_pool, v_pool, k_scale, v_scale, nullptr, nullptr, num_pages,
                                  block_table, max_pages_per_seq, seq_lens, nullptr, batch, 1, 1, batch, max_seq_len,
@@ -1331,6 +1368,7 @@ extern "C" int attn_decode_paged(void* out, float* lse, const void* q, const voi
                                  const int32_t* seq_lens, int batch, int max_seq_len, int page_size, int num_q_heads,
                                  int num_kv_heads, int head_dim, float softmax_scale, void* workspace,
                                  size_t workspace_bytes, int32_t* status, void* stream) {
+    NvtxRange nvtx_("attn_decode_paged");
     return dec::launch_decode(out, lse, q, k_pool, v_pool, num_pages, block_table, max_pages_per_seq, seq_lens,
                               nullptr, batch, 1, 1, batch, max_seq_len, page_size, num_q_heads, num_kv_heads,
                               head_dim, softmax_scale, workspace, workspace_bytes, status, stream);
@@ -1342,6 +1380,7 @@ extern "C" int attn_decode_paged_append(void* out, float* lse, const void* q, vo
                                         int batch, int max_seq_len, int page_size, int num_q_heads, int num_kv_heads,
                                         int head_dim, float softmax_scale, void* workspace, size_t workspace_bytes,
                                         int32_t* status, void* stream) {
+    NvtxRange nvtx_("attn_decode_paged_append");
     if (batch > 0 && (k_new == nullptr || v_new == nullptr)) return PA_ERR_NULL;
     return dec::launch_decode_kv(out, lse, q, k_pool, v_pool, nullptr, nullptr, k_new, v_new, num_pages, block_table,
                                  max_pages_per_seq, seq_lens, nullptr, batch, 1, 1, batch, max_seq_len, page_size,
@@ -1357,6 +1396,7 @@ extern "C" int attn_decode_multiquery_paged_append(void* out, float* lse, const 
                                                    int num_q_heads, int num_kv_heads, int head_dim,
                                                    float softmax_scale, void* workspace, size_t workspace_bytes,
                                                    int32_t* status, void* stream) {
+    NvtxRange nvtx_("attn_decode_multiquery_paged_append");
     if (max_q_len < 1 || max_q_len > kDecodeMaxQ) return PA_ERR_SHAPE;
     if (batch > 0 && (cu_seqlens_q == nullptr || k_new == nullptr || v_new == nullptr)) return PA_ERR_NULL;
     return dec::launch_decode_kv(out, lse, q, k_pool, v_pool, nullptr, nullptr, k_new, v_new, num_pages, block_table,
@@ -1372,6 +1412,7 @@ extern "C" int attn_decode_multiquery_paged(void* out, float* lse, const void* q
                                             int max_seq_len, int page_size, int num_q_heads, int num_kv_heads,
                                             int head_dim, float softmax_scale, void* workspace,
                                             size_t workspace_bytes, int32_t* status, void* stream) {
+    NvtxRange nvtx_("attn_decode_multiquery_paged");
     if (max_q_len < 1 || max_q_len > kDecodeMaxQ) return PA_ERR_SHAPE;
     if (batch > 0 && cu_seqlens_q == nullptr) return PA_ERR_NULL;
     return dec::launch_decode(out, lse, q, k_pool, v_pool, num_pages, block_table, max_pages_per_seq, seq_lens,
@@ -1401,17 +1442,23 @@ static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 namespace {
 std::mutex g_static_mu;
 void* g_static_ptr[64] = {};
+unsigned long long g_static_ctx[64] = {};  // context the cached address belongs to
 }  // namespace
 
 // Device address of g_static_scratch on the current device, looked up once
-// per device (the host-side name is only a stand-in, not a device address).
+// per device and context (the host-side name is only a stand-in, not a device
+// address).  A context created after a device reset has a new ID, so the
+// address is looked up again instead of pointing into the old context's memory.
 static int static_scratch_ptr(int device, void** out) {
     if (device < 0 || device >= 64) return PA_ERR_CUDA;
+    unsigned long long ctx = 0;
+    if (current_context_id(&ctx) != PA_OK) return PA_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_static_mu);
-    if (g_static_ptr[device] == nullptr) {
+    if (g_static_ptr[device] == nullptr || g_static_ctx[device] != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
         g_static_ptr[device] = p;
+        g_static_ctx[device] = ctx;
     }
     *out = g_static_ptr[device];
     return PA_OK;
@@ -1425,6 +1472,7 @@ extern "C" int attn_decode_paged_noalloc(void* out, float* lse, const void* q, c
                                          const int32_t* seq_lens, int batch, int max_seq_len, int page_size,
                                          int num_q_heads, int num_kv_heads, int head_dim, float softmax_scale,
                                          int32_t* status, void* stream) {
+    NvtxRange nvtx_("attn_decode_paged_noalloc");
     if (batch < 0) return PA_ERR_SHAPE;
     int rc = check_common_shapes(page_size, num_q_heads, num_kv_heads, head_dim);
     if (rc != PA_OK) return rc;

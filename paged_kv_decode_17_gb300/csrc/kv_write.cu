@@ -27,6 +27,7 @@
 // that the decode kernel reads the keys of one value column as one word.
 #include "pa_common.cuh"
 #include "pa_host.h"
+#include "pa_trace.h"
 
 #include <cmath>
 #include <cuda_fp8.h>
@@ -337,6 +338,7 @@ extern "C" int kv_write_paged(void* k_pool, void* v_pool, int num_pages, const v
                               int max_pages_per_seq, int batch, int total_new, int page_size, int num_kv_heads,
                               int head_dim, int32_t* status, void* stream) {
     using namespace pa;
+    NvtxRange nvtx_("kv_write_paged");
     if (batch < 0 || total_new < 0) return PA_ERR_SHAPE;
     if (head_dim != 64 && head_dim != 128) return PA_ERR_SHAPE;
     if (page_size < 16 || page_size > 256 || page_size % 16 != 0) return PA_ERR_SHAPE;
@@ -350,6 +352,7 @@ extern "C" int kv_write_paged(void* k_pool, void* v_pool, int num_pages, const v
     if (rc != PA_OK) return rc;
     const int blocks_needed = (total_new + kvw::kWarps - 1) / kvw::kWarps;
     const int grid = blocks_needed < dev.sm_count * 16 ? blocks_needed : dev.sm_count * 16;
+    log_config("kv writeback: head_dim %d, one warp per new row, grid %d CTAs x %d warps", head_dim, grid, kvw::kWarps);
     kvw::kv_write_kernel<<<grid, kvw::kWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<__nv_bfloat16*>(k_pool), static_cast<__nv_bfloat16*>(v_pool),
         static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new), cu_seqlens_new, seq_lens,
@@ -364,6 +367,7 @@ extern "C" int kv_write_paged_rope(void* k_pool, void* v_pool, int num_pages, co
                                    const void* q_norm_weight, const void* k_norm_weight, float norm_eps,
                                    int32_t* status, void* stream) {
     using namespace pa;
+    NvtxRange nvtx_("kv_write_paged_rope");
     if (batch < 0 || total_new < 0) return PA_ERR_SHAPE;
     if (head_dim != 64 && head_dim != 128) return PA_ERR_SHAPE;
     if (page_size < 16 || page_size > 256 || page_size % 16 != 0) return PA_ERR_SHAPE;
@@ -415,6 +419,8 @@ extern "C" int kv_write_paged_rope(void* k_pool, void* v_pool, int num_pages, co
     const int blocks_needed = (total_new + kvw::kWarps - 1) / kvw::kWarps;
     const int grid = blocks_needed < dev.sm_count * 16 ? blocks_needed : dev.sm_count * 16;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    log_config("kv writeback with RoPE%s%s: head_dim %d, grid %d CTAs x %d warps", k_norm_weight ? " + K norm" : "",
+               q ? " (+ queries in place)" : "", head_dim, grid, kvw::kWarps);
     if (head_dim == 128)
         kvw::kv_write_rope_kernel<128><<<grid, kvw::kWarps * 32, 0, st>>>(prm);
     else
@@ -428,6 +434,7 @@ extern "C" int kv_write_paged_fp8(void* k_pool, void* v_pool, int num_pages, con
                                   int batch, int total_new, int page_size, int num_kv_heads, int head_dim,
                                   int32_t* status, void* stream) {
     using namespace pa;
+    NvtxRange nvtx_("kv_write_paged_fp8");
     if (batch < 0 || total_new < 0) return PA_ERR_SHAPE;
     if (head_dim != 64 && head_dim != 128) return PA_ERR_SHAPE;
     if (page_size < 16 || page_size > 256 || (page_size & (page_size - 1)) != 0) return PA_ERR_SHAPE;
@@ -448,6 +455,7 @@ extern "C" int kv_write_paged_fp8(void* k_pool, void* v_pool, int num_pages, con
     auto* vp = static_cast<uint8_t*>(v_pool);
     auto* kn = static_cast<const __nv_bfloat16*>(k_new);
     auto* vn = static_cast<const __nv_bfloat16*>(v_new);
+    log_config("kv writeback to fp8 e4m3: head_dim %d, grid %d CTAs x %d warps", head_dim, grid, kvw::kWarps);
     if (head_dim == 128)
         kvw::kv_write_fp8_kernel<128><<<grid, kvw::kWarps * 32, 0, st>>>(
             kp, vp, kn, vn, k_scale, v_scale, cu_seqlens_new, seq_lens, block_table, num_pages, max_pages_per_seq,

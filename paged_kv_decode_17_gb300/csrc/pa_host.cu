@@ -30,6 +30,22 @@ void load_encode() {
     }
 }
 
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+void load_ctx() {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+}
+
 constexpr int kMaxKernelSlots = 32;
 bool g_smem_set[kMaxDevices][kMaxKernelSlots] = {};
 
@@ -65,6 +81,14 @@ int current_device(DeviceInfo* info) {
     }
     if (info->major != 10 || info->minor != 3) return PA_ERR_ARCH;
     return PA_OK;
+}
+
+int current_context_id(unsigned long long* id) {
+    std::call_once(g_ctx_once, load_ctx);
+    if (g_ctx_current == nullptr || g_ctx_id == nullptr) return PA_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return PA_ERR_CUDA;
+    return g_ctx_id(ctx, id) == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
 int encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t row_elems, uint32_t box_cols,
@@ -111,7 +135,7 @@ extern "C" const char* pa_status_string(int status) {
         case PA_ERR_SHAPE: return "unsupported or inconsistent sizes";
         case PA_ERR_WORKSPACE: return "workspace missing or too small";
         case PA_ERR_CUDA: return "CUDA runtime/driver call or kernel launch failed";
-        case PA_ERR_TIMEOUT: return "device: wait on an asynchronous copy timed out";
+        case PA_ERR_TIMEOUT: return "device: a prefill-kernel wait ran past its time limit";
         case PA_ERR_BAD_PAGE: return "device: block_table entry outside [0, num_pages)";
         case PA_ERR_BAD_LEN: return "device: sequence length / row count inconsistent";
         case PA_ERR_ARCH: return "current device is not an sm_103 GPU";

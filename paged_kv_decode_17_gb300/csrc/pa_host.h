@@ -22,6 +22,10 @@ struct DeviceInfo {
 // PA_ERR_CUDA or PA_ERR_ARCH (not an sm_103 GPU).
 int current_device(DeviceInfo* info);
 
+// Unique ID of the current CUDA context (a context created after a device
+// reset gets a new one).  Returns PA_OK or PA_ERR_CUDA.
+int current_context_id(unsigned long long* id);
+
 // Encode a 2-D bf16 tensor map over `rows` rows of `row_elems` elements
 // (row stride = row_elems * 2 bytes), box = box_cols x box_rows, 128-byte
 // swizzle.  Returns PA_OK or PA_ERR_CUDA.
@@ -57,11 +61,13 @@ namespace dec {
 // Split-K decode launcher (decode.cu).  cu_q == nullptr: one query row per
 // sequence.  Otherwise the entries with 1 <= q_len <= qmax are served, q_len
 // in (qmax, qcap] is reported as an error and longer entries are skipped.
+// per_segment: choose the operand order per segment (one-row entries of a
+// mixed call take the swapped-operand path even when qmax rows would not).
 int launch_decode(void* out, float* lse, const void* q, const void* k_pool, const void* v_pool, int num_pages,
                   const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
                   const int32_t* cu_q, int total_q, int qmax, int qcap, int batch, int max_seq_len, int page_size,
                   int num_q_heads, int num_kv_heads, int head_dim, float softmax_scale, void* workspace,
-                  size_t workspace_bytes, int32_t* status, void* stream);
+                  size_t workspace_bytes, int32_t* status, void* stream, bool per_segment = false);
 }  // namespace dec
 
 // Set the dynamic shared-memory limit of a kernel once per device.

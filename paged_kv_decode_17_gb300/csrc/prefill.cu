@@ -10,14 +10,12 @@
 // seq_len - q_len + i and sees keys 0 .. that position.
 //
 // GB300 design
-// * Work item = one 128-row query tile of one sequence for the query heads of
-//   one KV head.  A small plan kernel lists the query tiles sorted by their
-//   number of key tiles, heaviest first.  The main kernel is persistent: each
-//   thread-block cluster (up to 2 CTAs, one per SM) walks that list
-//   round-robin; the CTAs of a cluster take the head pairs of the same item,
-//   so each K/V tile is fetched once per cluster (TMA multicast).  Tensor
-//   memory, barriers and the cluster are set up once per CTA, and the next
-//   item's Q and K/V are loaded while the current item finishes.
+// * Work item = one 128-row query tile of one sequence for a pair of query
+//   heads of one KV head.  A small plan kernel lists the query tiles sorted by
+//   their number of key tiles, heaviest first.  The main kernel is persistent:
+//   each CTA (one per SM) walks that list round-robin.  Tensor memory and
+//   barriers are set up once per CTA, and the next item's Q and K/V are loaded
+//   while the current item finishes.
 // * warp 8 (producer): publishes each item through a 2-slot ring in shared
 //   memory, loads the two Q tiles by TMA (3-D tensor map over [rows][Hq][D],
 //   128-byte swizzle) and gathers K and V tiles: a 128-key tile is eight
@@ -47,6 +45,7 @@
 // PA_ERR_TIMEOUT and all roles fall through to a clean exit.
 #include "pa_common.cuh"
 #include "pa_host.h"
+#include "pa_trace.h"
 
 #include <algorithm>
 #include <mutex>
@@ -63,15 +62,11 @@ constexpr int UPT = BN / 16; // 16-key page blocks per KV tile
 #ifndef PA_PF_NV
 #define PA_PF_NV 2
 #endif
-#ifndef PA_PF_MAX_CLUSTER
-#define PA_PF_MAX_CLUSTER 2
-#endif
 // K and V tiles go through separate rings: the next K tile only waits for the
 // current scores (S) to be computed, not for the previous P.V to finish.
 constexpr int NK = PA_PF_NK;  // K ring depth
 constexpr int NV = PA_PF_NV;  // V ring depth
 constexpr int NSTAGE = NK + NV;  // stages 0 .. NK-1 hold K tiles, NK .. NSTAGE-1 V tiles
-constexpr int MAX_CLUSTER = PA_PF_MAX_CLUSTER;
 constexpr float TAU = 8.f;   // rescale threshold, log2 units
 // warps 0-7: softmax (head = warp / 4, row quarter = warp & 3)
 // warp 8: producer; warps 9 and 10: MMA issuers of head 0 and head 1
@@ -113,8 +108,8 @@ struct Params {
     int32_t* status;
     int num_pages, max_pages, batch, page_size;
     int Hq, Hkv, group;
-    int NPC;  // pair blocks per KV head (head pairs padded to a multiple of CS, / CS)
-    int CS;   // cluster size (CTAs sharing each K/V tile)
+    int NPC;  // head pairs per KV head
+    unsigned long long wait_ns;  // limit of any one wait (kWaitTimeoutNs unless overridden for tests)
     float scale_log2;
 };
 
@@ -134,21 +129,24 @@ struct Shared {
     uint64_t o_staged[2];                // per head: all 128 rows of O/l are in shared memory
     uint64_t o_read[2];                  // per head: the TMA store has read them (P buffer free again)
     uint64_t v_tail;                     // TMA copies of a V tile that runs past the sequence end land here
+    uint64_t mma_drain;                  // per MMA warp: all of its tensor-core operations have completed
     uint64_t item_full[2], item_empty[2];
     uint32_t tmem_base;
     int abort_flag;
     Item items[2];
 };
 
-__device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, Shared& sh, int32_t* status) {
+// Wait for phase `parity` of `bar`; false (and every other role falls through) once any
+// role of the CTA has waited longer than p.wait_ns, which records PA_ERR_TIMEOUT.
+__device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, Shared& sh, const Params& p) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*reinterpret_cast<volatile int*>(&sh.abort_flag)) return false;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        if (globaltimer_ns() - t0 > p.wait_ns) {
             *reinterpret_cast<volatile int*>(&sh.abort_flag) = 1;
-            report(status, PA_ERR_TIMEOUT);
+            report(p.status, PA_ERR_TIMEOUT);
             return false;
         }
     }
@@ -161,34 +159,6 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
-                                               uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
-        : "memory");
-}
-
-// Arrive on `bar` at the same offset in every CTA of `mask` once this thread's MMAs are done.
-__device__ __forceinline__ void commit_mc(uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
 }
 
 // max of three (one instruction on sm_100 and later)
@@ -298,9 +268,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int CS = p.CS;
-    const uint16_t cmask = (uint16_t)((1u << CS) - 1);
-    const int crank = CS > 1 ? (int)cluster_rank() : 0;
 
     if (tid == 0) {
         sh.abort_flag = 0;
@@ -319,13 +286,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(&sh.kv_full[s], 1);
-            mbar_init(&sh.kv_empty[s], 2 * CS);  // released by both MMA threads of every CTA of the cluster
+            mbar_init(&sh.kv_empty[s], 2);  // released by both MMA threads
         }
         mbar_init(&sh.v_tail, 1);
+        mbar_init(&sh.mma_drain, 2);
         fence_mbar_init();
     }
     __syncthreads();
-    if (CS > 1) cluster_sync();  // every CTA's barriers exist before anyone multicasts into them
     if (warp == WARP_TMA) {
         tc::tmem_alloc(&sh.tmem_base, C::TM_COLS);
         tc::tmem_relinquish();
@@ -338,8 +305,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint8_t* sQ = smem + C::OFF_Q;
     uint8_t* sP = smem + C::OFF_P;
     uint8_t* sKV = smem + C::OFF_KV;
-    const int n_clusters = gridDim.x / CS;
-    const int cluster_id = blockIdx.x / CS;
 
     if (warp == WARP_TMA) {
         // ===================================================== producer (whole warp)
@@ -350,12 +315,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         const long long n_items = (long long)__ldg(p.n_tiles) * p.Hkv * p.NPC;
         int kring = 0, vring = 0;     // K / V tiles issued so far
-        int tails = 0;                // uses of the v_tail barrier
+        int tails = 0;                // v_tail phases waited for
+        int tails_armed = 0;          // v_tail phases armed (copies issued)
+        bool v_open[NV] = {};         // V stage armed through v_tail, its kv_full arrival not yet made
         int qloads[2] = {0, 0};       // Q tiles loaded per head
         bool ok = true;
         for (int k = 0; ok; ++k) {
-            // ---- next item of this cluster (identical for every CTA of it)
-            const long long it = cluster_id + (long long)k * n_clusters;
+            // ---- next item of this CTA
+            const long long it = blockIdx.x + (long long)k * gridDim.x;
             Item itm;
             itm.end = it >= n_items;
             if (!itm.end) {
@@ -363,7 +330,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int ti = (int)(it / per);
                 const int rem = (int)(it - (long long)ti * per);
                 itm.g = rem / p.NPC;
-                const int pair = (rem - itm.g * p.NPC) * CS + crank;
+                const int pair = rem - itm.g * p.NPC;
                 const int2 bt = __ldg(p.tiles + ti);
                 itm.b = bt.x;
                 itm.t = bt.y;
@@ -378,7 +345,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 itm.n_kv = (itm.qmin + itm.rows_valid - 1) / BN + 1;
             }
             const int slot = k & 1;
-            ok = __all_sync(0xffffffffu, wait_ab(&sh.item_empty[slot], ((k >> 1) & 1) ^ 1, sh, p.status));
+            ok = __all_sync(0xffffffffu, wait_ab(&sh.item_empty[slot], ((k >> 1) & 1) ^ 1, sh, p));
             if (!ok) break;
             if (lane == 0) {
                 sh.items[slot] = itm;
@@ -390,7 +357,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int hh = 0; hh < itm.nheads && ok; ++hh) {
                 if (qloads[hh] > 0)
                     ok = __all_sync(0xffffffffu,
-                                    wait_ab(&sh.q_empty[hh], (qloads[hh] - 1) & 1, sh, p.status));
+                                    wait_ab(&sh.q_empty[hh], (qloads[hh] - 1) & 1, sh, p));
                 if (!ok) break;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&sh.bar_q[hh], C::Q_BYTES);
@@ -402,10 +369,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             if (!ok) break;
 
-            // ---- K / V tiles.  A tile is UPT x KB boxes: 16-key page blocks x 64-column halves.
-            // Box b is fetched by the cluster CTA of rank b % CS and multicast to all of them, so
-            // every CTA's barrier receives the whole tile.  Lane u < UPT resolves block u of a
-            // tile through the block table one tile ahead.
+            // ---- K / V tiles.  A tile is UPT x KB boxes: 16-key page blocks x 64-column halves,
+            // box b issued by lane b.  Lane u < UPT resolves block u of a tile through the block
+            // table one tile ahead.
             const int32_t* btab = p.block_table + (size_t)itm.b * p.max_pages;
             auto block_row = [&](int j) -> int {  // pool row of block `lane` of tile j, -1 if none
                 int row = -1;
@@ -429,15 +395,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const unsigned goodmask = __ballot_sync(0xffffffffu, my_row >= 0) & ((1u << UPT) - 1);
                 const int good = __popc(goodmask);
                 const int box_row = __shfl_sync(0xffffffffu, my_row, (lane / C::KB) % UPT);
-                const bool mine = lane < UPT * C::KB && (lane % CS) == crank && box_row >= 0;
+                const bool mine = lane < UPT * C::KB && box_row >= 0;
                 const bool tail = (j + 1) * BN > itm.seq_len;
                 for (int x = 0; x < 2 && ok; ++x) {
-                    const int i = x == 0 ? kring++ : vring++;
+                    const int i = x == 0 ? kring : vring;
                     const int depth = x == 0 ? NK : NV;
                     const int st = (x == 0 ? 0 : NK) + i % depth;
                     ok = __all_sync(0xffffffffu,
-                                    wait_ab(&sh.kv_empty[st], ((i / depth) & 1) ^ 1, sh, p.status));
+                                    wait_ab(&sh.kv_empty[st], ((i / depth) & 1) ^ 1, sh, p));
                     if (!ok) break;
+                    if (x == 0)
+                        ++kring;  // counted once armed: the drain below waits for armed tiles only
+                    else
+                        ++vring;
                     uint8_t* dst = sKV + st * C::KV_BYTES;
                     const bool via_tail = (x == 1) && tail;
                     uint64_t* land = via_tail ? &sh.v_tail : &sh.kv_full[st];
@@ -445,24 +415,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         if (good == 0)
                             mbar_arrive(land);
                         else
-                            mbar_arrive_expect_tx(land, good * 16 * D * 2);  // the whole tile, from all CTAs
+                            mbar_arrive_expect_tx(land, good * 16 * D * 2);  // the whole tile
                     }
                     __syncwarp();
                     if (mine) {
                         const int u = lane / C::KB, kb = lane - u * C::KB;
                         uint8_t* bdst = dst + kb * C::KV_KB + u * 2048;
                         const CUtensorMap* map = x == 0 ? &kmap : &vmap;
-                        if (CS > 1)
-                            tma_load_2d_mc(bdst, map, land, kb * 64, box_row, cmask);
-                        else
-                            tma_load_2d(bdst, map, land, kb * 64, box_row);
+                        tma_load_2d(bdst, map, land, kb * 64, box_row);
                     }
                     if (via_tail) {
+                        ++tails_armed;
+                        v_open[st - NK] = true;
                         // keys past the sequence end: their V rows may hold anything and 0 * NaN = NaN,
-                        // so zero them (in this CTA's copy) before any MMA may read this tile
-                        ok = __all_sync(0xffffffffu, wait_ab(&sh.v_tail, tails & 1, sh, p.status));
-                        ++tails;
+                        // so zero them before any MMA may read this tile
+                        ok = __all_sync(0xffffffffu, wait_ab(&sh.v_tail, tails & 1, sh, p));
                         if (!ok) break;
+                        ++tails;
                         const int first = itm.seq_len - j * BN;
                         const int nchunk = (BN - first) * 8 * C::KB;  // 16-byte chunks to clear
                         for (int c = lane; c < nchunk; c += 32) {
@@ -475,23 +444,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&sh.kv_full[st]);
+                        v_open[st - NK] = false;
                     }
                 }
             }
         }
-        // Before leaving: every copy into this CTA has landed and every MMA thread of the
-        // cluster has released the last stages (no remote arrival can still target us).
+        // Before leaving (also after an abort): every TMA copy issued into this CTA has
+        // landed.  Older tiles of a stage were consumed before the stage was re-armed, so
+        // only the last tile of each stage can still be in flight; a V tile armed through
+        // v_tail whose kv_full arrival was never made lands on v_tail.
         if (lane == 0) {
             for (int hh = 0; hh < 2; ++hh)
                 if (qloads[hh] > 0) mbar_wait(&sh.bar_q[hh], (qloads[hh] - 1) & 1);
-            for (int i = max(0, kring - NK); i < kring; ++i) {
-                mbar_wait(&sh.kv_full[i % NK], (i / NK) & 1);
-                mbar_wait(&sh.kv_empty[i % NK], (i / NK) & 1);
-            }
-            for (int i = max(0, vring - NV); i < vring; ++i) {
-                mbar_wait(&sh.kv_full[NK + i % NV], (i / NV) & 1);
-                mbar_wait(&sh.kv_empty[NK + i % NV], (i / NV) & 1);
-            }
+            for (int i = max(0, kring - NK); i < kring; ++i) mbar_wait(&sh.kv_full[i % NK], (i / NK) & 1);
+            for (int i = max(0, vring - NV); i < vring; ++i)
+                if (!v_open[i % NV]) mbar_wait(&sh.kv_full[NK + i % NV], (i / NV) & 1);
+            if (tails_armed > tails) mbar_wait(&sh.v_tail, (tails_armed - 1) & 1);
         }
         __syncwarp();
     } else if (warp == WARP_MMA0 || warp == WARP_MMA0 + 1) {
@@ -503,13 +471,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint32_t kv_base = smem_u32(sKV);
             const uint32_t t_s = tmem + C::TM_S0 + hh * BN;
             const uint32_t t_o = tmem + C::TM_O0 + hh * D;
-            // a K/V stage is free once every MMA thread of the cluster is done with it
-            auto release = [&](uint64_t* bar) {
-                if (CS > 1)
-                    commit_mc(bar, cmask);
-                else
-                    tc::commit(bar);
-            };
+            // a K/V stage is free once both MMA threads are done with it
+            auto release = [&](uint64_t* bar) { tc::commit(bar); };
             int kr = 0, vr = 0;  // K / V ring positions (same walk as the producer)
             // stage and phase of the K / V tile of key tile j of the current item
             auto kst = [&](int j) { return (kr + j) % NK; };
@@ -521,7 +484,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             int qn = 0;     // Q tiles consumed
             bool ok = true;
             for (int k = 0; ok; ++k) {
-                ok = wait_ab(&sh.item_full[k & 1], (k >> 1) & 1, sh, p.status);
+                ok = wait_ab(&sh.item_full[k & 1], (k >> 1) & 1, sh, p);
                 if (!ok) break;
                 const Item itm = sh.items[k & 1];
                 if (itm.end) break;
@@ -529,13 +492,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (hh >= itm.nheads) {
                     // not our head this time: still release every stage we pass
                     for (int j = 0; j < n && ok; ++j) {
-                        ok = wait_ab(&sh.kv_full[kst(j)], kph(j), sh, p.status);
+                        ok = wait_ab(&sh.kv_full[kst(j)], kph(j), sh, p);
                         if (ok) release(&sh.kv_empty[kst(j)]);
-                        if (ok) ok = wait_ab(&sh.kv_full[vst(j)], vph(j), sh, p.status);
+                        if (ok) ok = wait_ab(&sh.kv_full[vst(j)], vph(j), sh, p);
                         if (ok) release(&sh.kv_empty[vst(j)]);
                     }
                 } else {
-                    ok = wait_ab(&sh.bar_q[hh], qn & 1, sh, p.status);
+                    ok = wait_ab(&sh.bar_q[hh], qn & 1, sh, p);
                     ++qn;
                     auto issue_s = [&](int j) {
                         const uint32_t kaddr = kv_base + kst(j) * C::KV_BYTES;
@@ -562,8 +525,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         tc::commit(&sh.pv_done[hh]);
                     };
                     // scores of key tile 0 (the S buffer was freed by the previous tile's softmax)
-                    if (ok) ok = wait_ab(&sh.kv_full[kst(0)], kph(0), sh, p.status);
-                    if (ok && J > 0) ok = wait_ab(&sh.s_free[hh], (J - 1) & 1, sh, p.status);
+                    if (ok) ok = wait_ab(&sh.kv_full[kst(0)], kph(0), sh, p);
+                    if (ok && J > 0) ok = wait_ab(&sh.s_free[hh], (J - 1) & 1, sh, p);
                     if (ok) {
                         tc::fence_after_sync();
                         issue_s(0);
@@ -572,17 +535,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     for (int j = 0; j < n && ok; ++j) {
                         if (j + 1 < n) {
                             // next scores as soon as the softmax has pulled the current ones out of TMEM
-                            ok = wait_ab(&sh.kv_full[kst(j + 1)], kph(j + 1), sh, p.status) &&
-                                 wait_ab(&sh.s_free[hh], (J + j) & 1, sh, p.status);
+                            ok = wait_ab(&sh.kv_full[kst(j + 1)], kph(j + 1), sh, p) &&
+                                 wait_ab(&sh.s_free[hh], (J + j) & 1, sh, p);
                             if (!ok) break;
                             tc::fence_after_sync();
                             issue_s(j + 1);
                             release(&sh.kv_empty[kst(j + 1)]);
                         }
-                        ok = wait_ab(&sh.kv_full[vst(j)], vph(j), sh, p.status) &&
-                             wait_ab(&sh.p_ready[hh], (J + j) & 1, sh, p.status);
+                        ok = wait_ab(&sh.kv_full[vst(j)], vph(j), sh, p) &&
+                             wait_ab(&sh.p_ready[hh], (J + j) & 1, sh, p);
                         // the first P.V overwrites O: the previous item's epilogue must have read it
-                        if (ok && j == 0 && items > 0) ok = wait_ab(&sh.o_free[hh], (items - 1) & 1, sh, p.status);
+                        if (ok && j == 0 && items > 0) ok = wait_ab(&sh.o_free[hh], (items - 1) & 1, sh, p);
                         if (!ok) break;
                         tc::fence_after_sync();
                         issue_pv(j);
@@ -595,6 +558,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 vr += n;
                 mbar_arrive(&sh.item_empty[k & 1]);
             }
+            // every tensor-core operation this thread issued has completed (after an abort some
+            // may still run) before the CTA frees tensor memory and leaves
+            tc::commit(&sh.mma_drain);
+            mbar_wait(&sh.mma_drain, 0);
         }
         __syncwarp();
     } else {
@@ -612,7 +579,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         bool store_pending = false;  // the last of them may still be reading the P buffer
         bool ok = true;
         for (int k = 0; ok; ++k) {
-            ok = __all_sync(0xffffffffu, wait_ab(&sh.item_full[k & 1], (k >> 1) & 1, sh, p.status));
+            ok = __all_sync(0xffffffffu, wait_ab(&sh.item_full[k & 1], (k >> 1) & 1, sh, p));
             if (!ok) break;
             const Item itm = sh.items[k & 1];
             if (itm.end) break;
@@ -622,7 +589,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 float m_ref = -INFINITY, l = 0.f;
                 for (int j = 0; j < n && ok; ++j) {
                     const int jj = J + j;
-                    ok = __all_sync(0xffffffffu, wait_ab(&sh.s_full[hh], jj & 1, sh, p.status));
+                    ok = __all_sync(0xffffffffu, wait_ab(&sh.s_full[hh], jj & 1, sh, p));
                     if (!ok) break;
                     tc::fence_after_sync();
                     // the whole score row into registers, then S is free for the next tile's MMA
@@ -659,7 +626,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         // rescale O to a new reference maximum (all earlier PVs done once PV(j-1) is)
                         const float m_new = fmaxf(m_ref, mx);
                         const float alpha = ex2(m_ref - m_new);
-                        ok = __all_sync(0xffffffffu, wait_ab(&sh.pv_done[hh], (jj - 1) & 1, sh, p.status));
+                        ok = __all_sync(0xffffffffu, wait_ab(&sh.pv_done[hh], (jj - 1) & 1, sh, p));
                         if (!ok) break;
                         tc::fence_after_sync();
 #pragma unroll 1
@@ -696,7 +663,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     // previous item).  Waiting for it also keeps p_ready / pv_done within one
                     // phase of their waiters (mbarrier parity only tells adjacent phases apart).
                     if (jj > 0) {
-                        ok = __all_sync(0xffffffffu, wait_ab(&sh.pv_done[hh], (jj - 1) & 1, sh, p.status));
+                        ok = __all_sync(0xffffffffu, wait_ab(&sh.pv_done[hh], (jj - 1) & 1, sh, p));
                         if (!ok) break;
                     }
                     // the previous item's O may still be leaving the P buffer through a TMA store
@@ -705,7 +672,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             bulk_wait_read_all();
                             mbar_arrive(&sh.o_read[hh]);
                         }
-                        ok = __all_sync(0xffffffffu, wait_ab(&sh.o_read[hh], (nst - 1) & 1, sh, p.status));
+                        ok = __all_sync(0xffffffffu, wait_ab(&sh.o_read[hh], (nst - 1) & 1, sh, p));
                         if (!ok) break;
                         store_pending = false;
                     }
@@ -723,7 +690,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 // ---- epilogue: O / l -> bf16, then hand O back to the MMA thread
                 if (ok)
-                    ok = __all_sync(0xffffffffu, wait_ab(&sh.pv_done[hh], (J + n - 1) & 1, sh, p.status));
+                    ok = __all_sync(0xffffffffu, wait_ab(&sh.pv_done[hh], (J + n - 1) & 1, sh, p));
                 if (ok) {
                     tc::fence_after_sync();
                     const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -752,7 +719,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         fence_proxy_async_smem();
                         mbar_arrive(&sh.o_staged[hh]);
                         if (leader) {
-                            ok = wait_ab(&sh.o_staged[hh], nst & 1, sh, p.status);
+                            ok = wait_ab(&sh.o_staged[hh], nst & 1, sh, p);
                             if (ok) {
 #pragma unroll
                                 for (int kb = 0; kb < C::KB; ++kb)
@@ -797,7 +764,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     tc::fence_before_sync();
     __syncthreads();
-    if (CS > 1) cluster_sync();  // nobody multicasts into or arrives on this CTA any more
     tc::fence_after_sync();
     if (warp == WARP_TMA) tc::tmem_dealloc(tmem, C::TM_COLS);
 }
@@ -821,38 +787,42 @@ extern "C" size_t pa_prefill_workspace_bytes(int batch, int total_q, int num_q_h
 }
 
 namespace {
-// Clusters of the prefill kernel that can be resident at once (queried once per device / config).
+// CTAs of the prefill kernel that can be resident at once (queried once per device / head_dim).
 std::mutex g_occ_mu;
-int g_occ[64][2][9] = {};
+int g_occ[64][2] = {};
 
 template <int D>
-int max_clusters(int device, int CS, cudaLaunchConfig_t cfg) {
+int max_ctas(int device) {
     std::lock_guard<std::mutex> lk(g_occ_mu);
-    if (device < 0 || device >= 64 || CS < 1 || CS > 8) return 0;
-    int& v = g_occ[device][D == 128 ? 1 : 0][CS];
+    if (device < 0 || device >= 64) return 0;
+    int& v = g_occ[device][D == 128 ? 1 : 0];
     if (v == 0) {
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, pf::prefill_kernel<D>, &cfg) != cudaSuccess || n <= 0) return 0;
-        v = n;
+        int per_sm = 0, sms = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pf::prefill_kernel<D>, pf::NTHREADS,
+                                                          pf::Cfg<D>::SMEM_BYTES) != cudaSuccess ||
+            per_sm <= 0)
+            return 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0) return 0;
+        v = per_sm * sms;
     }
     return v;
 }
 
 template <int D>
-int launch_persistent(cudaLaunchConfig_t& cfg, int device, int CS, long long items_upper, const CUtensorMap& qmap,
+int launch_persistent(cudaStream_t st, int device, long long items_upper, const CUtensorMap& qmap,
                       const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& omap,
                       const pf::Params& prm) {
-    cfg.dynamicSmemBytes = pf::Cfg<D>::SMEM_BYTES;
     if (set_smem_limit_once((const void*)pf::prefill_kernel<D>, pf::Cfg<D>::SMEM_BYTES, device, D == 128 ? 2 : 3) !=
         PA_OK)
         return PA_ERR_CUDA;
-    cfg.gridDim = dim3((unsigned)CS, 1, 1);
-    long long nc = max_clusters<D>(device, CS, cfg);
-    if (nc <= 0) return PA_ERR_CUDA;
-    if (nc > items_upper) nc = items_upper;
-    cfg.gridDim = dim3((unsigned)(nc * CS), 1, 1);
-    return cudaLaunchKernelEx(&cfg, pf::prefill_kernel<D>, qmap, kmap, vmap, omap, prm) == cudaSuccess ? PA_OK
-                                                                                                 : PA_ERR_CUDA;
+    long long n = max_ctas<D>(device);
+    if (n <= 0) return PA_ERR_CUDA;
+    if (n > items_upper) n = items_upper;
+    log_config("varlen causal prefill: head_dim %d, persistent grid %lld CTAs x %d threads (1 per SM), "
+               "query tile %d rows x key tile %d, 2 heads per CTA, K ring %d / V ring %d stages, %d B smem",
+               D, n, pf::NTHREADS, pf::BM, pf::BN, pf::NK, pf::NV, pf::Cfg<D>::SMEM_BYTES);
+    pf::prefill_kernel<D><<<(unsigned)n, pf::NTHREADS, pf::Cfg<D>::SMEM_BYTES, st>>>(qmap, kmap, vmap, omap, prm);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 }  // namespace
 
@@ -863,6 +833,7 @@ extern "C" int attn_prefill_varlen_causal(void* out, float* lse, const void* q, 
                                           int max_seq_len, int page_size, int num_q_heads, int num_kv_heads,
                                           int head_dim, float softmax_scale, void* workspace,
                                           size_t workspace_bytes, int32_t* status, void* stream) {
+    NvtxRange nvtx_("attn_prefill_varlen_causal");
     if (batch < 0 || total_q < 0 || max_q_len < 0 || max_seq_len < 0) return PA_ERR_SHAPE;
     int rc = check_common_shapes(page_size, num_q_heads, num_kv_heads, head_dim);
     if (rc != PA_OK) return rc;
@@ -891,14 +862,12 @@ extern "C" int attn_prefill_varlen_causal(void* out, float* lse, const void* q, 
     rc = dec::launch_decode(out, lse, q, k_pool, v_pool, num_pages, block_table, max_pages_per_seq, seq_lens,
                             cu_seqlens_q, total_q, dec_qmax, kDecodeMaxQ, batch, max_seq_len, page_size,
                             num_q_heads, num_kv_heads, head_dim, softmax_scale, workspace, dec_bytes, status,
-                            stream);
+                            stream, /*per_segment=*/true);
     if (rc != PA_OK) return rc;
     if (max_q_len <= kDecodeMaxQ) return PA_OK;  // no entry needs the prefill kernel
 
     const int group = num_q_heads / num_kv_heads;
-    const int pairs = (group + 1) / 2;
-    const int CS = pairs < pf::MAX_CLUSTER ? pairs : pf::MAX_CLUSTER;
-    const int NPC = (pairs + CS - 1) / CS;  // pair blocks per KV head
+    const int NPC = (group + 1) / 2;  // head pairs per KV head
     const long long tiles_upper = (long long)(total_q + pf::BM - 1) / pf::BM + batch;
     const long long items_upper = tiles_upper * num_kv_heads * NPC;
 
@@ -938,20 +907,9 @@ extern "C" int attn_prefill_varlen_causal(void* out, float* lse, const void* q, 
     prm.Hkv = num_kv_heads;
     prm.group = group;
     prm.NPC = NPC;
-    prm.CS = CS;
     prm.scale_log2 = softmax_scale * kLog2e;
+    prm.wait_ns = prefill_wait_ns(kWaitTimeoutNs);
 
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(pf::NTHREADS, 1, 1);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (head_dim == 128)
-        return launch_persistent<128>(cfg, dev.device, CS, items_upper, qmap, kmap, vmap, omap, prm);
-    return launch_persistent<64>(cfg, dev.device, CS, items_upper, qmap, kmap, vmap, omap, prm);
+    if (head_dim == 128) return launch_persistent<128>(st, dev.device, items_upper, qmap, kmap, vmap, omap, prm);
+    return launch_persistent<64>(st, dev.device, items_upper, qmap, kmap, vmap, omap, prm);
 }

@@ -249,3 +249,47 @@ def test_append_with_pinned_host_rows(cuda_device):
     torch.cuda.synchronize()
     assert torch.equal(hout.view(torch.int16), ref.cpu().view(torch.int16))
     assert torch.equal(k2.view(torch.int16), case.k_pool.view(torch.int16))
+
+
+@pytest.mark.parametrize("chunk", ["1", "3"])
+def test_forced_small_chunks(cuda_device, monkeypatch, chunk):
+    """PAGEDATTN_DECODE_CHUNK shrinks the split-K chunks (in 16-key units), so even
+    tiny problems are split across many CTAs and merged; the result stays within
+    tolerance and run-to-run bit-identical."""
+    monkeypatch.setenv("PAGEDATTN_DECODE_CHUNK", chunk)
+    for case in (workloads.tiny_decode(seed=1), workloads.tiny_decode(seed=2, sharp=True),
+                 workloads.make_paged_case("chunks", [1, 700, 33, 2049], [1] * 4, 28, 4, 128, seed=44)):
+        _check(case, cuda_device)
+        a, la = _decode(case, cuda_device)
+        b, lb = _decode(case, cuda_device)
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)) and torch.equal(la, lb)
+
+
+def test_config_log_once_per_configuration(cuda_device, tmp_path):
+    """PAGEDATTN_LOG prints the chosen launch configuration once per distinct
+    configuration (a child process, so the environment is read fresh)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = (
+        "import sys; sys.path.insert(0, %r)\n"
+        "import torch, workloads, paged_kv_decode_17_gb300 as pa\n"
+        "dev = torch.device('cuda:0')\n"
+        "c = workloads.tiny_decode(seed=0).to(dev)\n"
+        "for _ in range(3):\n"
+        "    pa.attn_decode_paged(c.q, c.k_pool, c.v_pool, c.block_table, c.seq_lens, c.softmax_scale, max_seq_len=100)\n"
+        "m = workloads.make_paged_case('log', [300, 1], [200, 1], 8, 2, 128, seed=1).to(dev)\n"
+        "pa.attn_prefill_varlen_causal(m.q, m.k_pool, m.v_pool, m.block_table, m.cu_seqlens_q, m.seq_lens)\n"
+        "torch.cuda.synchronize()\n" % root)
+    env = dict(os.environ, PAGEDATTN_LOG="1")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stderr.splitlines() if l.startswith("[pagedattn]")]
+    dec = [l for l in lines if "split-K decode" in l]
+    assert len([l for l in dec if "head_dim 64" in l]) == 1, lines  # three identical calls, one line
+    assert any("per segment" in l for l in dec), lines  # the prefill call's one-row entries
+    assert any("varlen causal prefill" in l for l in lines), lines
+    env["PAGEDATTN_LOG"] = "0"
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "[pagedattn]" not in r.stderr

@@ -47,6 +47,11 @@ CASES = [
     ("page32", [500, 77], [300, 77], 8, 2, 128, 32),
     ("page64", [260, 1000], [260, 500], 4, 1, 128, 64),
     ("mixed_decode_rows", [900, 1, 77, 3000, 256], [256, 1, 1, 1, 256], 32, 8, 128, 16),
+    # one-row entries (swapped operand order: group x 1 <= 8 rows) next to 2-8-row blocks (plain
+    # order) and a prefill chunk in the same call
+    ("mixed_orders_g4", [2000, 1, 600, 77, 1500, 9], [1, 1, 3, 8, 300, 1], 16, 4, 128, 16),
+    ("mixed_orders_g8", [40, 5000, 333, 700], [1, 5, 1, 150], 16, 2, 128, 16),
+    ("mixed_orders_d64", [1200, 64, 900], [1, 2, 129], 8, 2, 64, 16),
 ]
 
 
@@ -138,6 +143,27 @@ def test_prefill_bad_page_reports_status(cuda_device):
     assert int(status.item()) == -6
 
 
+def test_wait_timeout_reports_status_and_context_survives(cuda_device, monkeypatch):
+    """With the prefill's wait limit cut to 1 ns (PAGEDATTN_PREFILL_WAIT_NS), waits
+    run out: the call returns, the status word holds PA_ERR_TIMEOUT (-5), every
+    CTA drains its copies and tensor-core work and exits, and the next call with
+    the normal limit is clean and correct."""
+    import time
+    pa = _pa()
+    case = workloads.make_paged_case("timeout", [3000, 2000, 1000, 600], [3000, 2000, 1000, 300], 8, 2, 128, seed=66)
+    g = case.to(cuda_device)
+    monkeypatch.setenv("PAGEDATTN_PREFILL_WAIT_NS", "1")
+    status = pa.new_status(cuda_device)
+    t0 = time.time()
+    pa.attn_prefill_varlen_causal(g.q, g.k_pool, g.v_pool, g.block_table, g.cu_seqlens_q, g.seq_lens,
+                                  g.softmax_scale, status=status)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 60.0
+    assert int(status.item()) == -5
+    monkeypatch.delenv("PAGEDATTN_PREFILL_WAIT_NS")
+    _check(case, cuda_device)  # clean status, oracle parity
+
+
 @pytest.mark.slow
 def test_varlen_prefill_full_size_sampled(cuda_device):
     """16 sequences of 512..4096 tokens, Hq=28, Hkv=4: writeback then prefill;
@@ -156,10 +182,8 @@ def test_varlen_prefill_full_size_sampled(cuda_device):
                       case.block_table)
     out, lse = _prefill(case, cuda_device)
     assert torch.isfinite(out.float()).all()
-    heads = [0, 13, 27]
-    ref_out, ref_lse = oracle.paged_attention(**args, heads=heads)
-    assert_attention_close(out[rows][:, heads], ref_out[:, heads], lse[rows][:, heads], ref_lse[:, heads],
-                           what="varlen_prefill sampled")
+    ref_out, ref_lse = oracle.paged_attention(**args)  # every head of the sampled sequences
+    assert_attention_close(out[rows], ref_out, lse[rows], ref_lse, what="varlen_prefill sampled")
 
 
 @pytest.mark.slow
@@ -179,7 +203,14 @@ def test_mixed_step_full_size_sampled(cuda_device):
     mid = sorted(decs, key=lambda b: lens[b])[len(decs) // 2]
     seqs = [chunk, mid, longest]
     args, rows = compact_for_oracle(case, seqs)
-    heads = [0, 13, 31]
-    ref_out, ref_lse = oracle.paged_attention(**args, heads=heads)
-    assert_attention_close(out[rows][:, heads], ref_out[:, heads], lse[rows][:, heads], ref_lse[:, heads],
-                           what="mixed_step sampled")
+    ref_out, ref_lse = oracle.paged_attention(**args)  # every head of the sampled sequences
+    assert_attention_close(out[rows], ref_out, lse[rows], ref_lse, what="mixed_step sampled")
+
+
+@pytest.mark.parametrize("name,seq_lens,q_lens,hq,hkv,d,ps", [CASES[-3], CASES[-1]], ids=["g4", "d64"])
+def test_mixed_call_with_every_segment_split(cuda_device, monkeypatch, name, seq_lens, q_lens, hq, hkv, d, ps):
+    """PAGEDATTN_DECODE_CHUNK=1 cuts the decode rows' KV into one-unit chunks, so
+    every short entry's result comes out of the log-sum-exp merge."""
+    monkeypatch.setenv("PAGEDATTN_DECODE_CHUNK", "1")
+    case = workloads.make_paged_case(name, seq_lens, q_lens, hq, hkv, d, page_size=ps, seed=len(name) * 7 + d)
+    _check(case, cuda_device)

@@ -3,9 +3,11 @@
 Some callers cannot allocate device memory (allocator or memory-pool
 callbacks, plugins inside a framework that owns every device allocation), so
 they cannot hand attn_decode_paged a workspace.  attn_decode_paged_noalloc
-keeps that scratch in a fixed device array inside the library.  This file is
-collected last on purpose: its calls share that array, and it must pass both
-alone in a fresh process and after every other test.
+keeps that scratch in a fixed device array inside the library.  Both calls run
+the same kernels with the same split, so their results must be bit-identical;
+the result is also checked against the fp64 oracle.  This file is collected
+last on purpose: its calls share that array, and it must pass both alone in a
+fresh process and after every other test.
 """
 
 import ctypes
@@ -13,8 +15,9 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 import workloads
-from tests.conftest import ATOL, RTOL
+from tests.conftest import assert_attention_close, compact_for_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -34,11 +37,6 @@ def _noalloc(lib, g, out, lse, status):
         status.data_ptr(), torch.cuda.current_stream().cuda_stream)
 
 
-def _close(a, b):
-    a, b = a.float(), b.float()
-    return bool(((a - b).abs() <= ATOL + RTOL * b.abs()).all())
-
-
 @pytest.mark.parametrize("make", [
     lambda dev: workloads.tiny_decode(seed=3, device=dev),
     lambda dev: workloads.make_paged_case("ragged", [3000, 1, 700, 12000, 45], [1] * 5, 32, 8, 128, seed=5,
@@ -50,6 +48,7 @@ def test_noalloc_matches_workspace_entry_point_twice(cuda_device, make):
     g = make(cuda_device)
     ref, ref_lse = pa.attn_decode_paged(g.q, g.k_pool, g.v_pool, g.block_table, g.seq_lens, g.softmax_scale,
                                         max_seq_len=max(1, g.max_seq_len), return_lse=True)
+    want_out, want_lse = oracle.paged_attention(**compact_for_oracle(g, list(range(g.batch)))[0])
     for _ in range(2):  # the second call sees what the first left in the shared array
         out = torch.full_like(g.q, float("nan"))
         lse = torch.full((g.batch, g.num_q_heads), float("nan"), device=cuda_device)
@@ -57,10 +56,11 @@ def test_noalloc_matches_workspace_entry_point_twice(cuda_device, make):
         assert _noalloc(lib, g, out, lse, status) == 0
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        assert _close(out, ref), "allocation-free output differs from attn_decode_paged"
-        fin = torch.isfinite(ref_lse)
-        assert torch.equal(torch.isfinite(lse), fin)
-        assert bool(((lse[fin] - ref_lse[fin]).abs() <= 1e-3).all())
+        # same kernels, same split, same merge order: bit-identical to the workspace entry point
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), \
+            "allocation-free output differs from attn_decode_paged"
+        assert torch.equal(lse, ref_lse), "allocation-free lse differs from attn_decode_paged"
+        assert_attention_close(out, want_out, lse, want_lse, what="attn_decode_paged_noalloc")
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(cuda_device):
