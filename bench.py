@@ -391,6 +391,27 @@ def _flush_l2(buf):
     buf.zero_()
 
 
+class _prefill_path:
+    """Select how attn_prefill_varlen_causal runs a call with prefill entries (the
+    library reads PAGEDATTN_PREFILL_PATH at every call): "fused" = one persistent
+    kernel for the decode rows and the prefill tiles, then the merge of split decode
+    rows; "separate" = split-K decode + merge, plan and prefill kernels."""
+
+    def __init__(self, path):
+        self.path = path
+
+    def __enter__(self):
+        self.old = os.environ.get("PAGEDATTN_PREFILL_PATH")
+        os.environ["PAGEDATTN_PREFILL_PATH"] = self.path
+        return self
+
+    def __exit__(self, *a):
+        if self.old is None:
+            os.environ.pop("PAGEDATTN_PREFILL_PATH", None)
+        else:
+            os.environ["PAGEDATTN_PREFILL_PATH"] = self.old
+
+
 def measure_prefill(pa, steps, warmup, peaks):
     """Varlen causal prefill step: writeback of every new row, then prefill.
     16 sequences of 512..4096 tokens, Hq=28, Hkv=4, D=128.  L2 is flushed
@@ -413,26 +434,30 @@ def measure_prefill(pa, steps, warmup, peaks):
                                       case.seq_lens, case.softmax_scale, max_q_len=case.max_q_len,
                                       max_seq_len=case.max_seq_len, out=out, workspace=ws)
 
-    for _ in range(warmup):
-        write()
-        attn()
-    torch.cuda.synchronize()
-    w_ms, a_ms = [], []
-    for _ in range(steps):
-        _flush_l2(flush)
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        e[0].record(stream)
-        write()
-        e[1].record(stream)
-        attn()
-        e[2].record(stream)
-        torch.cuda.synchronize()
-        w_ms.append(e[0].elapsed_time(e[1]))
-        a_ms.append(e[1].elapsed_time(e[2]))
+    def run(path):
+        with _prefill_path(path):
+            for _ in range(warmup):
+                write()
+                attn()
+            torch.cuda.synchronize()
+            w_ms, a_ms = [], []
+            for _ in range(steps):
+                _flush_l2(flush)
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                e[0].record(stream)
+                write()
+                e[1].record(stream)
+                attn()
+                e[2].record(stream)
+                torch.cuda.synchronize()
+                w_ms.append(e[0].elapsed_time(e[1]))
+                a_ms.append(e[1].elapsed_time(e[2]))
+        return statistics.median(w_ms), statistics.median(a_ms)
+
+    w, a = run("fused")
+    _, a_sep = run("separate")
     flops = roofline.prefill_flops(case.q_lens_host, case.seq_lens_host, case.num_q_heads, case.head_dim)
     wbytes = roofline.kv_write_bytes(case.total_q, case.num_kv_heads, case.head_dim)
-    a = statistics.median(a_ms)
-    w = statistics.median(w_ms)
     tflops = flops / (a * 1e-3) / 1e12
     res = {"workload": "varlen_prefill: 16 sequences, lengths uniform 512..4096 (seeded), no prior tokens, "
                        "Hq=28, Hkv=4, head_dim 128, 16-token pages; step = writeback of all new rows + prefill",
@@ -443,7 +468,10 @@ def measure_prefill(pa, steps, warmup, peaks):
            "kv_write": {"ms": w, "bytes": wbytes, "gbs": wbytes / (w * 1e-3) / 1e9,
                         "frac_hbm": wbytes / (w * 1e-3) / 1e9 / peaks["hbm_gbs"]},
            "l2": "flushed (256 MiB write) between iterations", "steps": steps,
-           "launches_per_step": 5}  # writeback, split-K decode + merge (no entry to serve here), plan, prefill
+           "path": "fused: one persistent kernel (decode rows, none here, then prefill tiles) + merge",
+           "launches_per_step": 3,  # writeback, fused kernel, merge
+           "separate_kernels": {"prefill_ms": a_sep, "tflops": flops / (a_sep * 1e-3) / 1e12,
+                                "launches_per_step": 5}}  # writeback, decode + merge, plan, prefill
     del case, flush
     torch.cuda.empty_cache()
     return res
@@ -561,18 +589,23 @@ def measure_mixed(pa, steps, warmup, peaks):
                                       case.seq_lens, case.softmax_scale, max_q_len=case.max_q_len,
                                       max_seq_len=case.max_seq_len, out=out, workspace=ws)
 
-    for _ in range(warmup):
-        attn()
-    torch.cuda.synchronize()
-    ms = []
-    for _ in range(steps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        attn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms.append(e0.elapsed_time(e1))
-    t = statistics.median(ms)
+    def run(path):
+        with _prefill_path(path):
+            for _ in range(warmup):
+                attn()
+            torch.cuda.synchronize()
+            ms = []
+            for _ in range(steps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                attn()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ms.append(e0.elapsed_time(e1))
+        return statistics.median(ms)
+
+    t = run("fused")
+    t_sep = run("separate")
     # entries with up to 8 query rows run on the split-K decode path (HBM-bound), longer ones on the prefill kernel
     dec = [(L, q) for L, q in zip(case.seq_lens_host, case.q_lens_host) if q <= 8]
     pre_q = [q for q in case.q_lens_host if q > 8]
@@ -586,7 +619,11 @@ def measure_mixed(pa, steps, warmup, peaks):
            "step_ms": t, "decode_kv_bytes": dbytes, "prefill_flops": flops,
            "t_roofline_ms": 1e3 * max(t_bytes, t_flops), "t_serial_roofline_ms": 1e3 * (t_bytes + t_flops),
            "frac_of_roofline": max(t_bytes, t_flops) / (t * 1e-3),
-           "tokens_per_s": case.total_q / (t * 1e-3), "launches_per_step": 4, "steps": steps,
+           "tokens_per_s": case.total_q / (t * 1e-3), "steps": steps,
+           "path": "fused: one persistent kernel (split-K decode rows, then prefill tiles) + merge",
+           "launches_per_step": 2,
+           "separate_kernels": {"step_ms": t_sep, "frac_of_roofline": max(t_bytes, t_flops) / (t_sep * 1e-3),
+                                "launches_per_step": 4},  # decode + merge, plan, prefill
            "l2": "inputs larger than L2 (about 9 GB of KV)"}
     del case
     torch.cuda.empty_cache()
@@ -773,7 +810,7 @@ def main(argv=None):
         line["multiquery"] = measure_multiquery(pa, psteps, 3, peaks)
         line["rope_writeback"] = measure_rope_writeback(pa, psteps, 3, peaks)
         line["fp8_decode"] = measure_fp8_decode(pa, psteps, 3, peaks)
-        line["gpu_launches"] += world * psteps * (2 * 2 + 5 + 4 + 2 + 1 + 2)
+        line["gpu_launches"] += world * psteps * (2 * 2 + (3 + 5) + (2 + 4) + 2 + 1 + 2)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_subprocess()
     if rank == 0:

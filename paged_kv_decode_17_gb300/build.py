@@ -23,7 +23,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libpagedattn.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
-SOURCES = ["pa_host.cu", "kv_write.cu", "decode.cu", "prefill.cu"]
+SOURCES = ["pa_host.cu", "kv_write.cu", "decode.cu", "prefill.cu", "mixed.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
           "-I" + INCLUDE, "-I" + CSRC]

@@ -15,6 +15,11 @@
 //   in the prefill kernel to n nanoseconds instead of 2 s.  A tiny limit makes
 //   the waits run out, which is how the tests exercise the timeout path
 //   (PA_ERR_TIMEOUT in the status word, a clean exit, a usable context).
+// * PAGEDATTN_PREFILL_PATH=fused|separate picks how attn_prefill_varlen_causal
+//   runs a call with prefill entries: one persistent kernel for the decode
+//   rows and the prefill tiles (plus the merge of split decode rows), or the
+//   split-K decode, the plan and the prefill as separate kernels.  Both compute
+//   the same result; the tests run both.
 #pragma once
 
 #include <nvtx3/nvToolsExt.h>
@@ -75,6 +80,15 @@ inline unsigned long long prefill_wait_ns(unsigned long long dflt) {
     const long long n = std::strtoll(v, &end, 10);
     if (end == v || *end != '\0' || n < 1 || n > 60000000000ll) return dflt;
     return (unsigned long long)n;
+}
+
+// 1: one fused launch, 2: separate kernels, 0: not set (the library's default).
+inline int prefill_path_override() {
+    const char* v = std::getenv("PAGEDATTN_PREFILL_PATH");
+    if (v == nullptr) return 0;
+    if (std::strcmp(v, "fused") == 0) return 1;
+    if (std::strcmp(v, "separate") == 0) return 2;
+    return 0;
 }
 
 }  // namespace pa

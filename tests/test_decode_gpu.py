@@ -289,7 +289,7 @@ def test_config_log_once_per_configuration(cuda_device, tmp_path):
     dec = [l for l in lines if "split-K decode" in l]
     assert len([l for l in dec if "head_dim 64" in l]) == 1, lines  # three identical calls, one line
     assert any("per segment" in l for l in dec), lines  # the prefill call's one-row entries
-    assert any("varlen causal prefill" in l for l in lines), lines
+    assert any("mixed step in one launch" in l for l in lines), lines  # the default path of that call
     env["PAGEDATTN_LOG"] = "0"
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0 and "[pagedattn]" not in r.stderr

@@ -55,10 +55,54 @@ CASES = [
 ]
 
 
+PATHS = ["fused", "separate"]  # one persistent launch for decode rows + prefill tiles, or separate kernels
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("name,seq_lens,q_lens,hq,hkv,d,ps", CASES, ids=[c[0] for c in CASES])
-def test_prefill_matches_oracle(cuda_device, name, seq_lens, q_lens, hq, hkv, d, ps):
+def test_prefill_matches_oracle(cuda_device, monkeypatch, path, name, seq_lens, q_lens, hq, hkv, d, ps):
+    monkeypatch.setenv("PAGEDATTN_PREFILL_PATH", path)
     case = workloads.make_paged_case(name, seq_lens, q_lens, hq, hkv, d, page_size=ps, seed=len(name) * 7 + d)
     _check(case, cuda_device)
+
+
+@pytest.mark.parametrize("name,seq_lens,q_lens,hq,hkv,d,ps", [CASES[3], CASES[-3], CASES[-1]],
+                         ids=["ragged_many", "mixed_orders_g4", "mixed_orders_d64"])
+def test_fused_and_separate_paths_agree(cuda_device, monkeypatch, name, seq_lens, q_lens, hq, hkv, d, ps):
+    """Prefill rows are computed item by item the same way on both paths (bit-identical);
+    decode rows may be split differently (same result within rounding)."""
+    case = workloads.make_paged_case(name, seq_lens, q_lens, hq, hkv, d, page_size=ps, seed=len(name) * 7 + d)
+    g = case.to(cuda_device)
+    res = {}
+    for path in PATHS:
+        monkeypatch.setenv("PAGEDATTN_PREFILL_PATH", path)
+        res[path] = _prefill(g, cuda_device)
+    cu = case.cu_seqlens_q.tolist()
+    long_rows = [r for b, q in enumerate(case.q_lens_host) if q > 8 for r in range(cu[b], cu[b + 1])]
+    short_rows = [r for b, q in enumerate(case.q_lens_host) if q <= 8 for r in range(cu[b], cu[b + 1])]
+    (of, lf), (os_, ls) = res["fused"], res["separate"]
+    if long_rows:
+        lr = torch.tensor(long_rows, device=cuda_device)
+        assert torch.equal(of[lr].view(torch.int16), os_[lr].view(torch.int16))
+        assert torch.equal(lf[lr], ls[lr])
+    if short_rows:
+        sr = torch.tensor(short_rows, device=cuda_device)
+        d_ = (of[sr].float() - os_[sr].float()).abs()
+        assert bool((d_ <= 2e-2 + 2e-2 * os_[sr].float().abs()).all())
+        assert float((lf[sr] - ls[sr]).abs().max()) < 1e-3
+
+
+def test_fused_path_repeated_calls_bit_identical(cuda_device):
+    """The plan flag and item counter of the fused launch are tagged per launch and
+    reset after it: back-to-back calls (different inputs in between) stay exact."""
+    a = workloads.make_paged_case("rep_a", [900, 1, 3000, 400], [300, 1, 1, 400], 16, 4, 128, seed=70).to(cuda_device)
+    b = workloads.make_paged_case("rep_b", [2000, 77], [1000, 1], 16, 4, 128, seed=71).to(cuda_device)
+    oa1, la1 = _prefill(a, cuda_device)
+    ob1, lb1 = _prefill(b, cuda_device)
+    oa2, la2 = _prefill(a, cuda_device)
+    ob2, lb2 = _prefill(b, cuda_device)
+    assert torch.equal(oa1.view(torch.int16), oa2.view(torch.int16)) and torch.equal(la1, la2)
+    assert torch.equal(ob1.view(torch.int16), ob2.view(torch.int16)) and torch.equal(lb1, lb2)
 
 
 def test_prefill_sharp_logits(cuda_device):
@@ -187,11 +231,13 @@ def test_varlen_prefill_full_size_sampled(cuda_device):
 
 
 @pytest.mark.slow
-def test_mixed_step_full_size_sampled(cuda_device):
+@pytest.mark.parametrize("path", PATHS)
+def test_mixed_step_full_size_sampled(cuda_device, monkeypatch, path):
     """The mixed serving step in one call (4 prefill chunks of 2048 tokens after
     0..8192 cached tokens, 60 decodes of 1k..64k, one 131,072-token decode;
     Hq=32, Hkv=8): the chunk with the most prior tokens, the longest decode and
-    a mid-length decode against the oracle on 3 heads."""
+    a mid-length decode against the oracle on every head; both paths."""
+    monkeypatch.setenv("PAGEDATTN_PREFILL_PATH", path)
     case = workloads.mixed_step(device=cuda_device)
     out, lse = _prefill(case, cuda_device)
     assert torch.isfinite(out.float()).all()
