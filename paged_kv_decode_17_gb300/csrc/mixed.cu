@@ -183,6 +183,9 @@ int g_occ[64][2] = {};
 
 template <int D>
 int resident_ctas(int device) {
+    // the occupancy query needs the kernel's dynamic shared-memory limit raised first
+    if (set_smem_limit_once((const void*)mixed_kernel<D>, MCfg<D>::SMEM_BYTES, device, D == 128 ? 17 : 18) != PA_OK)
+        return 0;
     std::lock_guard<std::mutex> lk(g_occ_mu);
     if (device < 0 || device >= 64) return 0;
     int& v = g_occ[device][D == 128 ? 1 : 0];
