@@ -24,7 +24,8 @@
 //   this launch's grid ID.
 // * Phase 2, prefill: the prefill kernel's roles (softmax warps 0-7, producer 8,
 //   MMA issuers 9-10) on the same shared memory and tensor memory.  Work items are
-//   claimed one at a time from a counter tagged with the grid ID, so a CTA whose
+//   claimed one at a time by a fetch-and-add on a counter that the plan's builder
+//   set up (tagged with the grid ID) before publishing the plan, so a CTA whose
 //   decode range ended early takes more of the heaviest-first list: the ragged end
 //   of the decode phase fills with prefill work instead of idling.
 // * The merge of split decode rows is a second, small kernel launched as this
@@ -137,6 +138,7 @@ __device__ __forceinline__ void build_plan(const MixParams& mp, const int t, int
     plan_sync();
     if (t == 0) {
         __stcg(mp.n_tiles, total);
+        __stcg(mp.item_ctr, (unsigned long long)tag << 32);  // claims start at item 0 of this launch
         __threadfence();
         const unsigned long long v = ((unsigned long long)tag << 32) | 1ull;
         asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(mp.plan_flag), "l"(v) : "memory");

@@ -178,3 +178,23 @@ def test_fp8_subnormal_codes(cuda_device):
     assert np.abs(ref_out).max() > 0.1  # the subnormal values carry the output
     out, lse = _decode_fp8(case, kc, vc, ks, vs, cuda_device)
     assert_attention_close(out, ref_out, lse, ref_lse, what="fp8 subnormal codes")
+
+
+@pytest.mark.parametrize("ps", [16, 64])
+def test_fp8_bad_page_reports_status(cuda_device, ps):
+    """A block-table entry outside the pool is reported (PA_ERR_BAD_PAGE) and its unit
+    skipped, both when 16-token pages are staged by bulk copies (the stage's barrier
+    phase still completes) and when larger pages are staged per lane; the call ends."""
+    pa = _pa()
+    case = workloads.make_paged_case("fp8_bad", [900, 300], [1, 1], 8, 2, 128, page_size=ps, seed=97)
+    ks, vs = _scales(2, 13, 0.01), _scales(2, 14, 0.01)
+    kc, vc = _fp8_pools(case, ks, vs)
+    g = case.to(cuda_device)
+    g.block_table[0, 2] = 10 ** 6
+    g.block_table[1, 0] = -3
+    status = pa.new_status(cuda_device)
+    pa.attn_decode_paged_fp8(g.q, torch.from_numpy(kc).to(cuda_device), torch.from_numpy(vc).to(cuda_device),
+                             torch.from_numpy(ks).to(cuda_device), torch.from_numpy(vs).to(cuda_device),
+                             g.block_table, g.seq_lens, g.softmax_scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -6
