@@ -107,7 +107,6 @@ int prepare_decode(DecodeLaunch* L, void* out, float* lse, const void* q, const 
     prm.RS = bd.RS;
     prm.min_chunk = min_chunk;
     prm.reset_words = nullptr;
-    prm.fp8_bulk = (fp8 && page_size == UNIT) ? 1 : 0;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     prm.seg_base = reinterpret_cast<int32_t*>(ws + wl.hdr);
     prm.G = grid;

@@ -113,8 +113,6 @@ struct Params {
     int RS;       // rows per workspace slot (16 x the largest row-block count)
     int min_chunk;  // smallest chunk, in units (MIN_CHUNK unless overridden for tests)
     unsigned long long* reset_words;  // null, or 2 words the merge kernel zeroes once the decode grid is done
-    int fp8_bulk;  // FP8 pools with 16-token pages: a unit's K rows and its transposed V block are each one
-                   // contiguous 16 x D-byte block, staged by two bulk copies instead of per-lane copies
     float scale_log2;
 };
 
@@ -256,21 +254,9 @@ __device__ __forceinline__ int unit_page(const Params& p, UnitIter& it, int lane
 // Rows past the sequence end are not copied; their V rows are zeroed (their
 // slots may hold anything and 0 * NaN = NaN), their K rows are masked later.
 // Every call commits exactly one cp.async group (possibly empty).
-// One bulk copy (TMA engine, no tensor map) of `bytes` contiguous bytes global -> shared,
-// completion counted in bytes on `bar`.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                         uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
-            "r"(dst),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
-// bar: the stage's mbarrier when FP8 units are staged by bulk copies (p.fp8_bulk), else unused.
 template <int D, bool FP8, bool SWAP, bool APPEND>
 __device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, int phys, uint8_t* stage,
-                                           int* phys_slot, int lane, uint64_t policy, uint64_t* bar) {
+                                           int* phys_slot, int lane, uint64_t policy) {
     using C = Cfg<D, FP8, SWAP>;
     constexpr int CH = D / 8;  // 16-byte chunks per row (bf16)
     const int j = (it.u - it.seg.start) >> it.seg.sh.nrb_shift;  // key block within the sequence
@@ -281,7 +267,6 @@ __device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, 
         if (lane == 0) {
             report(p.status, PA_ERR_BAD_PAGE);
             *phys_slot = -1;
-            if (FP8 && p.fp8_bulk) mbar_arrive(bar);  // nothing to copy: complete the stage's phase
         }
     } else {
         if (lane == 0) *phys_slot = phys;
@@ -296,27 +281,16 @@ __device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, 
             const char* ksrc = reinterpret_cast<const char*>(p.k_pool) + row * D;
             const char* vsrc = reinterpret_cast<const char*>(p.v_pool) +
                                (size_t)(phys * p.Hkv + it.seg.g) * D * p.page_size + sub * UNIT;
-            if (p.fp8_bulk) {
-                // 16-token pages: K rows (16 x D bytes, unswizzled) and the transposed V block
-                // (D rows of 16 bytes) are each one contiguous block: two bulk copies by lane 0
-                if (lane == 0) {
-                    fence_proxy_async_smem();  // the lanes' earlier reads of this stage come first
-                    mbar_arrive_expect_tx(bar, 2 * C::UNIT_BYTES);
-                    bulk_g2s(sbase, ksrc, C::UNIT_BYTES, bar, policy);
-                    bulk_g2s(sbase + C::UNIT_BYTES, vsrc, C::UNIT_BYTES, bar, policy);
-                }
-            } else {
 #pragma unroll
-                for (int i = 0; i < NCH / 32; ++i) {
-                    const int q = i * 32 + lane;
-                    if (q < UNIT * KCH) {
-                        const int r = q / KCH, c = q - r * KCH;
-                        const int sw = D == 128 ? (r & 7) : 0;
-                        if (r < valid) cp_async_16(sbase + r * D + ((c ^ sw) << 4), ksrc + r * D + c * 16, policy);
-                    } else {
-                        const int d = q - UNIT * KCH;  // keys past the end are cleared when the values are read
-                        cp_async_16(sbase + C::UNIT_BYTES + d * 16, vsrc + (size_t)d * p.page_size, policy);
-                    }
+            for (int i = 0; i < NCH / 32; ++i) {
+                const int q = i * 32 + lane;
+                if (q < UNIT * KCH) {
+                    const int r = q / KCH, c = q - r * KCH;
+                    const int sw = D == 128 ? (r & 7) : 0;
+                    if (r < valid) cp_async_16(sbase + r * D + ((c ^ sw) << 4), ksrc + r * D + c * 16, policy);
+                } else {
+                    const int d = q - UNIT * KCH;  // keys past the end are cleared when the values are read
+                    cp_async_16(sbase + C::UNIT_BYTES + d * 16, vsrc + (size_t)d * p.page_size, policy);
                 }
             }
         } else {
@@ -462,7 +436,6 @@ struct DecShared {
     int s_phys[W][Cfg<D, FP8, SW == 1>::DEPTH];  // page of each staged unit (-1: bad entry)
     float s_m[W][RB], s_l[W][RB], s_M[RB], s_L[RB];
     int s_plan[8];
-    uint64_t stage_bar[W][Cfg<D, FP8, SW == 1>::DEPTH];  // FP8 bulk staging: one mbarrier per stage
 };
 
 // Barrier over the W warps of one (virtual) CTA.
@@ -494,13 +467,6 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
     auto& s_plan = ds.s_plan;
 
     const int warp = tid >> 5, lane = tid & 31;
-    if (FP8 && p.fp8_bulk) {  // each warp's stage barriers (used by that warp only)
-        if (lane == 0) {
-            for (int i = 0; i < DEPTH; ++i) mbar_init(&ds.stage_bar[warp][i], 1);
-            fence_mbar_init();
-        }
-        __syncwarp();
-    }
     // Launched as a programmatic dependent: until pdl_wait() below, the previous kernel
     // of the stream may still run (the writeback of the newest K/V rows lets its
     // dependents start at once).  Before the wait the kernel reads only seq_lens, cu_q
@@ -616,8 +582,7 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
     for (int i = 0; i < DEPTH; ++i) {
         if (!it.done) {
             const int phys = i == 0 ? phys0 : unit_page(p, it, lane);
-            issue_unit<D, FP8, SWAP, APPEND>(p, it, phys, my_stages + i * C::STAGE_BYTES, &s_phys[warp][i], lane, policy,
-                                             &ds.stage_bar[warp][i]);
+            issue_unit<D, FP8, SWAP, APPEND>(p, it, phys, my_stages + i * C::STAGE_BYTES, &s_phys[warp][i], lane, policy);
             it.u += W;
             it.norm(p, warp);
         } else {
@@ -704,12 +669,7 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
 
         for (int u = pa_ + warp; u < pe; u += W) {
             const int st = consumed % DEPTH;
-            if (FP8 && p.fp8_bulk) {
-                // this unit's two bulk copies (the phase of its stage's barrier)
-                if (!mbar_wait(&ds.stage_bar[warp][st], (consumed / DEPTH) & 1)) report(p.status, PA_ERR_TIMEOUT);
-            } else {
-                cp_async_wait_group<DEPTH - 1>();  // this unit's group (DEPTH - 1 younger ones may fly)
-            }
+            cp_async_wait_group<DEPTH - 1>();  // this unit's group (DEPTH - 1 younger ones may fly)
             __syncwarp();
             const int phys = s_phys[warp][st];
             uint8_t* sk = my_stages + st * C::STAGE_BYTES;
@@ -728,8 +688,7 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
 #pragma unroll
                     for (int m = 0; m < D / 64; ++m) {
                         const int c = (lane & 3) * (D / 64) + m;
-                        const bool swz = D == 128 && !p.fp8_bulk;  // bulk-staged K rows are not swizzled
-                        const int swa = swz ? (keyA & 7) : 0, swb = swz ? (keyB & 7) : 0;
+                        const int swa = D == 128 ? (keyA & 7) : 0, swb = D == 128 ? (keyB & 7) : 0;
                         asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                                      : "=r"(w0[4 * m]), "=r"(w0[4 * m + 1]), "=r"(w0[4 * m + 2]), "=r"(w0[4 * m + 3])
                                      : "r"(kb + keyA * D + ((c ^ swa) << 4)));
@@ -828,7 +787,7 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
 #pragma unroll
                         for (int m = 0; m < D / 64; ++m) {
                             const int c = (lane & 3) * (D / 64) + m;
-                            const int sw = (D == 128 && !p.fp8_bulk) ? (krow & 7) : 0;
+                            const int sw = D == 128 ? (krow & 7) : 0;
                             uint32_t r0, r1, r2, r3;
                             asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                                          : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -968,7 +927,7 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
             if (!it.done) {
                 const int phys_next = unit_page(p, it, lane);
                 issue_unit<D, FP8, SWAP, APPEND>(p, it, phys_next, my_stages + st * C::STAGE_BYTES,
-                                                 &s_phys[warp][st], lane, policy, &ds.stage_bar[warp][st]);
+                                                 &s_phys[warp][st], lane, policy);
                 it.u += W;
                 it.norm(p, warp);
             } else {

@@ -20,6 +20,9 @@
 //   rows and the prefill tiles (plus the merge of split decode rows), or the
 //   split-K decode, the plan and the prefill as separate kernels.  Both compute
 //   the same result; the tests run both.
+// * PAGEDATTN_PREFILL_PAIR=1|0 forces the stand-alone prefill kernel to run as
+//   CTA pairs (one M = 256 MMA per tile over two SMs; head_dim 128 only) or as
+//   single CTAs, whatever the head group; the tests use it to cover both.
 #pragma once
 
 #include <nvtx3/nvToolsExt.h>
@@ -80,6 +83,15 @@ inline unsigned long long prefill_wait_ns(unsigned long long dflt) {
     const long long n = std::strtoll(v, &end, 10);
     if (end == v || *end != '\0' || n < 1 || n > 60000000000ll) return dflt;
     return (unsigned long long)n;
+}
+
+// 1: CTA pairs, 2: single CTAs, 0: not set (the library's default).
+inline int prefill_pair_override() {
+    const char* v = std::getenv("PAGEDATTN_PREFILL_PAIR");
+    if (v == nullptr) return 0;
+    if (std::strcmp(v, "1") == 0) return 1;
+    if (std::strcmp(v, "0") == 0) return 2;
+    return 0;
 }
 
 // 1: one fused launch, 2: separate kernels, 0: not set (the library's default).

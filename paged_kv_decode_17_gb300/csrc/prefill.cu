@@ -65,42 +65,68 @@ extern "C" size_t pa_prefill_workspace_bytes(int batch, int total_q, int num_q_h
 }
 
 namespace {
-// CTAs of the prefill kernel that can be resident at once (queried once per device / head_dim).
+// CTAs of the prefill kernel that can be resident at once (queried once per device / variant).
 std::mutex g_occ_mu;
-int g_occ[64][2] = {};
+int g_occ[64][3] = {};
 
-template <int D>
-int max_ctas(int device) {
+template <int D, bool PAIR>
+int max_ctas(int device, cudaLaunchConfig_t cfg) {
     std::lock_guard<std::mutex> lk(g_occ_mu);
     if (device < 0 || device >= 64) return 0;
-    int& v = g_occ[device][D == 128 ? 1 : 0];
+    int& v = g_occ[device][PAIR ? 2 : (D == 128 ? 1 : 0)];
     if (v == 0) {
-        int per_sm = 0, sms = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pf::prefill_kernel<D>, pf::NTHREADS,
-                                                          pf::Cfg<D>::SMEM_BYTES) != cudaSuccess ||
-            per_sm <= 0)
-            return 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0) return 0;
-        v = per_sm * sms;
+        if (PAIR) {
+            int n = 0;
+            cfg.gridDim = dim3(2, 1, 1);
+            if (cudaOccupancyMaxActiveClusters(&n, pf::prefill_kernel<D, PAIR>, &cfg) != cudaSuccess || n <= 0)
+                return 0;
+            v = 2 * n;
+        } else {
+            int per_sm = 0, sms = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pf::prefill_kernel<D, PAIR>, pf::NTHREADS,
+                                                              pf::Cfg<D, PAIR>::SMEM_BYTES) != cudaSuccess ||
+                per_sm <= 0)
+                return 0;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0)
+                return 0;
+            v = per_sm * sms;
+        }
     }
     return v;
 }
 
-template <int D>
+template <int D, bool PAIR>
 int launch_persistent(cudaStream_t st, int device, long long items_upper, const CUtensorMap& qmap,
                       const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& omap,
                       const pf::Params& prm) {
-    if (set_smem_limit_once((const void*)pf::prefill_kernel<D>, pf::Cfg<D>::SMEM_BYTES, device, D == 128 ? 2 : 3) !=
-        PA_OK)
+    using C = pf::Cfg<D, PAIR>;
+    if (set_smem_limit_once((const void*)pf::prefill_kernel<D, PAIR>, C::SMEM_BYTES, device,
+                            PAIR ? 19 : (D == 128 ? 2 : 3)) != PA_OK)
         return PA_ERR_CUDA;
-    long long n = max_ctas<D>(device);
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(pf::NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = PAIR ? 1 : 0;
+    long long n = max_ctas<D, PAIR>(device, cfg);
     if (n <= 0) return PA_ERR_CUDA;
-    if (n > items_upper) n = items_upper;
-    log_config("varlen causal prefill: head_dim %d, persistent grid %lld CTAs x %d threads (1 per SM), "
-               "query tile %d rows x key tile %d, 2 heads per CTA, K ring %d / V ring %d stages, %d B smem",
-               D, n, pf::NTHREADS, pf::BM, pf::BN, pf::NK, pf::NV, pf::Cfg<D>::SMEM_BYTES);
-    pf::prefill_kernel<D><<<(unsigned)n, pf::NTHREADS, pf::Cfg<D>::SMEM_BYTES, st>>>(qmap, kmap, vmap, omap, prm);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    const long long units = PAIR ? 2 * items_upper : items_upper;  // a pair works on one item at a time
+    if (n > units) n = units;
+    if (PAIR) n &= ~1ll;
+    cfg.gridDim = dim3((unsigned)n, 1, 1);
+    log_config("varlen causal prefill: head_dim %d, persistent grid %lld CTAs x %d threads (1 per SM)%s, "
+               "query tile %d rows x key tile %d, %s, K ring %d / V ring %d stages, %d B smem",
+               D, n, pf::NTHREADS, PAIR ? " in CTA pairs (one M = 256 MMA per tile, cta_group::2)" : "",
+               pf::BM, pf::BN, PAIR ? "4 heads per pair" : "2 heads per CTA", C::NKr, C::NVr, C::SMEM_BYTES);
+    return cudaLaunchKernelEx(&cfg, pf::prefill_kernel<D, PAIR>, qmap, kmap, vmap, omap, prm) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 }  // namespace
 
@@ -144,9 +170,15 @@ extern "C" int attn_prefill_varlen_causal(void* out, float* lse, const void* q, 
                                   stream, /*per_segment=*/true);
 
     const int group = num_q_heads / num_kv_heads;
-    const int NPC = (group + 1) / 2;  // head pairs per KV head
+    // the stand-alone prefill runs as CTA pairs (4 heads per pair) where that wastes no more head
+    // slots than single CTAs (2 heads each) do: head_dim 128 and a group of 4k or 4k - 1 heads
+    const int pair_ovr = prefill_pair_override();
+    const bool pair = head_dim == 128 && (pair_ovr == 1 || (pair_ovr == 0 && group >= 3 && (group % 4 == 0 || group % 4 == 3)));
+    const int NPC = (group + 1) / 2;  // head pairs per KV head (single CTAs; the fused kernel)
+    const int NPC_PAIR = (group + 3) / 4;  // blocks of 4 heads per KV head (CTA pairs)
     const long long tiles_upper = (long long)(total_q + pf::BM - 1) / pf::BM + batch;
     const long long items_upper = tiles_upper * num_kv_heads * NPC;
+    const long long items_upper_pair = tiles_upper * num_kv_heads * NPC_PAIR;
 
     // plan: query tiles sorted by cost
     const pf::PlanArea plan = pf::plan_area(static_cast<uint8_t*>(workspace) + align_up(dec_bytes, 256));
@@ -198,6 +230,11 @@ extern "C" int attn_prefill_varlen_causal(void* out, float* lse, const void* q, 
     pf::prefill_plan_kernel<<<1, pf::PLAN_THREADS, plan_smem, st>>>(
         cu_seqlens_q, seq_lens, batch, max_pages_per_seq * page_size, max_cost, plan.tiles, plan.n_tiles, status);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-    if (head_dim == 128) return launch_persistent<128>(st, dev.device, items_upper, qmap, kmap, vmap, omap, prm);
-    return launch_persistent<64>(st, dev.device, items_upper, qmap, kmap, vmap, omap, prm);
+    if (pair) {
+        prm.NPC = NPC_PAIR;
+        return launch_persistent<128, true>(st, dev.device, items_upper_pair, qmap, kmap, vmap, omap, prm);
+    }
+    if (head_dim == 128)
+        return launch_persistent<128, false>(st, dev.device, items_upper, qmap, kmap, vmap, omap, prm);
+    return launch_persistent<64, false>(st, dev.device, items_upper, qmap, kmap, vmap, omap, prm);
 }

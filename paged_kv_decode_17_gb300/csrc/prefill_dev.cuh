@@ -64,7 +64,9 @@ constexpr int UPT = BN / 16; // 16-key page blocks per KV tile
 // current scores (S) to be computed, not for the previous P.V to finish.
 constexpr int NK = PA_PF_NK;  // K ring depth
 constexpr int NV = PA_PF_NV;  // V ring depth
-constexpr int NSTAGE = NK + NV;  // stages 0 .. NK-1 hold K tiles, NK .. NSTAGE-1 V tiles
+// CTA pairs (cta_group::2, below) stage half tiles, so deeper rings fit
+constexpr int PNK = 2, PNV = 3;
+constexpr int NSTAGE_MAX = PNK + PNV;  // stages 0 .. NK-1 hold K tiles, the next NV V tiles
 constexpr float TAU = 8.f;   // rescale threshold, log2 units
 // warps 0-7: softmax (head = warp / 4, row quarter = warp & 3)
 // warp 8: producer; warps 9 and 10: MMA issuers of head 0 and head 1
@@ -72,27 +74,39 @@ constexpr int NTHREADS = 352;
 constexpr int WARP_TMA = 8, WARP_MMA0 = 9;
 constexpr int PLAN_THREADS = 512;
 
-template <int D>
+// PAIR: a cluster of two CTAs on two SMs runs each tile as one M = 256 MMA
+// (cta_group::2): each CTA holds its own 128 query rows (two heads' Q and P), half of
+// every K tile (keys 0-63 in the first CTA, 64-127 in the second) and half of every V
+// tile (value columns 0-63 / 64-127); the MMA reads the other half from the peer's
+// shared memory, and each CTA's tensor memory receives its own rows' S and O.
+template <int D, bool PAIR = false>
 struct Cfg {
+    static_assert(!PAIR || D == 128, "a CTA pair splits V into two 128-byte column blocks");
     static constexpr int KB = D / 64;               // 128-byte column blocks per row
+    static constexpr int NKr = PAIR ? PNK : NK;     // ring depths
+    static constexpr int NVr = PAIR ? PNV : NV;
+    static constexpr int NST = NKr + NVr;
     static constexpr int Q_BYTES = BM * D * 2;      // one head's Q tile
-    static constexpr int KV_BYTES = BN * D * 2;     // one K or V tile
+    static constexpr int KV_BYTES = BN * D * 2 / (PAIR ? 2 : 1);  // one K or V stage
     static constexpr int P_BYTES = BM * BN * 2;     // one P tile
     static constexpr int Q_KB = BM * 128;           // bytes per column block of a Q tile
-    static constexpr int KV_KB = BN * 128;          // bytes per column block of a K/V tile
+    static constexpr int KV_KB = BN * 128;          // bytes per column block of a V stage (of a K stage, unpaired)
+    static constexpr int K_KB = (PAIR ? BN / 2 : BN) * 128;  // bytes per column block of a K stage
+    static constexpr int VKB = PAIR ? 1 : KB;       // column blocks per V stage
     static constexpr int P_KB = BM * 128;           // bytes per 64-key column block of a P tile
     static constexpr int OFF_Q = 0;                 // Q[head]
     static constexpr int OFF_P = 2 * Q_BYTES;       // P[head]
     static constexpr int OFF_KV = OFF_P + 2 * P_BYTES;
-    static constexpr int SMEM_BYTES = 1024 + OFF_KV + NSTAGE * KV_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + OFF_KV + NST * KV_BYTES;
     // TMEM columns: S[head] (BN fp32), O[head] (D fp32)
     static constexpr int TM_S0 = 0;
     static constexpr int TM_O0 = 2 * BN;
     static constexpr int TM_USED = 2 * BN + 2 * D;
     static constexpr int TM_COLS = TM_USED <= 256 ? 256 : 512;
     static_assert(TM_USED <= 512, "more than the 512 TMEM columns");
-    static constexpr uint32_t IDESC_S = tc::idesc_bf16(BM, BN, 0, 0);   // Q K-major, K K-major
-    static constexpr uint32_t IDESC_PV = tc::idesc_bf16(BM, D, 0, 1);   // P K-major, V MN-major
+    static constexpr int MM = PAIR ? 2 * BM : BM;   // rows of one MMA
+    static constexpr uint32_t IDESC_S = tc::idesc_bf16(MM, BN, 0, 0);   // Q K-major, K K-major
+    static constexpr uint32_t IDESC_PV = tc::idesc_bf16(MM, D, 0, 1);   // P K-major, V MN-major
 };
 
 struct Params {
@@ -106,7 +120,7 @@ struct Params {
     int32_t* status;
     int num_pages, max_pages, batch, page_size;
     int Hq, Hkv, group;
-    int NPC;  // head pairs per KV head
+    int NPC;  // head pairs (CTA pairs: blocks of 4 heads) per KV head
     unsigned long long wait_ns;  // limit of any one wait (kWaitTimeoutNs unless overridden for tests)
     float scale_log2;
 };
@@ -115,12 +129,15 @@ struct Params {
 struct Item {
     int end;  // 1: no more items
     int b, t, q_len, seq_len, row0, g, h0, nheads, n_kv, rows_valid, qmin;
+    int nstore;  // head slots whose results are stored (a CTA pair computes a last valid head twice)
+    int hmax;    // last query head of the KV group: slots past it compute it again
 };
 
 struct Shared {
     uint64_t bar_q[2], q_empty[2];  // per head: Q tile landed / Q tile no longer read
-    uint64_t kv_full[NSTAGE];
-    uint64_t kv_empty[NSTAGE];
+    uint64_t kv_full[NSTAGE_MAX];
+    uint64_t kv_empty[NSTAGE_MAX];
+    uint64_t v_peer[PNV];                // CTA pairs: the second CTA has cleared its rows of a V tile past the end
     uint64_t s_full[2], s_free[2];
     uint64_t p_ready[2], pv_done[2];
     uint64_t o_free[2];                  // per head: the epilogue has read O out of TMEM
@@ -133,6 +150,84 @@ struct Shared {
     int abort_flag;
     Item items[2];
 };
+
+// ---------------------------------------------------------------------------------- CTA pairs
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_cta(const void* local, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+    return a;
+}
+
+// Arrive (release, cluster scope) on an mbarrier given by its cluster address.
+__device__ __forceinline__ void arrive_cluster(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// TMA loads into this CTA's shared memory whose completion is counted on the first
+// CTA's barrier (cluster address `bar`).
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+namespace tc2 {  // tcgen05 for CTA pairs (a kernel uses one CTA group throughout)
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on the barrier at cluster address `bar` once this thread's MMAs are done.
+__device__ __forceinline__ void commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+}  // namespace tc2
+
+// Bounded wait that reports nothing (drains): true once the phase completed.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 <= limit_ns)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
 
 // Wait for phase `parity` of `bar`; false (and every other role falls through) once any
 // role of the CTA has waited longer than p.wait_ns, which records PA_ERR_TIMEOUT.
@@ -240,13 +335,18 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
 // One persistent CTA's prefill work: warps 0-7 softmax, 8 producer, 9-10 MMA; any
 // further warps only take part in the CTA-wide barriers.  smem: 1024-byte aligned,
 // Cfg<D>::SMEM_BYTES - 1024 bytes.
-template <int D>
+template <int D, bool PAIR = false>
 __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUtensorMap& kmap,
                                              const CUtensorMap& vmap, const CUtensorMap& omap, const Params& p,
                                              uint8_t* smem, Shared& sh, const ItemSource src) {
-    using C = Cfg<D>;
+    using C = Cfg<D, PAIR>;
+    constexpr int NKr = C::NKr, NVr = C::NVr;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    const uint32_t crank = PAIR ? cluster_rank() : 0u;  // 0: the CTA that issues the pair's MMAs
+    const bool lead = crank == 0;
+    // per-warp arrivals of the softmax warps (of both CTAs of a pair) on the MMA-side barriers
+    constexpr int SMX_ARRIVALS = PAIR ? 8 : 4;
 
     if (tid == 0) {
         sh.abort_flag = 0;
@@ -254,27 +354,34 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
             mbar_init(&sh.bar_q[h], 1);
             mbar_init(&sh.q_empty[h], 1);
             mbar_init(&sh.s_full[h], 1);
-            mbar_init(&sh.s_free[h], 4 * 32);
-            mbar_init(&sh.p_ready[h], 4 * 32);
+            mbar_init(&sh.s_free[h], SMX_ARRIVALS);
+            mbar_init(&sh.p_ready[h], SMX_ARRIVALS);
             mbar_init(&sh.pv_done[h], 1);
-            mbar_init(&sh.o_free[h], 4 * 32);
+            mbar_init(&sh.o_free[h], SMX_ARRIVALS);
             mbar_init(&sh.o_staged[h], 4 * 32);
             mbar_init(&sh.o_read[h], 1);
             mbar_init(&sh.item_full[h], 1);
             mbar_init(&sh.item_empty[h], 2 + 8);  // lane 0 of both MMA warps and of the 8 softmax warps
         }
-        for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(&sh.kv_full[s], 1);
+        for (int s = 0; s < C::NST; ++s) {
+            mbar_init(&sh.kv_full[s], 1);   // the (first CTA's) producer arms it for the whole tile
             mbar_init(&sh.kv_empty[s], 2);  // released by both MMA threads
         }
+        for (int s = 0; s < PNV; ++s) mbar_init(&sh.v_peer[s], 1);
         mbar_init(&sh.v_tail, 1);
         mbar_init(&sh.mma_drain, 2);
         fence_mbar_init();
     }
     __syncthreads();
+    if (PAIR) cluster_sync();  // both CTAs' barriers exist before either signals the other's
     if (warp == WARP_TMA) {
-        tc::tmem_alloc(&sh.tmem_base, C::TM_COLS);
-        tc::tmem_relinquish();
+        if (PAIR) {
+            tc2::tmem_alloc(&sh.tmem_base, C::TM_COLS);
+            tc2::tmem_relinquish();
+        } else {
+            tc::tmem_alloc(&sh.tmem_base, C::TM_COLS);
+            tc::tmem_relinquish();
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -311,11 +418,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
         int kring = 0, vring = 0;     // K / V tiles issued so far
         int tails = 0;                // v_tail phases waited for
         int tails_armed = 0;          // v_tail phases armed (copies issued)
-        bool v_open[NV] = {};         // V stage armed through v_tail, its kv_full arrival not yet made
+        bool v_open[NVr] = {};        // V stage armed through v_tail, its kv_full arrival not yet made
         int qloads[2] = {0, 0};       // Q tiles loaded per head
         for (int k = 0; ok; ++k) {
-            // ---- next item of this CTA
-            long long it = blockIdx.x + (long long)k * gridDim.x;
+            // ---- next item of this CTA (of this pair: both CTAs walk the same list)
+            long long it = PAIR ? (long long)(blockIdx.x >> 1) + (long long)k * (gridDim.x >> 1)
+                                : (long long)blockIdx.x + (long long)k * gridDim.x;
             if (src.counter != nullptr) {
                 long long c = n_items;
                 if (lane == 0 && ok) {
@@ -334,7 +442,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                 const int ti = (int)(it / per);
                 const int rem = (int)(it - (long long)ti * per);
                 itm.g = rem / p.NPC;
-                const int pair = rem - itm.g * p.NPC;
+                const int pair = rem - itm.g * p.NPC;  // (CTA pairs: block of 4 heads)
                 const int2 bt = __ldcg(p.tiles + ti);
                 itm.b = bt.x;
                 itm.t = bt.y;
@@ -342,8 +450,11 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                 itm.q_len = __ldg(p.cu_q + itm.b + 1) - c0;
                 itm.seq_len = __ldg(p.seq_lens + itm.b);
                 itm.row0 = c0 + itm.t * BM;
-                itm.h0 = itm.g * p.group + 2 * pair;
-                itm.nheads = max(0, min(2, p.group - 2 * pair));
+                const int hfirst = PAIR ? 4 * pair + 2 * (int)crank : 2 * pair;  // within the KV group
+                itm.h0 = itm.g * p.group + hfirst;
+                itm.nstore = max(0, min(2, p.group - hfirst));
+                itm.nheads = PAIR ? 2 : itm.nstore;  // a pair computes both slots (the MMA spans both CTAs)
+                itm.hmax = itm.g * p.group + p.group - 1;
                 itm.rows_valid = min(BM, itm.q_len - itm.t * BM);
                 itm.qmin = itm.seq_len - itm.q_len + itm.t * BM;
                 itm.n_kv = (itm.qmin + itm.rows_valid - 1) / BN + 1;
@@ -364,10 +475,20 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                                     wait_ab(&sh.q_empty[hh], (qloads[hh] - 1) & 1, sh, p));
                 if (!ok) break;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&sh.bar_q[hh], C::Q_BYTES);
-                    for (int kb = 0; kb < C::KB; ++kb)
-                        tma_load_3d(sQ + hh * C::Q_BYTES + kb * C::Q_KB, &qmap, &sh.bar_q[hh], kb * 64,
-                                    itm.h0 + hh, itm.row0);
+                    const int head = min(itm.h0 + hh, itm.hmax);
+                    if (!PAIR) {
+                        mbar_arrive_expect_tx(&sh.bar_q[hh], C::Q_BYTES);
+                        for (int kb = 0; kb < C::KB; ++kb)
+                            tma_load_3d(sQ + hh * C::Q_BYTES + kb * C::Q_KB, &qmap, &sh.bar_q[hh], kb * 64, head,
+                                        itm.row0);
+                    } else {
+                        // both CTAs' Q tiles land on the first CTA's barrier, armed there for both
+                        if (lead) mbar_arrive_expect_tx(&sh.bar_q[hh], 2 * C::Q_BYTES);
+                        const uint32_t bq = map_cta(&sh.bar_q[hh], 0);
+                        for (int kb = 0; kb < C::KB; ++kb)
+                            tma_load_3d_pair(sQ + hh * C::Q_BYTES + kb * C::Q_KB, &qmap, bq, kb * 64, head,
+                                             itm.row0);
+                    }
                 }
                 ++qloads[hh];
             }
@@ -398,13 +519,11 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                 next_row = block_row(j + 1);
                 const unsigned goodmask = __ballot_sync(0xffffffffu, my_row >= 0) & ((1u << UPT) - 1);
                 const int good = __popc(goodmask);
-                const int box_row = __shfl_sync(0xffffffffu, my_row, (lane / C::KB) % UPT);
-                const bool mine = lane < UPT * C::KB && box_row >= 0;
                 const bool tail = (j + 1) * BN > itm.seq_len;
                 for (int x = 0; x < 2 && ok; ++x) {
                     const int i = x == 0 ? kring : vring;
-                    const int depth = x == 0 ? NK : NV;
-                    const int st = (x == 0 ? 0 : NK) + i % depth;
+                    const int depth = x == 0 ? NKr : NVr;
+                    const int st = (x == 0 ? 0 : NKr) + i % depth;
                     ok = __all_sync(0xffffffffu,
                                     wait_ab(&sh.kv_empty[st], ((i / depth) & 1) ^ 1, sh, p));
                     if (!ok) break;
@@ -413,42 +532,81 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                     else
                         ++vring;
                     uint8_t* dst = sKV + st * C::KV_BYTES;
+                    // this lane's box: page block u, 64-column block kb, and its place in the stage.
+                    // Unpaired: all UPT x KB boxes.  Pair: K keys 64 r .. 64 r + 63 (blocks 4 r .. 4 r + 3,
+                    // both column blocks), V columns 64 r .. 64 r + 63 of every block.
+                    int u, kb, off;
+                    bool has;
+                    if (!PAIR) {
+                        u = lane / C::KB;
+                        kb = lane - u * C::KB;
+                        has = lane < UPT * C::KB;
+                        off = kb * C::KV_KB + u * 2048;
+                    } else if (x == 0) {
+                        u = 4 * (int)crank + (lane >> 1);
+                        kb = lane & 1;
+                        has = lane < 8;
+                        off = kb * C::K_KB + (lane >> 1) * 2048;
+                    } else {
+                        u = lane;
+                        kb = (int)crank;
+                        has = lane < UPT;
+                        off = u * 2048;
+                    }
+                    const int box_row = __shfl_sync(0xffffffffu, my_row, u & 31);
+                    const bool mine = has && box_row >= 0;
                     const bool via_tail = (x == 1) && tail;
-                    uint64_t* land = via_tail ? &sh.v_tail : &sh.kv_full[st];
-                    if (lane == 0) {
-                        if (good == 0)
-                            mbar_arrive(land);
-                        else
-                            mbar_arrive_expect_tx(land, good * 16 * D * 2);  // the whole tile
-                    }
-                    __syncwarp();
-                    if (mine) {
-                        const int u = lane / C::KB, kb = lane - u * C::KB;
-                        uint8_t* bdst = dst + kb * C::KV_KB + u * 2048;
-                        const CUtensorMap* map = x == 0 ? &kmap : &vmap;
-                        tma_load_2d(bdst, map, land, kb * 64, box_row);
-                    }
-                    if (via_tail) {
-                        ++tails_armed;
-                        v_open[st - NK] = true;
+                    const CUtensorMap* map = x == 0 ? &kmap : &vmap;
+                    if (!via_tail) {
+                        if (lane == 0 && lead) {  // armed for the whole tile (both CTAs of a pair)
+                            if (good == 0)
+                                mbar_arrive(&sh.kv_full[st]);
+                            else
+                                mbar_arrive_expect_tx(&sh.kv_full[st], good * 16 * D * 2);
+                        }
+                        __syncwarp();
+                        if (mine) {
+                            if (PAIR)
+                                tma_load_2d_pair(dst + off, map, map_cta(&sh.kv_full[st], 0), kb * 64, box_row);
+                            else
+                                tma_load_2d(dst + off, map, &sh.kv_full[st], kb * 64, box_row);
+                        }
+                    } else {
                         // keys past the sequence end: their V rows may hold anything and 0 * NaN = NaN,
-                        // so zero them before any MMA may read this tile
+                        // so this CTA's copies land on v_tail and it zeroes those rows of its columns
+                        // before it lets any MMA read the tile
+                        const int own_bytes = good * 16 * 128 * C::VKB;
+                        if (lane == 0) {
+                            if (own_bytes == 0)
+                                mbar_arrive(&sh.v_tail);
+                            else
+                                mbar_arrive_expect_tx(&sh.v_tail, own_bytes);
+                        }
+                        __syncwarp();
+                        if (mine) tma_load_2d(dst + off, map, &sh.v_tail, kb * 64, box_row);
+                        ++tails_armed;
+                        v_open[st - NKr] = true;
                         ok = __all_sync(0xffffffffu, wait_ab(&sh.v_tail, tails & 1, sh, p));
                         if (!ok) break;
                         ++tails;
                         const int first = itm.seq_len - j * BN;
-                        const int nchunk = (BN - first) * 8 * C::KB;  // 16-byte chunks to clear
+                        const int nchunk = (BN - first) * 8 * C::VKB;  // 16-byte chunks to clear
                         for (int c = lane; c < nchunk; c += 32) {
-                            const int kb = c / ((BN - first) * 8);
-                            const int rem = c - kb * (BN - first) * 8;
+                            const int cb = c / ((BN - first) * 8);
+                            const int rem = c - cb * (BN - first) * 8;
                             const int r = first + rem / 8;
-                            *reinterpret_cast<uint4*>(dst + kb * C::KV_KB + r * 128 + (rem & 7) * 16) =
+                            *reinterpret_cast<uint4*>(dst + cb * C::KV_KB + r * 128 + (rem & 7) * 16) =
                                 make_uint4(0, 0, 0, 0);
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&sh.kv_full[st]);
-                        v_open[st - NK] = false;
+                        if (lane == 0) {
+                            if (lead)
+                                mbar_arrive(&sh.kv_full[st]);
+                            else
+                                arrive_cluster(map_cta(&sh.v_peer[st - NKr], 0));
+                        }
+                        v_open[st - NKr] = false;
                     }
                 }
             }
@@ -456,33 +614,68 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
         // Before leaving (also after an abort): every TMA copy issued into this CTA has
         // landed.  Older tiles of a stage were consumed before the stage was re-armed, so
         // only the last tile of each stage can still be in flight; a V tile armed through
-        // v_tail whose kv_full arrival was never made lands on v_tail.
+        // v_tail whose kv_full arrival was never made lands on v_tail.  In a pair the
+        // second CTA's copies land on the first CTA's barriers: the first CTA waits for
+        // what it armed (after an abort a phase may lack copies the peer never issued,
+        // hence the short limit), and copies the peer issued for a phase the first CTA
+        // never armed are covered at the very end (both CTAs wait out any copy in flight
+        // when either of them aborted).
         if (lane == 0) {
-            for (int hh = 0; hh < 2; ++hh)
-                if (qloads[hh] > 0) mbar_wait(&sh.bar_q[hh], (qloads[hh] - 1) & 1);
-            for (int i = max(0, kring - NK); i < kring; ++i) mbar_wait(&sh.kv_full[i % NK], (i / NK) & 1);
-            for (int i = max(0, vring - NV); i < vring; ++i)
-                if (!v_open[i % NV]) mbar_wait(&sh.kv_full[NK + i % NV], (i / NV) & 1);
+            if (lead) {
+                const uint64_t lim = PAIR ? 5000000ull : kWaitTimeoutNs;
+                for (int hh = 0; hh < 2; ++hh)
+                    if (qloads[hh] > 0) mbar_wait_for(&sh.bar_q[hh], (qloads[hh] - 1) & 1, lim);
+                for (int i = max(0, kring - NKr); i < kring; ++i)
+                    mbar_wait_for(&sh.kv_full[i % NKr], (i / NKr) & 1, lim);
+                for (int i = max(0, vring - NVr); i < vring; ++i)
+                    if (!v_open[i % NVr]) mbar_wait_for(&sh.kv_full[NKr + i % NVr], (i / NVr) & 1, lim);
+            }
             if (tails_armed > tails) mbar_wait(&sh.v_tail, (tails_armed - 1) & 1);
         }
         __syncwarp();
     } else if (warp == WARP_MMA0 || warp == WARP_MMA0 + 1) {
         // ===================================================== MMA issuer of one head
         const int hh = warp - WARP_MMA0;
-        if (lane == 0) {
+        if (PAIR && !lead) {
+            // the second CTA of a pair issues no MMA (the first CTA's M = 256 MMAs cover its rows):
+            // it only follows the item ring
+            if (lane == 0)
+                for (int k = 0;; ++k) {
+                    if (!wait_ab(&sh.item_full[k & 1], (k >> 1) & 1, sh, p)) break;
+                    const bool end = sh.items[k & 1].end != 0;
+                    mbar_arrive(&sh.item_empty[k & 1]);
+                    if (end) break;
+                }
+        } else if (lane == 0) {
             const uint32_t qaddr = smem_u32(sQ) + hh * C::Q_BYTES;
             const uint32_t paddr = smem_u32(sP) + hh * C::P_BYTES;
             const uint32_t kv_base = smem_u32(sKV);
             const uint32_t t_s = tmem + C::TM_S0 + hh * BN;
             const uint32_t t_o = tmem + C::TM_O0 + hh * D;
+            // completion of this thread's MMAs signalled on a barrier (of both CTAs of a pair)
+            auto commit_to = [&](uint64_t* bar) {
+                if (PAIR) {
+                    tc2::commit(map_cta(bar, 0));
+                    tc2::commit(map_cta(bar, 1));
+                } else {
+                    tc::commit(bar);
+                }
+            };
+            auto mma = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+                if (PAIR)
+                    tc2::mma_ss(d, a, b, idesc, acc);
+                else
+                    tc::mma_ss(d, a, b, idesc, acc);
+            };
             // a K/V stage is free once both MMA threads are done with it
-            auto release = [&](uint64_t* bar) { tc::commit(bar); };
+            auto release = [&](uint64_t* bar) { commit_to(bar); };
             int kr = 0, vr = 0;  // K / V ring positions (same walk as the producer)
+            int vtails[PNV] = {};  // pair: V tiles past the end seen per stage (phases of v_peer)
             // stage and phase of the K / V tile of key tile j of the current item
-            auto kst = [&](int j) { return (kr + j) % NK; };
-            auto kph = [&](int j) { return (uint32_t)(((kr + j) / NK) & 1); };
-            auto vst = [&](int j) { return NK + (vr + j) % NV; };
-            auto vph = [&](int j) { return (uint32_t)(((vr + j) / NV) & 1); };
+            auto kst = [&](int j) { return (kr + j) % NKr; };
+            auto kph = [&](int j) { return (uint32_t)(((kr + j) / NKr) & 1); };
+            auto vst = [&](int j) { return NKr + (vr + j) % NVr; };
+            auto vph = [&](int j) { return (uint32_t)(((vr + j) / NVr) & 1); };
             int J = 0;      // tiles this head has computed (phase counter of its S / P barriers)
             int items = 0;  // items this head has computed
             int qn = 0;     // Q tiles consumed
@@ -511,11 +704,11 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                             const uint64_t ad =
                                 tc::smem_desc_sw128(qaddr + (kk >> 2) * C::Q_KB + (kk & 3) * 32, 16, 1024);
                             const uint64_t bd =
-                                tc::smem_desc_sw128(kaddr + (kk >> 2) * C::KV_KB + (kk & 3) * 32, 16, 1024);
-                            tc::mma_ss(t_s, ad, bd, C::IDESC_S, kk > 0);
+                                tc::smem_desc_sw128(kaddr + (kk >> 2) * C::K_KB + (kk & 3) * 32, 16, 1024);
+                            mma(t_s, ad, bd, C::IDESC_S, kk > 0);
                         }
-                        tc::commit(&sh.s_full[hh]);
-                        if (j == n - 1) tc::commit(&sh.q_empty[hh]);  // last read of this Q tile
+                        commit_to(&sh.s_full[hh]);
+                        if (j == n - 1) commit_to(&sh.q_empty[hh]);  // last read of this Q tile
                     };
                     auto issue_pv = [&](int j) {
                         const uint32_t vaddr = kv_base + vst(j) * C::KV_BYTES;
@@ -524,9 +717,9 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                             const uint64_t ad =
                                 tc::smem_desc_sw128(paddr + (kk >> 2) * C::P_KB + (kk & 3) * 32, 16, 1024);
                             const uint64_t bd = tc::smem_desc_sw128(vaddr + kk * 2048, C::KV_KB, 1024);
-                            tc::mma_ss(t_o, ad, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                            mma(t_o, ad, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
                         }
-                        tc::commit(&sh.pv_done[hh]);
+                        commit_to(&sh.pv_done[hh]);
                     };
                     // scores of key tile 0 (the S buffer was freed by the previous tile's softmax)
                     if (ok) ok = wait_ab(&sh.kv_full[kst(0)], kph(0), sh, p);
@@ -548,6 +741,11 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                         }
                         ok = wait_ab(&sh.kv_full[vst(j)], vph(j), sh, p) &&
                              wait_ab(&sh.p_ready[hh], (J + j) & 1, sh, p);
+                        if (PAIR && ok && (j + 1) * BN > itm.seq_len) {  // the peer zeroed its rows past the end
+                            const int vs = vst(j) - NKr;
+                            ok = wait_ab(&sh.v_peer[vs], vtails[vs] & 1, sh, p);
+                            ++vtails[vs];
+                        }
                         // the first P.V overwrites O: the previous item's epilogue must have read it
                         if (ok && j == 0 && items > 0) ok = wait_ab(&sh.o_free[hh], (items - 1) & 1, sh, p);
                         if (!ok) break;
@@ -564,7 +762,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
             }
             // every tensor-core operation this thread issued has completed (after an abort some
             // may still run) before the CTA frees tensor memory and leaves
-            tc::commit(&sh.mma_drain);
+            if (PAIR)
+                tc2::commit(map_cta(&sh.mma_drain, 0));
+            else
+                tc::commit(&sh.mma_drain);
             mbar_wait(&sh.mma_drain, 0);
         }
         __syncwarp();
@@ -577,6 +778,17 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
         const uint32_t t_s = tmem + lane_off + C::TM_S0 + hh * BN;
         const uint32_t t_o = tmem + lane_off + C::TM_O0 + hh * D;
         uint8_t* prow = sP + hh * C::P_BYTES + r * 128;
+        // one arrival per warp (after every lane's accesses) on a barrier of the MMA side:
+        // in a pair, the first CTA's barrier counts both CTAs' warps
+        auto smx_arrive = [&](uint64_t* bar) {
+            __syncwarp();
+            if (lane == 0) {
+                if (PAIR)
+                    arrive_cluster(map_cta(bar, 0));
+                else
+                    mbar_arrive(bar);
+            }
+        };
         const bool leader = quarter == 0 && lane == 0;
         int J = 0;  // tiles of this head so far (phase counter, shared with the MMA thread)
         int nst = 0;               // O tiles written out through the P buffer by TMA stores
@@ -607,7 +819,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                     }
                     tc::wait_ld();
                     tc::fence_before_sync();
-                    mbar_arrive(&sh.s_free[hh]);
+                    smx_arrive(&sh.s_free[hh]);
                     if ((j + 1) * BN - 1 > itm.qmin) {  // diagonal tile: some key is after some row
 #pragma unroll
                         for (int c = 0; c < BN; ++c)
@@ -690,7 +902,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                     l += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
                     fence_proxy_async_smem();
                     tc::fence_before_sync();
-                    mbar_arrive(&sh.p_ready[hh]);
+                    smx_arrive(&sh.p_ready[hh]);
                 }
                 // ---- epilogue: O / l -> bf16, then hand O back to the MMA thread
                 if (ok)
@@ -698,9 +910,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                 if (ok) {
                     tc::fence_after_sync();
                     const float inv = l > 0.f ? 1.f / l : 0.f;
-                    const bool store = r < itm.rows_valid;
-                    const int h = itm.h0 + hh;
-                    if (itm.rows_valid == BM) {
+                    // a pair may compute the KV group's last head in two slots: one copy is stored
+                    const bool keep = hh < itm.nstore;
+                    const bool store = keep && r < itm.rows_valid;
+                    const int h = min(itm.h0 + hh, itm.hmax);
+                    if (!keep) {
+                    } else if (itm.rows_valid == BM) {
                         // full tile: O/l -> bf16 into the P buffer (free: the last P.V is done) in the
                         // swizzled layout of a 64-column TMA box, then one thread stores it with TMA
 #pragma unroll 1
@@ -756,7 +971,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                     if (store && p.lse != nullptr)
                         p.lse[(size_t)(itm.row0 + r) * p.Hq + h] = l > 0.f ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
                     tc::fence_before_sync();
-                    mbar_arrive(&sh.o_free[hh]);
+                    smx_arrive(&sh.o_free[hh]);
                 }
                 J += n;
             }
@@ -768,11 +983,32 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
 
     tc::fence_before_sync();
     __syncthreads();
+    if (PAIR) {
+        cluster_sync();  // every role of both CTAs is done
+        if (tid == 0) {
+            // after an abort in either CTA, a TMA copy may still be landing in this CTA's shared
+            // memory (issued for a phase the first CTA never armed): wait it out
+            uint32_t peer_abort;
+            asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(peer_abort) : "r"(map_cta(&sh.abort_flag, crank ^ 1u)));
+            if (peer_abort != 0 || *reinterpret_cast<volatile int*>(&sh.abort_flag) != 0) {
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 200000ull) {
+                }
+            }
+        }
+        cluster_sync();  // neither CTA leaves while the other may still read its flag
+    }
     tc::fence_after_sync();
-    if (warp == WARP_TMA) tc::tmem_dealloc(tmem, C::TM_COLS);
+    if (warp == WARP_TMA) {
+        if (PAIR)
+            tc2::tmem_dealloc(tmem, C::TM_COLS);
+        else
+            tc::tmem_dealloc(tmem, C::TM_COLS);
+    }
 }
 
-template <int D>
+// PAIR: launched in clusters of two CTAs (the pair), gridDim.x even.
+template <int D, bool PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
@@ -780,7 +1016,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ Shared sh;
-    prefill_body<D>(qmap, kmap, vmap, omap, p, smem, sh, ItemSource{nullptr, nullptr, 0u});
+    prefill_body<D, PAIR>(qmap, kmap, vmap, omap, p, smem, sh, ItemSource{nullptr, nullptr, 0u});
 }
 
 // Plan area of the workspace (after the decode part):

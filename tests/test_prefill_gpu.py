@@ -58,12 +58,45 @@ CASES = [
 PATHS = ["fused", "separate"]  # one persistent launch for decode rows + prefill tiles, or separate kernels
 
 
-@pytest.mark.parametrize("path", PATHS)
+def _set_path(monkeypatch, path):
+    """fused / separate (the stand-alone prefill choosing CTA pairs or single CTAs by head
+    group) / pairs (stand-alone prefill forced to CTA pairs, head_dim 128) / singles."""
+    monkeypatch.setenv("PAGEDATTN_PREFILL_PATH", "fused" if path == "fused" else "separate")
+    if path == "pairs":
+        monkeypatch.setenv("PAGEDATTN_PREFILL_PAIR", "1")
+    elif path == "singles":
+        monkeypatch.setenv("PAGEDATTN_PREFILL_PAIR", "0")
+    else:
+        monkeypatch.delenv("PAGEDATTN_PREFILL_PAIR", raising=False)
+
+
+@pytest.mark.parametrize("path", PATHS + ["pairs", "singles"])
 @pytest.mark.parametrize("name,seq_lens,q_lens,hq,hkv,d,ps", CASES, ids=[c[0] for c in CASES])
 def test_prefill_matches_oracle(cuda_device, monkeypatch, path, name, seq_lens, q_lens, hq, hkv, d, ps):
-    monkeypatch.setenv("PAGEDATTN_PREFILL_PATH", path)
+    _set_path(monkeypatch, path)
     case = workloads.make_paged_case(name, seq_lens, q_lens, hq, hkv, d, page_size=ps, seed=len(name) * 7 + d)
     _check(case, cuda_device)
+
+
+@pytest.mark.parametrize("name,seq_lens,q_lens,hq,hkv,d,ps", [c for c in CASES if c[5] == 128],
+                         ids=[c[0] for c in CASES if c[5] == 128])
+def test_pairs_and_singles_bit_identical(cuda_device, monkeypatch, name, seq_lens, q_lens, hq, hkv, d, ps):
+    """A CTA pair computes each tile's S = Q K^T and O += P V as one M = 256 MMA over two
+    SMs, but every row sees the same keys in the same order and the same softmax: the
+    prefill rows come out bit-identical to single CTAs'."""
+    case = workloads.make_paged_case(name, seq_lens, q_lens, hq, hkv, d, page_size=ps, seed=len(name) * 7 + d)
+    g = case.to(cuda_device)
+    res = {}
+    for path in ("pairs", "singles"):
+        _set_path(monkeypatch, path)
+        res[path] = _prefill(g, cuda_device)
+    cu = case.cu_seqlens_q.tolist()
+    rows = [r for b, q in enumerate(case.q_lens_host) if q > 8 for r in range(cu[b], cu[b + 1])]
+    if rows:
+        ri = torch.tensor(rows, device=cuda_device)
+        (op, lp), (os_, ls) = res["pairs"], res["singles"]
+        assert torch.equal(op[ri].view(torch.int16), os_[ri].view(torch.int16))
+        assert torch.equal(lp[ri], ls[ri])
 
 
 @pytest.mark.parametrize("name,seq_lens,q_lens,hq,hkv,d,ps", [CASES[3], CASES[-3], CASES[-1]],
@@ -187,7 +220,8 @@ def test_prefill_bad_page_reports_status(cuda_device):
     assert int(status.item()) == -6
 
 
-def test_wait_timeout_reports_status_and_context_survives(cuda_device, monkeypatch):
+@pytest.mark.parametrize("path", ["fused", "pairs", "singles"])
+def test_wait_timeout_reports_status_and_context_survives(cuda_device, monkeypatch, path):
     """With the prefill's wait limit cut to 1 ns (PAGEDATTN_PREFILL_WAIT_NS), waits
     run out: the call returns, the status word holds PA_ERR_TIMEOUT (-5), every
     CTA drains its copies and tensor-core work and exits, and the next call with
@@ -196,6 +230,7 @@ def test_wait_timeout_reports_status_and_context_survives(cuda_device, monkeypat
     pa = _pa()
     case = workloads.make_paged_case("timeout", [3000, 2000, 1000, 600], [3000, 2000, 1000, 300], 8, 2, 128, seed=66)
     g = case.to(cuda_device)
+    _set_path(monkeypatch, path)
     monkeypatch.setenv("PAGEDATTN_PREFILL_WAIT_NS", "1")
     status = pa.new_status(cuda_device)
     t0 = time.time()
@@ -209,10 +244,12 @@ def test_wait_timeout_reports_status_and_context_survives(cuda_device, monkeypat
 
 
 @pytest.mark.slow
-def test_varlen_prefill_full_size_sampled(cuda_device):
+@pytest.mark.parametrize("path", PATHS)
+def test_varlen_prefill_full_size_sampled(cuda_device, monkeypatch, path):  # separate: CTA pairs (group 7)
     """16 sequences of 512..4096 tokens, Hq=28, Hkv=4: writeback then prefill;
-    the shortest and the longest sequence checked against the oracle on 3 heads."""
+    the shortest and the longest sequence checked against the oracle on every head."""
     pa = _pa()
+    _set_path(monkeypatch, path)
     case = workloads.varlen_prefill(device=cuda_device)
     lens = case.seq_lens_host
     seqs = [int(np.argmin(lens)), int(np.argmax(lens))]
@@ -232,7 +269,7 @@ def test_varlen_prefill_full_size_sampled(cuda_device):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("path", PATHS)
-def test_mixed_step_full_size_sampled(cuda_device, monkeypatch, path):
+def test_mixed_step_full_size_sampled(cuda_device, monkeypatch, path):  # separate: CTA pairs (group 4)
     """The mixed serving step in one call (4 prefill chunks of 2048 tokens after
     0..8192 cached tokens, 60 decodes of 1k..64k, one 131,072-token decode;
     Hq=32, Hkv=8): the chunk with the most prior tokens, the longest decode and
