@@ -20,9 +20,9 @@
 //   rows and the prefill tiles (plus the merge of split decode rows), or the
 //   split-K decode, the plan and the prefill as separate kernels.  Both compute
 //   the same result; the tests run both.
-// * PAGEDATTN_PREFILL_PAIR=1|0 forces the stand-alone prefill kernel to run as
-//   CTA pairs (one M = 256 MMA per tile over two SMs; head_dim 128 only) or as
-//   single CTAs, whatever the head group; the tests use it to cover both.
+// * PAGEDATTN_PREFILL_PAIR=1 runs the stand-alone prefill kernel as CTA pairs
+//   (one M = 256 MMA per tile over two SMs; head_dim 128 only) instead of
+//   single CTAs (the default, measured faster); the tests cover both.
 #pragma once
 
 #include <nvtx3/nvToolsExt.h>

@@ -170,10 +170,11 @@ extern "C" int attn_prefill_varlen_causal(void* out, float* lse, const void* q, 
                                   stream, /*per_segment=*/true);
 
     const int group = num_q_heads / num_kv_heads;
-    // the stand-alone prefill runs as CTA pairs (4 heads per pair) where that wastes no more head
-    // slots than single CTAs (2 heads each) do: head_dim 128 and a group of 4k or 4k - 1 heads
-    const int pair_ovr = prefill_pair_override();
-    const bool pair = head_dim == 128 && (pair_ovr == 1 || (pair_ovr == 0 && group >= 3 && (group % 4 == 0 || group % 4 == 3)));
+    // CTA pairs (one M = 256 MMA per tile over two SMs) only when asked for: measured on the
+    // 16 x 512..4096-token prefill (Hq 28, Hkv 4) they took 1.11 ms against 0.74 ms for single
+    // CTAs -- every tile's softmax / MMA hand-over (scores freed, P ready, MMA done) then
+    // crosses SMs, and with one S and one P buffer per head that latency is on the critical path
+    const bool pair = head_dim == 128 && prefill_pair_override() == 1;
     const int NPC = (group + 1) / 2;  // head pairs per KV head (single CTAs; the fused kernel)
     const int NPC_PAIR = (group + 3) / 4;  // blocks of 4 heads per KV head (CTA pairs)
     const long long tiles_upper = (long long)(total_q + pf::BM - 1) / pf::BM + batch;

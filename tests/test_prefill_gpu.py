@@ -59,8 +59,8 @@ PATHS = ["fused", "separate"]  # one persistent launch for decode rows + prefill
 
 
 def _set_path(monkeypatch, path):
-    """fused / separate (the stand-alone prefill choosing CTA pairs or single CTAs by head
-    group) / pairs (stand-alone prefill forced to CTA pairs, head_dim 128) / singles."""
+    """fused / separate (stand-alone prefill, single CTAs by default) / pairs (stand-alone
+    prefill as CTA pairs, head_dim 128) / singles (stand-alone prefill, single CTAs)."""
     monkeypatch.setenv("PAGEDATTN_PREFILL_PATH", "fused" if path == "fused" else "separate")
     if path == "pairs":
         monkeypatch.setenv("PAGEDATTN_PREFILL_PAIR", "1")
@@ -245,7 +245,7 @@ def test_wait_timeout_reports_status_and_context_survives(cuda_device, monkeypat
 
 @pytest.mark.slow
 @pytest.mark.parametrize("path", PATHS)
-def test_varlen_prefill_full_size_sampled(cuda_device, monkeypatch, path):  # separate: CTA pairs (group 7)
+def test_varlen_prefill_full_size_sampled(cuda_device, monkeypatch, path):
     """16 sequences of 512..4096 tokens, Hq=28, Hkv=4: writeback then prefill;
     the shortest and the longest sequence checked against the oracle on every head."""
     pa = _pa()
@@ -269,7 +269,7 @@ def test_varlen_prefill_full_size_sampled(cuda_device, monkeypatch, path):  # se
 
 @pytest.mark.slow
 @pytest.mark.parametrize("path", PATHS)
-def test_mixed_step_full_size_sampled(cuda_device, monkeypatch, path):  # separate: CTA pairs (group 4)
+def test_mixed_step_full_size_sampled(cuda_device, monkeypatch, path):
     """The mixed serving step in one call (4 prefill chunks of 2048 tokens after
     0..8192 cached tokens, 60 decodes of 1k..64k, one 131,072-token decode;
     Hq=32, Hkv=8): the chunk with the most prior tokens, the longest decode and
