@@ -573,12 +573,12 @@ def measure_rope_writeback(pa, steps, warmup, peaks):
     return res
 
 
-def measure_mixed(pa, steps, warmup, peaks):
+def measure_mixed(pa, steps, warmup, peaks, small=False):
     """Mixed serving step in one call: 4 prefill chunks of 2048 tokens after
     0..8192 cached tokens + 60 decodes (1k..64k context) + one 131,072-token
     decode; Hq=32, Hkv=8, D=128.  Inputs (about 9 GB of KV) exceed L2."""
     dev = torch.device("cuda", torch.cuda.current_device())
-    case = workloads.mixed_step(device=dev)
+    case = (workloads.mixed_step_small if small else workloads.mixed_step)(device=dev)
     stream = torch.cuda.current_stream()
     ws = pa.Workspace(pa.prefill_workspace_bytes(case.batch, case.total_q, case.num_q_heads, case.num_kv_heads,
                                                  case.head_dim), dev)
@@ -614,8 +614,10 @@ def measure_mixed(pa, steps, warmup, peaks):
     flops = roofline.prefill_flops(pre_q, pre_L, case.num_q_heads, case.head_dim)
     t_bytes = dbytes / (peaks["hbm_gbs"] * 1e9)
     t_flops = flops / (peaks["bf16_tflops"] * 1e12)
-    res = {"workload": "mixed_step: 4 prefill chunks x 2048 tokens (0..8192 prior) + 60 decodes (1k..64k) + "
-                       "1 decode at 131072; Hq=32, Hkv=8, head_dim 128, 16-token pages",
+    res = {"workload": ("mixed_step_small: 4 prefill chunks x 2048 tokens (0..8192 prior) + 60 decodes (1k..4k) "
+                        "+ 1 decode at 16384" if small else
+                        "mixed_step: 4 prefill chunks x 2048 tokens (0..8192 prior) + 60 decodes (1k..64k) + "
+                        "1 decode at 131072") + "; Hq=32, Hkv=8, head_dim 128, 16-token pages",
            "step_ms": t, "decode_kv_bytes": dbytes, "prefill_flops": flops,
            "t_roofline_ms": 1e3 * max(t_bytes, t_flops), "t_serial_roofline_ms": 1e3 * (t_bytes + t_flops),
            "frac_of_roofline": max(t_bytes, t_flops) / (t * 1e-3),
@@ -630,7 +632,7 @@ def measure_mixed(pa, steps, warmup, peaks):
     return res
 
 
-def measure_ragged_decode(pa, steps, warmup, peaks):
+def measure_ragged_decode(pa, steps, warmup, peaks, small=False):
     """Ragged Llama-3-8B-shaped decode step: batch 64, contexts uniform on
     [1, 32768] (seeded), Hq=32, Hkv=8, D=128, 16-token pages scattered over a
     131,072-page pool; the same call as the headline step (split-K decode with
@@ -638,7 +640,7 @@ def measure_ragged_decode(pa, steps, warmup, peaks):
     KV per step, far above L2, so no flush; K calls back to back, then K calls
     with an event on each side."""
     dev = torch.device("cuda", torch.cuda.current_device())
-    case = workloads.llama8b_ragged_decode(device=dev)
+    case = (workloads.llama8b_ragged_small if small else workloads.llama8b_ragged_decode)(device=dev)
     stream = torch.cuda.current_stream()
     B, Hq, D = case.q.shape
     ws = pa.Workspace(pa.decode_workspace_bytes(B, Hq, case.num_kv_heads, D), dev)
@@ -668,9 +670,11 @@ def measure_ragged_decode(pa, steps, warmup, peaks):
     t_iso = statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(steps))
     kv = roofline.decode_kv_bytes(case.seq_lens_host, case.num_kv_heads, D)
     gbs = kv / (t * 1e-3) / 1e9
-    res = {"workload": "llama8b_ragged_decode: batch 64, contexts uniform on [1, 32768] (seeded), Hq=32, Hkv=8, "
-                       "head_dim 128, 16-token pages in a 131072-page pool; step = split-K decode with the newest "
-                       "row of each sequence written back in the same kernel (attn_decode_paged_append)",
+    res = {"workload": ("llama8b_ragged_small: the first 16 sequences of the batch-64 draw, pool = pages needed"
+                        if small else "llama8b_ragged_decode: batch 64, contexts uniform on [1, 32768] (seeded), "
+                        "Hq=32, Hkv=8, head_dim 128, 16-token pages in a 131072-page pool") +
+                       "; step = split-K decode with the newest row of each sequence written back in the same "
+                       "kernel (attn_decode_paged_append)",
            "tokens_in_context": int(sum(case.seq_lens_host)), "ms": t, "ms_isolated": t_iso, "kv_bytes": kv,
            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": gbs / peaks["hbm_gbs"], "frac_isolated": kv / (t_iso * 1e-3) / 1e9 / peaks["hbm_gbs"],
@@ -731,6 +735,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-only", action="store_true", help="skip the prefill and mixed-step measurements")
+    ap.add_argument("--small", action="store_true",
+                    help="with --only mixed / llama8b_ragged: the profiling-size workload (about 1 GB of KV)")
     ap.add_argument("--only", choices=["prefill", "mixed", "multiquery", "rope_writeback", "fp8_decode",
                                        "llama8b_ragged"],
                     default=None,
@@ -751,7 +757,8 @@ def main(argv=None):
         fn = {"prefill": measure_prefill, "mixed": measure_mixed, "multiquery": measure_multiquery,
               "rope_writeback": measure_rope_writeback, "fp8_decode": measure_fp8_decode,
               "llama8b_ragged": measure_ragged_decode}[args.only]
-        res = fn(pa, args.steps, args.warmup, peaks)
+        kw = {"small": True} if args.small and args.only in ("mixed", "llama8b_ragged") else {}
+        res = fn(pa, args.steps, args.warmup, peaks, **kw)
         if rank == 0:
             print(json.dumps({"only": args.only, args.only: res}), flush=True)
         return 0
@@ -770,7 +777,7 @@ def main(argv=None):
     dec_avg = statistics.mean(dec_ms)
     launch_ms = ms_per_step
     achieved = kv_bytes / (launch_ms * 1e-3) / 1e9
-    traffic = profile_traffic("attn_decode_qwen7b_ncu.md", ["paged_kv_decode_17_gb300/csrc/decode.cu",
+    traffic = profile_traffic("attn_decode_qwen7b_ncu.md", ["paged_kv_decode_17_gb300/csrc/decode_dev.cuh",
                                                             "paged_kv_decode_17_gb300/csrc/pa_common.cuh"])
     e2e_ms, h2d, d2h = measure_decode_e2e(pa, case, args.steps, args.warmup)
     e2e_ms = max_over_ranks(pg, e2e_ms)

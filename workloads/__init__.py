@@ -359,6 +359,34 @@ def mixed_step(seed: int = 4, device="cpu") -> PagedCase:
     )
 
 
+def mixed_step_small(seed: int = 4, device="cpu") -> PagedCase:
+    """The mixed step at profiling size: the same 4 prefill chunks of 2048 tokens
+    after 0-8192 prior tokens, 60 decodes with contexts uniform on [1024, 4096]
+    and one 16,384-token decode (about 0.7 GB of KV, still above L2)."""
+    gen = torch.Generator().manual_seed(seed)
+    priors = _uniform_ints(gen, 0, 8192, 4)
+    dec = _uniform_ints(gen, 1024, 4096, 60)
+    seq_lens = [p + 2048 for p in priors] + dec + [16384]
+    q_lens = [2048] * 4 + [1] * 61
+    need = sum(-(-s // 16) for s in seq_lens)
+    return make_paged_case(
+        "mixed_step_small", seq_lens=seq_lens, q_lens=q_lens, num_q_heads=32, num_kv_heads=8,
+        head_dim=128, page_size=16, num_pages=need + need // 10, seed=seed, device=device,
+    )
+
+
+def llama8b_ragged_small(seed: int = 2, device="cpu") -> PagedCase:
+    """The ragged Llama-3-8B-shaped decode at profiling size: batch 16 with
+    contexts uniform on [1, 32768] (the first 16 of the batch-64 draw), pool
+    = the pages needed (about 1 GB of KV)."""
+    lens = llama8b_ragged_lens(seed, 64, 32768)[:16]
+    need = sum(-(-s // 16) for s in lens)
+    return make_paged_case(
+        "llama8b_ragged_small", seq_lens=lens, q_lens=[1] * 16, num_q_heads=32, num_kv_heads=8, head_dim=128,
+        page_size=16, num_pages=need, max_pages_per_seq=32768 // 16, seed=seed, device=device,
+    )
+
+
 def awkward_cases(device="cpu", seed: int = 10) -> Dict[str, PagedCase]:
     """Small cases at the places fast paths skip work: one-token contexts,
     partially filled pages, contexts 127 and 4096, batch 1 and 32, extreme
