@@ -11,42 +11,36 @@
 //
 // GB300 design
 // * Work item = one 128-row query tile of one sequence for a pair of query
-//   heads of one KV head.  The query tiles are listed sorted by their number of
-//   key tiles, heaviest first (by a small plan kernel, or inside the mixed-step
-//   kernel).  The kernel is persistent, one CTA per SM; items are taken either
-//   round-robin or, in the mixed-step kernel, one at a time from a counter.
-//   Tensor memory and barriers are set up once per CTA, and the next item's Q
-//   and K/V are loaded while the current item finishes.
+//   heads of one KV head.  A small plan kernel lists the query tiles sorted by
+//   their number of key tiles, heaviest first.  The main kernel is persistent:
+//   each CTA (one per SM) walks that list round-robin.  Tensor memory and
+//   barriers are set up once per CTA, and the next item's Q and K/V are loaded
+//   while the current item finishes.
 // * warp 8 (producer): publishes each item through a 2-slot ring in shared
 //   memory, loads the two Q tiles by TMA (3-D tensor map over [rows][Hq][D],
 //   128-byte swizzle) and gathers K and V tiles: a 128-key tile is eight
 //   16-row page blocks found through the block table (one tile ahead), each
 //   64-column half a 128-byte-swizzled TMA box.  K and V tiles have
-//   separate rings (1 and 2 stages).
+//   separate rings (1 and 2 stages), so the next K tile loads as soon as the
+//   current scores are computed.
 // * warps 9 / 10 (MMA, one per head): one thread issues tcgen05.mma:
 //   S_h = Q_h K^T into TMEM (fp32, 128 columns) and O_h += P_h V into TMEM
-//   (fp32, D columns) with P_h read from TMEM (the A operand), where the
-//   softmax left it over the first 64 columns of S_h.  The next tile's scores
-//   overwrite P_h, so they are issued once this tile's P.V has read it; while
-//   one head waits, the other head's MMAs keep the tensor core busy.  (P in
-//   TMEM instead of shared memory saves, per tile and head, a 32 KB store by
-//   the softmax and a 32 KB operand read by the MMA, in a kernel whose shared
-//   memory otherwise moves about 384 KB per 128-key tile.)
+//   (fp32, D columns); the next tile's scores are issued as soon as the
+//   softmax has pulled the current ones out of TMEM.
 // * warps 0-3 / 4-7 (softmax, head 0 / 1): thread = row = TMEM lane; the
 //   whole score row goes to registers, is masked on diagonal tiles, and
-//   2^(s * scale * log2 e - m) becomes P (bf16, two keys per 32-bit column)
-//   in the row's TMEM lane.  O is rescaled in TMEM only when a row
+//   2^(s * scale * log2 e - m) becomes P (bf16) in shared memory in the
+//   swizzled K-major operand layout.  O is rescaled in TMEM only when a row
 //   maximum grows by more than TAU = 8 (log2 units): until then the
 //   exponentials are taken against the older, smaller maximum, which keeps
 //   them <= 2^8 and the result exact, because the final division uses the
 //   same reference maximum for numerator and denominator.  At the end of an
 //   item they normalise O; a full 128-row tile goes as bf16 into the head's
-//   staging buffer in shared memory, in the swizzled layout of a TMA box, and
-//   one thread writes it out with TMA tensor stores, so the warps move on to
-//   the next item at once (the next item's staging waits only for the store
-//   to have read the buffer).  A partial tile is stored directly, row by row,
-//   since a whole box would overwrite the next sequence's rows.
-// * CTA pairs (PAIR, optional): see Cfg.
+//   P buffer (free once the last P.V is done), in the swizzled layout of a
+//   TMA box, and one thread writes it out with TMA tensor stores, so the
+//   warps move on to the next item at once (the next P store waits only for
+//   the store to have read the buffer).  A partial tile is stored directly,
+//   row by row, since a whole box would overwrite the next sequence's rows.
 // Every wait is bounded; a timeout sets a CTA-wide abort flag, records
 // PA_ERR_TIMEOUT and all roles fall through to a clean exit.
 #pragma once
@@ -94,14 +88,14 @@ struct Cfg {
     static constexpr int NST = NKr + NVr;
     static constexpr int Q_BYTES = BM * D * 2;      // one head's Q tile
     static constexpr int KV_BYTES = BN * D * 2 / (PAIR ? 2 : 1);  // one K or V stage
-    static constexpr int P_BYTES = BM * BN * 2;     // one head's output staging buffer (>= BM x D bf16)
+    static constexpr int P_BYTES = BM * BN * 2;     // one P tile
     static constexpr int Q_KB = BM * 128;           // bytes per column block of a Q tile
     static constexpr int KV_KB = BN * 128;          // bytes per column block of a V stage (of a K stage, unpaired)
     static constexpr int K_KB = (PAIR ? BN / 2 : BN) * 128;  // bytes per column block of a K stage
     static constexpr int VKB = PAIR ? 1 : KB;       // column blocks per V stage
-    static constexpr int P_KB = BM * 128;           // bytes per 64-column block of a staging buffer
+    static constexpr int P_KB = BM * 128;           // bytes per 64-key column block of a P tile
     static constexpr int OFF_Q = 0;                 // Q[head]
-    static constexpr int OFF_P = 2 * Q_BYTES;       // output staging[head]
+    static constexpr int OFF_P = 2 * Q_BYTES;       // P[head]
     static constexpr int OFF_KV = OFF_P + 2 * P_BYTES;
     static constexpr int SMEM_BYTES = 1024 + OFF_KV + NST * KV_BYTES;
     // TMEM columns: S[head] (BN fp32), O[head] (D fp32)
@@ -144,7 +138,7 @@ struct Shared {
     uint64_t kv_full[NSTAGE_MAX];
     uint64_t kv_empty[NSTAGE_MAX];
     uint64_t v_peer[PNV];                // CTA pairs: the second CTA has cleared its rows of a V tile past the end
-    uint64_t s_full[2];
+    uint64_t s_full[2], s_free[2];
     uint64_t p_ready[2], pv_done[2];
     uint64_t o_free[2];                  // per head: the epilogue has read O out of TMEM
     uint64_t o_staged[2];                // per head: all 128 rows of O/l are in shared memory
@@ -217,16 +211,6 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// D (+)= A[tmem] * B[smem desc]: A (this CTA's 128 rows) read from tensor memory.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // Arrive on the barrier at cluster address `bar` once this thread's MMAs are done.
@@ -370,6 +354,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
             mbar_init(&sh.bar_q[h], 1);
             mbar_init(&sh.q_empty[h], 1);
             mbar_init(&sh.s_full[h], 1);
+            mbar_init(&sh.s_free[h], SMX_ARRIVALS);
             mbar_init(&sh.p_ready[h], SMX_ARRIVALS);
             mbar_init(&sh.pv_done[h], 1);
             mbar_init(&sh.o_free[h], SMX_ARRIVALS);
@@ -663,6 +648,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                 }
         } else if (lane == 0) {
             const uint32_t qaddr = smem_u32(sQ) + hh * C::Q_BYTES;
+            const uint32_t paddr = smem_u32(sP) + hh * C::P_BYTES;
             const uint32_t kv_base = smem_u32(sKV);
             const uint32_t t_s = tmem + C::TM_S0 + hh * BN;
             const uint32_t t_o = tmem + C::TM_O0 + hh * D;
@@ -724,29 +710,35 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                         commit_to(&sh.s_full[hh]);
                         if (j == n - 1) commit_to(&sh.q_empty[hh]);  // last read of this Q tile
                     };
-                    // O += P V with P (bf16, two keys per 32-bit column) read from tensor memory,
-                    // where the softmax left it over the first BN / 2 columns of S
                     auto issue_pv = [&](int j) {
                         const uint32_t vaddr = kv_base + vst(j) * C::KV_BYTES;
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk) {
+                            const uint64_t ad =
+                                tc::smem_desc_sw128(paddr + (kk >> 2) * C::P_KB + (kk & 3) * 32, 16, 1024);
                             const uint64_t bd = tc::smem_desc_sw128(vaddr + kk * 2048, C::KV_KB, 1024);
-                            if (PAIR)
-                                tc2::mma_ts(t_o, t_s + kk * 8, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-                            else
-                                tc::mma_ts(t_o, t_s + kk * 8, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                            mma(t_o, ad, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
                         }
                         commit_to(&sh.pv_done[hh]);
                     };
-                    // scores of key tile 0: S (and P over it) is free once the previous tile's P.V is done
+                    // scores of key tile 0 (the S buffer was freed by the previous tile's softmax)
                     if (ok) ok = wait_ab(&sh.kv_full[kst(0)], kph(0), sh, p);
-                    if (ok && J > 0) ok = wait_ab(&sh.pv_done[hh], (J - 1) & 1, sh, p);
+                    if (ok && J > 0) ok = wait_ab(&sh.s_free[hh], (J - 1) & 1, sh, p);
                     if (ok) {
                         tc::fence_after_sync();
                         issue_s(0);
                         release(&sh.kv_empty[kst(0)]);
                     }
                     for (int j = 0; j < n && ok; ++j) {
+                        if (j + 1 < n) {
+                            // next scores as soon as the softmax has pulled the current ones out of TMEM
+                            ok = wait_ab(&sh.kv_full[kst(j + 1)], kph(j + 1), sh, p) &&
+                                 wait_ab(&sh.s_free[hh], (J + j) & 1, sh, p);
+                            if (!ok) break;
+                            tc::fence_after_sync();
+                            issue_s(j + 1);
+                            release(&sh.kv_empty[kst(j + 1)]);
+                        }
                         ok = wait_ab(&sh.kv_full[vst(j)], vph(j), sh, p) &&
                              wait_ab(&sh.p_ready[hh], (J + j) & 1, sh, p);
                         if (PAIR && ok && (j + 1) * BN > itm.seq_len) {  // the peer zeroed its rows past the end
@@ -760,16 +752,6 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                         tc::fence_after_sync();
                         issue_pv(j);
                         release(&sh.kv_empty[vst(j)]);
-                        if (j + 1 < n) {
-                            // the next scores overwrite P: once this P.V has read it (the other head's
-                            // MMAs keep the tensor core busy meanwhile)
-                            ok = wait_ab(&sh.kv_full[kst(j + 1)], kph(j + 1), sh, p) &&
-                                 wait_ab(&sh.pv_done[hh], (J + j) & 1, sh, p);
-                            if (!ok) break;
-                            tc::fence_after_sync();
-                            issue_s(j + 1);
-                            release(&sh.kv_empty[kst(j + 1)]);
-                        }
                     }
                     J += n;
                     ++items;
@@ -836,6 +818,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                         for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(sr[i]);
                     }
                     tc::wait_ld();
+                    tc::fence_before_sync();
+                    smx_arrive(&sh.s_free[hh]);
                     if ((j + 1) * BN - 1 > itm.qmin) {  // diagonal tile: some key is after some row
 #pragma unroll
                         for (int c = 0; c < BN; ++c)
@@ -855,10 +839,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                     if (j == 0) {
                         m_ref = mx;
                     } else if (__any_sync(0xffffffffu, mx > m_ref + TAU)) {
-                        // rescale O to a new reference maximum.  Every earlier P.V is done: these
-                        // scores were computed after P.V(j-1) (it read P from the same columns)
+                        // rescale O to a new reference maximum (all earlier PVs done once PV(j-1) is)
                         const float m_new = fmaxf(m_ref, mx);
                         const float alpha = ex2(m_ref - m_new);
+                        ok = __all_sync(0xffffffffu, wait_ab(&sh.pv_done[hh], (jj - 1) & 1, sh, p));
+                        if (!ok) break;
+                        tc::fence_after_sync();
 #pragma unroll 1
                         for (int c0 = 0; c0 < D; c0 += 32) {
                             uint32_t o[32];
@@ -873,32 +859,48 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                         m_ref = m_new;
                     }
                     // p = 2^(s * scale_log2 - m_ref): the arguments two at a time (packed FFMA), one
-                    // MUFU each, packed to bf16 in registers; the sum in four packed accumulators
+                    // MUFU each, packed to bf16 in registers while the previous tile's P.V may still
+                    // be running; the sum in four packed accumulators
                     const float neg = -m_ref;
                     float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                    // P (bf16) goes into tensor memory over the first BN / 2 columns of this row's S
-                    // (read out above; the next S is computed only after the P.V has read P): the A
-                    // operand of the P.V MMA, two keys per 32-bit column, key 2i in the low half.
-                    // 32 keys at a time, so the stores overlap the remaining exponentials.
+                    uint32_t pk[BN / 2];
 #pragma unroll
-                    for (int qt = 0; qt < 4; ++qt) {
-                        uint32_t pk[16];
+                    for (int q = 0; q < BN / 8; ++q) {  // 16-byte chunk q = keys 8q .. 8q+7
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {  // keys 32 qt + 8q .. + 7
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int c = 32 * qt + 8 * q + 2 * i;
-                                float a0, a1;
-                                ffma2(a0, a1, x[c], x[c + 1], p.scale_log2, neg);
-                                const float p0 = ex2(a0), p1 = ex2(a1);
-                                fadd2(s8[2 * i], s8[2 * i + 1], p0, p1);
-                                pk[4 * q + i] = pack_bf16x2(p0, p1);
-                            }
+                        for (int i = 0; i < 4; ++i) {
+                            float a0, a1;
+                            ffma2(a0, a1, x[8 * q + 2 * i], x[8 * q + 2 * i + 1], p.scale_log2, neg);
+                            const float p0 = ex2(a0), p1 = ex2(a1);
+                            fadd2(s8[2 * i], s8[2 * i + 1], p0, p1);
+                            pk[4 * q + i] = pack_bf16x2(p0, p1);
                         }
-                        tc::st_32x32b_x16(t_s + 16 * qt, pk);
+                    }
+                    // the P buffer was last read by the previous tile's P.V (possibly of the
+                    // previous item).  Waiting for it also keeps p_ready / pv_done within one
+                    // phase of their waiters (mbarrier parity only tells adjacent phases apart).
+                    if (jj > 0) {
+                        ok = __all_sync(0xffffffffu, wait_ab(&sh.pv_done[hh], (jj - 1) & 1, sh, p));
+                        if (!ok) break;
+                    }
+                    // the previous item's O may still be leaving the P buffer through a TMA store
+                    if (store_pending) {
+                        if (leader) {
+                            bulk_wait_read_all();
+                            mbar_arrive(&sh.o_read[hh]);
+                        }
+                        ok = __all_sync(0xffffffffu, wait_ab(&sh.o_read[hh], (nst - 1) & 1, sh, p));
+                        if (!ok) break;
+                        store_pending = false;
+                    }
+                    // P (bf16) to shared memory in the 128-byte-swizzled K-major layout
+#pragma unroll
+                    for (int q = 0; q < BN / 8; ++q) {
+                        const int kb = q >> 3, c = q & 7;
+                        *reinterpret_cast<uint4*>(prow + kb * C::P_KB + ((c ^ (r & 7)) << 4)) =
+                            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                     }
                     l += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
-                    tc::wait_st();
+                    fence_proxy_async_smem();
                     tc::fence_before_sync();
                     smx_arrive(&sh.p_ready[hh]);
                 }
@@ -914,18 +916,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                     const int h = min(itm.h0 + hh, itm.hmax);
                     if (!keep) {
                     } else if (itm.rows_valid == BM) {
-                        // full tile: O/l -> bf16 into the head's staging buffer in the swizzled layout
-                        // of a 64-column TMA box, then one thread stores it with TMA.  The previous
-                        // item's O may still be leaving that buffer through its TMA store.
-                        if (store_pending) {
-                            if (leader) {
-                                bulk_wait_read_all();
-                                mbar_arrive(&sh.o_read[hh]);
-                            }
-                            ok = __all_sync(0xffffffffu, wait_ab(&sh.o_read[hh], (nst - 1) & 1, sh, p));
-                            if (!ok) break;  // (leaves the item loop: an abort)
-                            store_pending = false;
-                        }
+                        // full tile: O/l -> bf16 into the P buffer (free: the last P.V is done) in the
+                        // swizzled layout of a 64-column TMA box, then one thread stores it with TMA
 #pragma unroll 1
                         for (int c0 = 0; c0 < D; c0 += 32) {
                             uint32_t o[32];
