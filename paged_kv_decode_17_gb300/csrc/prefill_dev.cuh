@@ -11,11 +11,12 @@
 //
 // GB300 design
 // * Work item = one 128-row query tile of one sequence for a pair of query
-//   heads of one KV head.  A small plan kernel lists the query tiles sorted by
-//   their number of key tiles, heaviest first.  The main kernel is persistent:
-//   each CTA (one per SM) walks that list round-robin.  Tensor memory and
-//   barriers are set up once per CTA, and the next item's Q and K/V are loaded
-//   while the current item finishes.
+//   heads of one KV head.  The query tiles are listed sorted by their number of
+//   key tiles, heaviest first (by a small plan kernel, or inside the mixed-step
+//   kernel).  The kernel is persistent, one CTA per SM; items are taken either
+//   round-robin or, in the mixed-step kernel, one at a time from a counter.
+//   Tensor memory and barriers are set up once per CTA, and the next item's Q
+//   and K/V are loaded while the current item finishes.
 // * warp 8 (producer): publishes each item through a 2-slot ring in shared
 //   memory, loads the two Q tiles by TMA (3-D tensor map over [rows][Hq][D],
 //   128-byte swizzle) and gathers K and V tiles: a 128-key tile is eight
@@ -41,6 +42,7 @@
 //   warps move on to the next item at once (the next P store waits only for
 //   the store to have read the buffer).  A partial tile is stored directly,
 //   row by row, since a whole box would overwrite the next sequence's rows.
+// * CTA pairs (PAIR, optional): see Cfg.
 // Every wait is bounded; a timeout sets a CTA-wide abort flag, records
 // PA_ERR_TIMEOUT and all roles fall through to a clean exit.
 #pragma once
