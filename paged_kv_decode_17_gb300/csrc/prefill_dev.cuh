@@ -128,17 +128,11 @@ struct Params {
 };
 
 // One work item as published by the producer.
-// Its two head slots share the K/V tiles of one sequence and KV head; each slot has its
-// own query head and query tile (with an odd group, the group's last head takes two
-// adjacent query tiles of the sequence in one item instead of idling half the CTA).
 struct Item {
     int end;  // 1: no more items
-    int b, g, q_len, seq_len;
-    int n_kv;    // key tiles loaded for the item: the larger of the slots' counts
-    int nheads;  // head slots computed
+    int b, t, q_len, seq_len, row0, g, h0, nheads, n_kv, rows_valid, qmin;
     int nstore;  // head slots whose results are stored (a CTA pair computes a last valid head twice)
-    int head[2], row0[2], rows_valid[2], qmin[2], nkv[2];  // per slot: query head, first row of its tile,
-                                                           // rows, position of row 0, key tiles it sees
+    int hmax;    // last query head of the KV group: slots past it compute it again
 };
 
 struct Shared {
@@ -453,44 +447,19 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                 const int pair = rem - itm.g * p.NPC;  // (CTA pairs: block of 4 heads)
                 const int2 bt = __ldcg(p.tiles + ti);
                 itm.b = bt.x;
-                const int t = bt.y;
+                itm.t = bt.y;
                 const int c0 = __ldg(p.cu_q + itm.b);
                 itm.q_len = __ldg(p.cu_q + itm.b + 1) - c0;
                 itm.seq_len = __ldg(p.seq_lens + itm.b);
-                const int hlast = itm.g * p.group + p.group - 1;
-                int t1 = t, hs0, hs1;  // slot 1's query tile; the slots' heads
-                if (PAIR) {
-                    // a pair computes both slots of both CTAs (the MMA spans them); slots past the
-                    // group's last head compute it again and store nothing
-                    const int hfirst = 4 * pair + 2 * (int)crank;
-                    hs0 = min(itm.g * p.group + hfirst, hlast);
-                    hs1 = min(itm.g * p.group + hfirst + 1, hlast);
-                    itm.nheads = 2;
-                    itm.nstore = max(0, min(2, p.group - hfirst));
-                } else if ((p.group & 1) && pair == p.NPC - 1) {
-                    // the group's last head alone: its query tiles t and t + 1 share this item (and
-                    // its K/V tiles); the item listed for tile t + 1 is empty
-                    hs0 = hs1 = hlast;
-                    const int nt = (itm.q_len + BM - 1) / BM;
-                    t1 = t + 1;
-                    itm.nheads = (t & 1) ? 0 : (t1 < nt ? 2 : 1);
-                    itm.nstore = itm.nheads;
-                } else {
-                    hs0 = itm.g * p.group + 2 * pair;
-                    hs1 = hs0 + 1;
-                    itm.nheads = itm.nstore = min(2, p.group - 2 * pair);
-                }
-                itm.n_kv = 0;
-#pragma unroll
-                for (int sl = 0; sl < 2; ++sl) {
-                    const int ts = sl ? t1 : t;
-                    itm.head[sl] = sl ? hs1 : hs0;
-                    itm.row0[sl] = c0 + ts * BM;
-                    itm.rows_valid[sl] = min(BM, itm.q_len - ts * BM);
-                    itm.qmin[sl] = itm.seq_len - itm.q_len + ts * BM;
-                    itm.nkv[sl] = (itm.qmin[sl] + itm.rows_valid[sl] - 1) / BN + 1;
-                    if (sl < itm.nheads) itm.n_kv = max(itm.n_kv, itm.nkv[sl]);
-                }
+                itm.row0 = c0 + itm.t * BM;
+                const int hfirst = PAIR ? 4 * pair + 2 * (int)crank : 2 * pair;  // within the KV group
+                itm.h0 = itm.g * p.group + hfirst;
+                itm.nstore = max(0, min(2, p.group - hfirst));
+                itm.nheads = PAIR ? 2 : itm.nstore;  // a pair computes both slots (the MMA spans both CTAs)
+                itm.hmax = itm.g * p.group + p.group - 1;
+                itm.rows_valid = min(BM, itm.q_len - itm.t * BM);
+                itm.qmin = itm.seq_len - itm.q_len + itm.t * BM;
+                itm.n_kv = (itm.qmin + itm.rows_valid - 1) / BN + 1;
             }
             const int slot = k & 1;
             ok = __all_sync(0xffffffffu, wait_ab(&sh.item_empty[slot], ((k >> 1) & 1) ^ 1, sh, p));
@@ -508,19 +477,19 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                                     wait_ab(&sh.q_empty[hh], (qloads[hh] - 1) & 1, sh, p));
                 if (!ok) break;
                 if (lane == 0) {
-                    const int head = itm.head[hh];
+                    const int head = min(itm.h0 + hh, itm.hmax);
                     if (!PAIR) {
                         mbar_arrive_expect_tx(&sh.bar_q[hh], C::Q_BYTES);
                         for (int kb = 0; kb < C::KB; ++kb)
                             tma_load_3d(sQ + hh * C::Q_BYTES + kb * C::Q_KB, &qmap, &sh.bar_q[hh], kb * 64, head,
-                                        itm.row0[hh]);
+                                        itm.row0);
                     } else {
                         // both CTAs' Q tiles land on the first CTA's barrier, armed there for both
                         if (lead) mbar_arrive_expect_tx(&sh.bar_q[hh], 2 * C::Q_BYTES);
                         const uint32_t bq = map_cta(&sh.bar_q[hh], 0);
                         for (int kb = 0; kb < C::KB; ++kb)
                             tma_load_3d_pair(sQ + hh * C::Q_BYTES + kb * C::Q_KB, &qmap, bq, kb * 64, head,
-                                             itm.row0[hh]);
+                                             itm.row0);
                     }
                 }
                 ++qloads[hh];
@@ -730,8 +699,6 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                 } else {
                     ok = wait_ab(&sh.bar_q[hh], qn & 1, sh, p);
                     ++qn;
-                    const int nall = n;             // key tiles of the item (both slots)
-                    const int n = itm.nkv[hh];      // key tiles this slot's query tile sees
                     auto issue_s = [&](int j) {
                         const uint32_t kaddr = kv_base + kst(j) * C::KV_BYTES;
 #pragma unroll
@@ -788,13 +755,6 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                         issue_pv(j);
                         release(&sh.kv_empty[vst(j)]);
                     }
-                    // the other slot's query tile sees more key tiles: release those stages too
-                    for (int j = n; j < nall && ok; ++j) {
-                        ok = wait_ab(&sh.kv_full[kst(j)], kph(j), sh, p);
-                        if (ok) release(&sh.kv_empty[kst(j)]);
-                        if (ok) ok = wait_ab(&sh.kv_full[vst(j)], vph(j), sh, p);
-                        if (ok) release(&sh.kv_empty[vst(j)]);
-                    }
                     J += n;
                     ++items;
                 }
@@ -842,9 +802,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
             const Item itm = sh.items[k & 1];
             if (itm.end) break;
             if (hh < itm.nheads) {
-                const int n = itm.nkv[hh];  // key tiles this slot's query tile sees
-                const int qmin = itm.qmin[hh];
-                const int qpos = qmin + r;
+                const int n = itm.n_kv;
+                const int qpos = itm.qmin + r;
                 float m_ref = -INFINITY, l = 0.f;
                 for (int j = 0; j < n && ok; ++j) {
                     const int jj = J + j;
@@ -863,7 +822,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                     tc::wait_ld();
                     tc::fence_before_sync();
                     smx_arrive(&sh.s_free[hh]);
-                    if ((j + 1) * BN - 1 > qmin) {  // diagonal tile: some key is after some row
+                    if ((j + 1) * BN - 1 > itm.qmin) {  // diagonal tile: some key is after some row
 #pragma unroll
                         for (int c = 0; c < BN; ++c)
                             if (j * BN + c > qpos) x[c] = -INFINITY;
@@ -955,11 +914,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                     const float inv = l > 0.f ? 1.f / l : 0.f;
                     // a pair may compute the KV group's last head in two slots: one copy is stored
                     const bool keep = hh < itm.nstore;
-                    const bool store = keep && r < itm.rows_valid[hh];
-                    const int h = itm.head[hh];
-                    const int row0 = itm.row0[hh];
+                    const bool store = keep && r < itm.rows_valid;
+                    const int h = min(itm.h0 + hh, itm.hmax);
                     if (!keep) {
-                    } else if (itm.rows_valid[hh] == BM) {
+                    } else if (itm.rows_valid == BM) {
                         // full tile: O/l -> bf16 into the P buffer (free: the last P.V is done) in the
                         // swizzled layout of a 64-column TMA box, then one thread stores it with TMA
 #pragma unroll 1
@@ -986,14 +944,14 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                             if (ok) {
 #pragma unroll
                                 for (int kb = 0; kb < C::KB; ++kb)
-                                    tma_store_3d(&omap, sP + hh * C::P_BYTES + kb * C::P_KB, kb * 64, h, row0);
+                                    tma_store_3d(&omap, sP + hh * C::P_BYTES + kb * C::P_KB, kb * 64, h, itm.row0);
                                 bulk_commit();
                             }
                         }
                         ++nst;
                         store_pending = true;
                     } else {
-                    __nv_bfloat16* orow = p.out + ((size_t)(row0 + r) * p.Hq + h) * D;
+                    __nv_bfloat16* orow = p.out + ((size_t)(itm.row0 + r) * p.Hq + h) * D;
 #pragma unroll 1
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t o[32];
@@ -1013,7 +971,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                     }
                     }
                     if (store && p.lse != nullptr)
-                        p.lse[(size_t)(row0 + r) * p.Hq + h] = l > 0.f ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+                        p.lse[(size_t)(itm.row0 + r) * p.Hq + h] = l > 0.f ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
                     tc::fence_before_sync();
                     smx_arrive(&sh.o_free[hh]);
                 }
