@@ -1,10 +1,10 @@
 // Eager K/V writeback into pages ("Inside Ion", section "IonAttention in One
 // Paragraph": KV pages are written back eagerly as they are produced).
 //
-// One warp per new token: it finds the token's sequence by counting the
-// cu_seqlens_new entries at or below it (one coalesced load per 32 sequences),
+// Each warp moves new rows (two at a time): it finds a row's sequence by counting
+// the cu_seqlens_new entries at or below it (one coalesced load per 32 sequences),
 // resolves (page, slot) through the block table, and
-// copies the token's [Hkv][D] K and V rows with 16-byte vector loads and
+// copies the row's [Hkv][D] K and V vectors with 16-byte vector loads and
 // stores.  A bit-exact copy; nothing else in the pools is written.
 //
 // kv_write_paged_rope fuses the step before it ("The Stack Below the Stack,
@@ -53,6 +53,25 @@ __device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu_new, int 
     return cnt - 1;
 }
 
+// Sequences of new rows t0 and t1 (see find_seq), counted in one pass.
+__device__ __forceinline__ void find_seq2(const int32_t* __restrict__ cu_new, int batch, int t0, int t1, int& b0,
+                                          int& b1) {
+    const int lane = threadIdx.x & 31;
+    int c0 = 0, c1 = 0;
+    for (int c = 0; c <= batch; c += 32) {
+        const int idx = c + lane;
+        const int v = idx <= batch ? __ldg(cu_new + idx) : 0x7fffffff;
+        c0 += __popc(__ballot_sync(0xffffffffu, v <= t0));
+        c1 += __popc(__ballot_sync(0xffffffffu, v <= t1));
+    }
+    b0 = c0 - 1;
+    b1 = c1 - 1;
+}
+
+// One warp moves two new rows at a time (rows t and t + stride of its grid-stride walk):
+// both rows' vectors are loaded first, then both rows' (sequence, page, slot) lookups run
+// side by side -- each is a chain of dependent loads (cu_seqlens, seq_lens, block table) --
+// and both rows are stored.  Two independent chains per warp hide each other's latency.
 __global__ void __launch_bounds__(kWarps * 32) kv_write_kernel(
     __nv_bfloat16* __restrict__ k_pool, __nv_bfloat16* __restrict__ v_pool, const __nv_bfloat16* __restrict__ k_new,
     const __nv_bfloat16* __restrict__ v_new, const int32_t* __restrict__ cu_new, const int32_t* __restrict__ seq_lens,
@@ -63,43 +82,73 @@ __global__ void __launch_bounds__(kWarps * 32) kv_write_kernel(
     const int vec_per_head = head_dim / 8;  // 16-byte vectors per row
     const int vec_per_tok = num_kv_heads * vec_per_head;
     const int nwarps = gridDim.x * kWarps;
-    for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < total_new; t += nwarps) {
-        const uint4* ks = reinterpret_cast<const uint4*>(k_new + (size_t)t * num_kv_heads * head_dim);
-        const uint4* vs = reinterpret_cast<const uint4*>(v_new + (size_t)t * num_kv_heads * head_dim);
-        // the row's first vectors depend only on t: load them while the sequence is looked up
-        uint4 k0 = make_uint4(0, 0, 0, 0), v0 = k0, k1 = k0, v1 = k0;
-        if (lane < vec_per_tok) {
-            k0 = __ldg(ks + lane);
-            v0 = __ldg(vs + lane);
+    for (int ta = blockIdx.x * kWarps + (threadIdx.x >> 5); ta < total_new; ta += 2 * nwarps) {
+        const int tt[2] = {ta, ta + nwarps};
+        uint4 kr[2][2], vr[2][2];  // [row][vector lane, lane + 32]
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            kr[u][0] = kr[u][1] = vr[u][0] = vr[u][1] = make_uint4(0, 0, 0, 0);
+            if (tt[u] < total_new) {
+                const uint4* ks = reinterpret_cast<const uint4*>(k_new + (size_t)tt[u] * num_kv_heads * head_dim);
+                const uint4* vs = reinterpret_cast<const uint4*>(v_new + (size_t)tt[u] * num_kv_heads * head_dim);
+                if (lane < vec_per_tok) {
+                    kr[u][0] = __ldg(ks + lane);
+                    vr[u][0] = __ldg(vs + lane);
+                }
+                if (lane + 32 < vec_per_tok) {
+                    kr[u][1] = __ldg(ks + lane + 32);
+                    vr[u][1] = __ldg(vs + lane + 32);
+                }
+            }
         }
-        if (lane + 32 < vec_per_tok) {
-            k1 = __ldg(ks + lane + 32);
-            v1 = __ldg(vs + lane + 32);
+        int bb[2];
+        find_seq2(cu_new, batch, tt[0], tt[1] < total_new ? tt[1] : tt[0], bb[0], bb[1]);
+        int c0[2], n_b[2], L[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int b = min(max(bb[u], 0), batch - 1);  // (checked below)
+            c0[u] = __ldg(cu_new + b);
+            n_b[u] = __ldg(cu_new + b + 1) - c0[u];
+            L[u] = __ldg(seq_lens + b);
         }
-        const int b = find_seq(cu_new, batch, t);
-        const int c0 = __ldg(cu_new + b);
-        const int n_b = __ldg(cu_new + b + 1) - c0;
-        const int i = t - c0;
-        const int L = __ldg(seq_lens + b);
-        const int pos = L - n_b + i;
-        if (b < 0 || b >= batch || n_b <= 0 || i >= n_b || pos < 0 || pos >= max_pages * page_size) {
-            if (lane == 0) report(status, PA_ERR_BAD_LEN);
-            continue;
+        int phys[2], slot[2];
+        bool okk[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int b = bb[u];
+            const int i = tt[u] - c0[u];
+            const int pos = L[u] - n_b[u] + i;
+            okk[u] = tt[u] < total_new;
+            phys[u] = -1;
+            slot[u] = 0;
+            if (okk[u] && (b < 0 || b >= batch || n_b[u] <= 0 || i >= n_b[u] || pos < 0 ||
+                           pos >= max_pages * page_size)) {
+                if (lane == 0) report(status, PA_ERR_BAD_LEN);
+                okk[u] = false;
+            }
+            if (okk[u]) {
+                phys[u] = __ldg(block_table + (size_t)b * max_pages + pos / page_size);
+                slot[u] = pos % page_size;
+            }
         }
-        const int phys = __ldg(block_table + (size_t)b * max_pages + pos / page_size);
-        if (phys < 0 || phys >= num_pages) {
-            if (lane == 0) report(status, PA_ERR_BAD_PAGE);
-            continue;
-        }
-        const int slot = pos % page_size;
-        for (int v = lane; v < vec_per_tok; v += 32) {
-            const int g = v / vec_per_head;
-            const int c = v - g * vec_per_head;
-            const size_t dst = (((size_t)phys * num_kv_heads + g) * page_size + slot) * head_dim / 8 + c;
-            const uint4 kv = v == lane ? k0 : (v == lane + 32 ? k1 : __ldg(ks + v));
-            const uint4 vv = v == lane ? v0 : (v == lane + 32 ? v1 : __ldg(vs + v));
-            reinterpret_cast<uint4*>(k_pool)[dst] = kv;
-            reinterpret_cast<uint4*>(v_pool)[dst] = vv;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (!okk[u]) continue;
+            if (phys[u] < 0 || phys[u] >= num_pages) {
+                if (lane == 0) report(status, PA_ERR_BAD_PAGE);
+                continue;
+            }
+            const uint4* ks = reinterpret_cast<const uint4*>(k_new + (size_t)tt[u] * num_kv_heads * head_dim);
+            const uint4* vs = reinterpret_cast<const uint4*>(v_new + (size_t)tt[u] * num_kv_heads * head_dim);
+            for (int v = lane; v < vec_per_tok; v += 32) {
+                const int g = v / vec_per_head;
+                const int c = v - g * vec_per_head;
+                const size_t dst = (((size_t)phys[u] * num_kv_heads + g) * page_size + slot[u]) * head_dim / 8 + c;
+                const uint4 kv = v == lane ? kr[u][0] : (v == lane + 32 ? kr[u][1] : __ldg(ks + v));
+                const uint4 vv = v == lane ? vr[u][0] : (v == lane + 32 ? vr[u][1] : __ldg(vs + v));
+                reinterpret_cast<uint4*>(k_pool)[dst] = kv;
+                reinterpret_cast<uint4*>(v_pool)[dst] = vv;
+            }
         }
     }
 }
@@ -350,9 +399,10 @@ extern "C" int kv_write_paged(void* k_pool, void* v_pool, int num_pages, const v
     DeviceInfo dev;
     int rc = current_device(&dev);
     if (rc != PA_OK) return rc;
-    const int blocks_needed = (total_new + kvw::kWarps - 1) / kvw::kWarps;
+    const int blocks_needed = (total_new + 2 * kvw::kWarps - 1) / (2 * kvw::kWarps);  // two rows per warp
     const int grid = blocks_needed < dev.sm_count * 16 ? blocks_needed : dev.sm_count * 16;
-    log_config("kv writeback: head_dim %d, one warp per new row, grid %d CTAs x %d warps", head_dim, grid, kvw::kWarps);
+    log_config("kv writeback: head_dim %d, two new rows per warp at a time, grid %d CTAs x %d warps", head_dim, grid,
+               kvw::kWarps);
     kvw::kv_write_kernel<<<grid, kvw::kWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<__nv_bfloat16*>(k_pool), static_cast<__nv_bfloat16*>(v_pool),
         static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new), cu_seqlens_new, seq_lens,

@@ -67,3 +67,14 @@ def test_kv_write_bad_page_reports_status(cuda_device):
     # sequence 0 was still written, the bad rows were skipped
     after_k = bits(g.k_pool)
     assert (after_k != before_k).any()
+
+
+def test_kv_write_many_sequences(cuda_device):
+    # more than 32 sequences (the row -> sequence count spans several 32-entry chunks of cu_seqlens),
+    # an odd number of new rows, and rows past the 64 vectors a warp holds (Hkv 8, D 128)
+    gen = torch.Generator().manual_seed(35)
+    B = 70
+    q_lens = torch.randint(0, 7, (B,), generator=gen).tolist()
+    seq_lens = [q + int(torch.randint(0, 90, (1,), generator=gen)) for q in q_lens]
+    case = workloads.make_paged_case("wb_many", seq_lens, q_lens, 16, 8, 128, prewritten=False, seed=35)
+    _run_and_compare(case, cuda_device)
