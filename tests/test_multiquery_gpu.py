@@ -201,3 +201,21 @@ def test_multiquery_append_matches_writeback_then_decode(cuda_device, lens, qlen
     assert torch.equal(v2.view(torch.int16), case.v_pool.view(torch.int16))
     ref_out, ref_lse = oracle.paged_attention(**oracle_args(case))
     assert_attention_close(out2, ref_out, lse2, ref_lse, what="mq_append")
+
+
+@pytest.mark.parametrize("chunk", ["1", "5"])
+def test_multiquery_small_chunks(cuda_device, monkeypatch, chunk):
+    """Small split-K chunks (PAGEDATTN_DECODE_CHUNK, in 16-key units): many CTA
+    ranges per segment, so range boundaries fall between the row blocks of one
+    key block (segments of 2 and 4 row blocks), and a ragged call mixes segments
+    of 1, 2 and 4 row blocks.  Against the oracle, and bit-identical run to run."""
+    monkeypatch.setenv("PAGEDATTN_DECODE_CHUNK", chunk)
+    for name, lens, qlens, hq, hkv, d in [("sc_q4_g7", [2000, 4, 129, 700], [4, 4, 4, 4], 28, 4, 128),
+                                         ("sc_q8_g7", [3000, 8, 77], [8, 8, 8], 7, 1, 128),
+                                         ("sc_ragged", [400, 1, 65, 5000, 3, 999], [1, 1, 5, 8, 3, 2], 16, 2, 128),
+                                         ("sc_d64", [700, 50, 333], [3, 3, 7], 32, 2, 64)]:
+        case = workloads.make_paged_case(name, lens, qlens, hq, hkv, d, page_size=16, seed=len(name) * 7 + d)
+        _check(case, cuda_device)
+        a, la = _mq(case, cuda_device)
+        b, lb = _mq(case, cuda_device)
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)) and torch.equal(la, lb)
