@@ -686,7 +686,7 @@ def measure_ragged_decode(pa, steps, warmup, peaks, small=False):
                         "frac": gbs / peaks["hbm_gbs"], "frac_isolated": kv / (t_iso * 1e-3) / 1e9 / peaks["hbm_gbs"],
                         "peak_source": peaks["source"]},
            "tokens_per_s": B / (t * 1e-3), "steps": steps, "launches_per_step": 2,
-           "l2": "inputs larger than L2 (about 4.3 GB of KV), no flush"}
+           "l2": "inputs larger than L2 (%.2f GB of KV), no flush" % (kv / 1e9)}
     del case
     torch.cuda.empty_cache()
     return res
