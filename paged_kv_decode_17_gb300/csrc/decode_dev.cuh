@@ -34,7 +34,9 @@
 //   the first find it in L2.  With q_len > 1 (multi-query decode, e.g. the
 //   verification of speculated tokens) row i of the query block sees keys
 //   0 .. seq_len - q_len + i.  Scores, running max/sum and O stay in fp32
-//   registers.
+//   registers; O is rescaled only when a row's maximum grows by more than
+//   kDecTau (conditional rescaling, "The Stack Below the Stack, Part 2",
+//   section 2.3).
 // * At the end of the CTA's part of a segment the states of the warps that
 //   hold the same row block are merged in shared memory in a fixed order.  A
 //   segment covered by one chunk is normalised and stored directly; otherwise
@@ -61,6 +63,11 @@ constexpr int UNIT = 16;       // tokens per unit
 constexpr int RB = 16;         // rows per row block (mma M)
 constexpr int SBR = 64;        // rows per segment (at most W row blocks)
 constexpr int MIN_CHUNK = 16;  // minimum units per CTA
+// Conditional rescaling (log2 units): a row's reference maximum moves only when a
+// unit's scores exceed it by more than this, so the exponentials stay <= 2^8 and O and
+// l are rescaled rarely.  The result is unchanged: numerator and denominator are taken
+// against the same reference.
+constexpr float kDecTau = 8.f;
 // CTAs (of 4 warps) per SM: they hide each other's latency.  The swapped-operand
 // FP8 variant is bound by its own instruction latency and runs three per SM (in
 // 168 registers, with shallower staging so the shared memory fits); the others
@@ -352,10 +359,15 @@ __device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// two e4m3 codes (low byte first) -> two fp16 values (low half first); exact
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xFFFFu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// four e4m3 codes (bytes 0 .. 3 of w) -> two fp16 pairs: lo = codes 0, 1 and hi = codes 2, 3
+// (low half first); exact.  One conversion instruction per pair, reading the 16-bit halves
+// of w in place (a helper that returns the halves separately costs two byte permutes more
+// per pair to split and repack them).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 cl, ch;\n\tmov.b32 {cl, ch}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, cl;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, ch;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -698,8 +710,9 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
                     }
 #pragma unroll
                     for (int kk = 0; kk < KSTEPS; ++kk) {
-                        const uint32_t a[4] = {e4m3x2_to_f16x2(w0[kk]), e4m3x2_to_f16x2(w1[kk]),
-                                               e4m3x2_to_f16x2(w0[kk] >> 16), e4m3x2_to_f16x2(w1[kk] >> 16)};
+                        uint32_t a[4];
+                        e4m3x4_to_f16x2x2(w0[kk], a[0], a[2]);
+                        e4m3x4_to_f16x2x2(w1[kk], a[1], a[3]);
                         const uint32_t (&qb)[4] = qa[kk];
                         mma_16816_f16((kk & 1) ? sb : sa, a, qb[0], qb[1]);
                     }
@@ -725,7 +738,7 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
                     rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, o_));
                     rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, o_));
                 }
-                const float mn0 = fmaxf(m0, rm0), mn1 = fmaxf(m1, rm1);
+                const float mn0 = rm0 > m0 + kDecTau ? rm0 : m0, mn1 = rm1 > m1 + kDecTau ? rm1 : m1;
                 const float mr0 = mn0 == -INFINITY ? 0.f : mn0, mr1 = mn1 == -INFINITY ? 0.f : mn1;
                 const float a0 = ex2(m0 - mr0), a1 = ex2(m1 - mr1);
                 m0 = mn0;
@@ -755,8 +768,9 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
                         asm volatile("ld.shared.u32 %0, [%1];"
                                      : "=r"(wh)
                                      : "r"(vb + (n * 16 + 8 + qr) * 16 + (lane & 3) * 4));
-                        const uint32_t a[4] = {e4m3x2_to_f16x2(wl), e4m3x2_to_f16x2(wh), e4m3x2_to_f16x2(wl >> 16),
-                                               e4m3x2_to_f16x2(wh >> 16)};
+                        uint32_t a[4];
+                        e4m3x4_to_f16x2x2(wl, a[0], a[2]);
+                        e4m3x4_to_f16x2x2(wh, a[1], a[3]);
                         mma_16816_f16(o[n], a, b0, b1);
                     }
                 } else {
@@ -799,7 +813,8 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
                         }
 #pragma unroll
                         for (int kk = 0; kk < KSTEPS; ++kk) {
-                            const uint32_t b0 = e4m3x2_to_f16x2(w[kk]), b1 = e4m3x2_to_f16x2(w[kk] >> 16);
+                            uint32_t b0, b1;
+                            e4m3x4_to_f16x2x2(w[kk], b0, b1);
                             mma_16816_f16((kk & 1) ? s2[t] : s[t], qa[kk], b0, b1);
                         }
                     }
@@ -840,7 +855,7 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
                 rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, 2));
                 rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 1));
                 rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 2));
-                const float mn0 = fmaxf(m0, rm0), mn1 = fmaxf(m1, rm1);
+                const float mn0 = rm0 > m0 + kDecTau ? rm0 : m0, mn1 = rm1 > m1 + kDecTau ? rm1 : m1;
                 // a row with no visible key yet keeps m = -inf; measure from 0 then so
                 // that nothing computes -inf - (-inf)
                 const float mr0 = mn0 == -INFINITY ? 0.f : mn0, mr1 = mn1 == -INFINITY ? 0.f : mn1;
@@ -879,7 +894,9 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
                     for (int n = 0; n < NT; ++n) {
                         uint32_t w;
                         asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(vb + (n * 8 + qr) * 16 + (lane & 3) * 4));
-                        mma_16816_f16(o[n], pa, e4m3x2_to_f16x2(w), e4m3x2_to_f16x2(w >> 16));
+                        uint32_t b0, b1;
+                        e4m3x4_to_f16x2x2(w, b0, b1);
+                        mma_16816_f16(o[n], pa, b0, b1);
                     }
                 } else {
                 pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
