@@ -254,6 +254,33 @@ __device__ __forceinline__ int unit_page(const Params& p, UnitIter& it, int lane
     return __shfl_sync(0xffffffffu, it.pc_phys, k);
 }
 
+// Per-lane parts of the bf16 staging copies' addresses, the same for every unit.
+// In step j of K and of V, lane l copies 16-byte chunk cc = l mod CH of row
+// r = RPI j + l / CH (CH = D / 8 chunks per row, RPI = 32 / CH rows per step); the
+// chunk sits at row * 2D + src in the pool and at RPI j * 128 + dst[j mod SWP] in
+// the stage (the 128-byte swizzle of row r only depends on j mod SWP).
+// FP8: the K rows are D bytes (CH = D / 16 chunks, RPI = 32 / CH rows per step, 128-byte
+// swizzle at D = 128); each lane then copies one 16-byte transposed V row per step.
+template <int D, bool FP8 = false>
+struct CopyLanes {
+    static constexpr int CH = FP8 ? D / 16 : D / 8, RPI = 32 / CH;
+    static constexpr int SWP = (FP8 && D != 128) ? 1 : 8 / RPI, STEPS = UNIT / RPI;
+    static constexpr int ROW = FP8 ? D : 2 * D;  // bytes per K row
+    uint32_t src;
+    uint32_t dst[SWP];
+    __device__ __forceinline__ explicit CopyLanes(int lane) {
+        const int rl = lane / CH, cc = lane % CH;
+        src = (uint32_t)(rl * ROW + cc * 16);
+#pragma unroll
+        for (int k = 0; k < SWP; ++k) {
+            if (FP8)
+                dst[k] = (uint32_t)(rl * D + ((D == 128 ? ((cc ^ rl ^ (RPI * k)) & 7) : cc) << 4));
+            else
+                dst[k] = (uint32_t)(rl * 128 + (cc >> 3) * (UNIT * 128) + ((((cc & 7) ^ rl ^ (RPI * k)) & 7) << 4));
+        }
+    }
+};
+
 // Stage one unit (16 keys of K and of V) with 16-byte cp.async copies, written
 // in the 128-byte-swizzled layout the ldmatrix reads expect: 16-byte chunk c of
 // row r of a 64-column box sits at r * 128 + ((c ^ (r & 7)) * 16).  Lanes
@@ -263,7 +290,7 @@ __device__ __forceinline__ int unit_page(const Params& p, UnitIter& it, int lane
 // Every call commits exactly one cp.async group (possibly empty).
 template <int D, bool FP8, bool SWAP, bool APPEND>
 __device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, int phys, uint8_t* stage,
-                                           int* phys_slot, int lane, uint64_t policy) {
+                                           int* phys_slot, int lane, uint64_t policy, const CopyLanes<D, FP8>& cl) {
     using C = Cfg<D, FP8, SWAP>;
     constexpr int CH = D / 8;  // 16-byte chunks per row (bf16)
     const int j = (it.u - it.seg.start) >> it.seg.sh.nrb_shift;  // key block within the sequence
@@ -288,6 +315,21 @@ __device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, 
             const char* ksrc = reinterpret_cast<const char*>(p.k_pool) + row * D;
             const char* vsrc = reinterpret_cast<const char*>(p.v_pool) +
                                (size_t)(phys * p.Hkv + it.seg.g) * D * p.page_size + sub * UNIT;
+            if (valid == UNIT) {
+                // every K row is valid: no per-row test, addresses from cl
+                using CL = CopyLanes<D, true>;
+                const char* ks = ksrc + cl.src;
+#pragma unroll
+                for (int jj = 0; jj < CL::STEPS; ++jj)
+                    cp_async_16(sbase + jj * CL::RPI * D + cl.dst[jj % CL::SWP], ks + jj * CL::RPI * D, policy);
+                const char* vs = vsrc + (size_t)lane * p.page_size;
+                const size_t vstep = (size_t)32 * p.page_size;
+#pragma unroll
+                for (int jj = 0; jj < D / 32; ++jj)
+                    cp_async_16(sbase + C::UNIT_BYTES + (jj * 32 + lane) * 16, vs + jj * vstep, policy);
+                cp_async_commit();
+                return;
+            }
 #pragma unroll
             for (int i = 0; i < NCH / 32; ++i) {
                 const int q = i * 32 + lane;
@@ -307,7 +349,18 @@ __device__ __forceinline__ void issue_unit(const Params& p, const UnitIter& it, 
             // the sequence), not yet in the pool; that unit (one per sequence and head) is staged
             // by a second copy loop that takes them from k_new / v_new
             const int nf = APPEND ? it.seg.sh.len - it.seg.sh.qlen - tok0 : UNIT;
-            if (APPEND && nf < UNIT) {
+            if (valid == UNIT && nf >= UNIT) {
+                // every row of the unit is in the pool: no per-row test, addresses from cl
+                using CL = CopyLanes<D, false>;
+                const char* ks = ksrc + cl.src;
+                const char* vs = vsrc + cl.src;
+#pragma unroll
+                for (int jj = 0; jj < CL::STEPS; ++jj) {
+                    const uint32_t d = sbase + cl.dst[jj % CL::SWP] + jj * CL::RPI * 128;
+                    cp_async_16(d, ks + jj * CL::RPI * D * 2, policy);
+                    cp_async_16(d + C::UNIT_BYTES, vs + jj * CL::RPI * D * 2, policy);
+                }
+            } else if (APPEND && nf < UNIT) {
                 const size_t nrow = q_row(p, it.seg.b) * p.Hkv + it.seg.g;  // new token 0, head g
                 const char* knew = reinterpret_cast<const char*>(p.k_new + nrow * D);
                 const char* vnew = reinterpret_cast<const char*>(p.v_new + nrow * D);
@@ -503,6 +556,7 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
 
     const uint64_t policy = policy_evict_first();
     uint8_t* my_stages = stages + warp * DEPTH * C::STAGE_BYTES;
+    const CopyLanes<D, FP8> cl(lane);
 
     // per-lane ldmatrix geometry (see the fragment layouts of mma.m16n8k16)
     const int mi = lane >> 3, ri = lane & 7;
@@ -512,6 +566,15 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
     const int v_dsel = mi >> 1;
     const int qr = lane >> 2;       // row group of this lane in mma fragments
     const int qc = (lane & 3) * 2;  // column pair of this lane
+    // this lane's ldmatrix address within a 64-column box for 16-byte chunk 2 k + dsel
+    // (k = 0 .. 3) of its row: A = (v_key, v_dsel), B = (k_key, k_dsel); chunk 2 (k + 4) + dsel
+    // is the same offset in the next box
+    uint32_t offA[4], offB[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        offA[k] = (uint32_t)(v_key * 128 + (((2 * k + v_dsel) ^ (v_key & 7)) << 4));
+        offB[k] = (uint32_t)(k_key * 128 + (((2 * k + k_dsel) ^ (k_key & 7)) << 4));
+    }
 
     const int cidx = vcta;  // this range's chunk
     Seg seg0;
@@ -594,7 +657,8 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
     for (int i = 0; i < DEPTH; ++i) {
         if (!it.done) {
             const int phys = i == 0 ? phys0 : unit_page(p, it, lane);
-            issue_unit<D, FP8, SWAP, APPEND>(p, it, phys, my_stages + i * C::STAGE_BYTES, &s_phys[warp][i], lane, policy);
+            issue_unit<D, FP8, SWAP, APPEND>(p, it, phys, my_stages + i * C::STAGE_BYTES, &s_phys[warp][i], lane, policy,
+                                             cl);
             it.u += W;
             it.norm(p, warp);
         } else {
@@ -719,9 +783,7 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
                 } else {
 #pragma unroll
                     for (int kk = 0; kk < KSTEPS; ++kk) {
-                        const int dch = kk * 2 + v_dsel;
-                        const uint32_t addr =
-                            kb + (dch >> 3) * C::BOX_BYTES + v_key * 128 + (((dch & 7) ^ (v_key & 7)) << 4);
+                        const uint32_t addr = kb + (kk >> 2) * C::BOX_BYTES + offA[kk & 3];
                         uint32_t a[4];
                         ldsm_x4(addr, a[0], a[1], a[2], a[3]);
                         mma_16816((kk & 1) ? sb : sa, a, qa[kk][0], qa[kk][1]);
@@ -776,9 +838,7 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
                 } else {
 #pragma unroll
                     for (int n = 0; n < D / 16; ++n) {
-                        const int dch = n * 2 + k_dsel;
-                        const uint32_t addr =
-                            vb + (dch >> 3) * C::BOX_BYTES + k_key * 128 + (((dch & 7) ^ (k_key & 7)) << 4);
+                        const uint32_t addr = vb + (n >> 2) * C::BOX_BYTES + offB[n & 3];
                         uint32_t a[4];
                         ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
                         mma_16816(o[n], a, b0, b1);
@@ -821,9 +881,7 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
                 } else {
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; ++kk) {
-                    const int dch = kk * 2 + k_dsel;
-                    const uint32_t addr =
-                        kb + (dch >> 3) * C::BOX_BYTES + k_key * 128 + (((dch & 7) ^ (k_key & 7)) << 4);
+                    const uint32_t addr = kb + (kk >> 2) * C::BOX_BYTES + offB[kk & 3];
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4(addr, b0, b1, b2, b3);
                     if (kk & 1) {
@@ -906,9 +964,7 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
                 // O += P V
 #pragma unroll
                 for (int jj = 0; jj < D / 16; ++jj) {
-                    const int dch = jj * 2 + v_dsel;
-                    const uint32_t addr =
-                        vb + (dch >> 3) * C::BOX_BYTES + v_key * 128 + (((dch & 7) ^ (v_key & 7)) << 4);
+                    const uint32_t addr = vb + (jj >> 2) * C::BOX_BYTES + offA[jj & 3];
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4_trans(addr, b0, b1, b2, b3);
                     mma_16816(o[2 * jj], pa, b0, b1);
@@ -944,7 +1000,7 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
             if (!it.done) {
                 const int phys_next = unit_page(p, it, lane);
                 issue_unit<D, FP8, SWAP, APPEND>(p, it, phys_next, my_stages + st * C::STAGE_BYTES,
-                                                 &s_phys[warp][st], lane, policy);
+                                                 &s_phys[warp][st], lane, policy, cl);
                 it.u += W;
                 it.norm(p, warp);
             } else {
