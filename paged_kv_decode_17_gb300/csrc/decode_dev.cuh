@@ -683,7 +683,7 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
         // Q fragments of this warp's rows (rows >= my_rows are zero) and the
         // number of keys each of the lane's two rows may see
         uint32_t qa[KSTEPS][4];
-        int lim0 = cs.sh.len, lim1 = cs.sh.len;
+        int lim0 = cs.sh.len, lim1 = cs.sh.len, lim_all;
         // this lane's two softmax rows
         const int rA = swp ? (lane & 3) * 2 : qr, rB = swp ? rA + 1 : qr + 8;
         {
@@ -698,6 +698,8 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
                 if (rA < my_rows) lim0 = qlast + fa / p.group + 1;
                 if (rB < my_rows) lim1 = qlast + fb / p.group + 1;
             }
+            // units ending at or below every row's limit need no mask
+            lim_all = __reduce_min_sync(0xffffffffu, min(lim0, lim1));
             const uint32_t* q0 = reinterpret_cast<const uint32_t*>(p.q + ((qrow + (r0ok ? i0 : 0)) * p.Hq + h0) * D);
             const uint32_t* q8 = reinterpret_cast<const uint32_t*>(p.q + ((qrow + (r8ok ? i8 : 0)) * p.Hq + h8) * D);
             if constexpr (FP8) {
@@ -790,10 +792,14 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
                     }
                 }
                 // scale, mask: element 0 / 1 = (keyA, rows rA / rB), 2 / 3 = (keyB, rows rA / rB)
-                const float x0 = keyA < vis0 ? (sa[0] + sb[0]) * sl : -INFINITY;
-                const float x1 = keyA < vis1 ? (sa[1] + sb[1]) * sl : -INFINITY;
-                const float x2 = keyB < vis0 ? (sa[2] + sb[2]) * sl : -INFINITY;
-                const float x3 = keyB < vis1 ? (sa[3] + sb[3]) * sl : -INFINITY;
+                float x0 = (sa[0] + sb[0]) * sl, x1 = (sa[1] + sb[1]) * sl;
+                float x2 = (sa[2] + sb[2]) * sl, x3 = (sa[3] + sb[3]) * sl;
+                if (tok0 + UNIT > lim_all) {
+                    x0 = keyA < vis0 ? x0 : -INFINITY;
+                    x1 = keyA < vis1 ? x1 : -INFINITY;
+                    x2 = keyB < vis0 ? x2 : -INFINITY;
+                    x3 = keyB < vis1 ? x3 : -INFINITY;
+                }
                 float rm0 = fmaxf(x0, x2), rm1 = fmaxf(x1, x3);
 #pragma unroll
                 for (int o_ = 4; o_ < 32; o_ <<= 1) {
@@ -900,11 +906,17 @@ __device__ __forceinline__ void decode_body(const Params& p, const int vcta, con
                 // scale to log2 domain, mask keys past the sequence end or the row's position
                 float x[2][4];
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
+                for (int j = 0; j < 2; ++j)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int key = FP8 ? (lane & 3) * 4 + 2 * j + (e & 1) : j * 8 + qc + (e & 1);
-                        x[j][e] = key < ((e & 2) ? vis1 : vis0) ? s[j][e] * sl : -INFINITY;
+                    for (int e = 0; e < 4; ++e) x[j][e] = s[j][e] * sl;
+                if (tok0 + UNIT > lim_all) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int key = FP8 ? (lane & 3) * 4 + 2 * j + (e & 1) : j * 8 + qc + (e & 1);
+                            if (key >= ((e & 2) ? vis1 : vis0)) x[j][e] = -INFINITY;
+                        }
                     }
                 }
                 float rm0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
