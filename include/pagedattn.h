@@ -286,7 +286,9 @@ int kv_write_paged(void* k_pool, void* v_pool, int num_pages, const void* k_new,
  *   q_norm_weight, k_norm_weight  bf16 [head_dim] or NULL (no normalisation)
  *   norm_eps       >= 0 and finite
  * Angles are reduced exactly (64-bit fixed-point turns), so positions up to
- * 2^31 keep full fp32 accuracy.
+ * 2^31 keep full fp32 accuracy.  A row whose block-table entry lies outside
+ * the pool records PA_ERR_BAD_PAGE and writes no K/V; its query rows are
+ * still normalised and rotated (they do not depend on the page).
  */
 int kv_write_paged_rope(void* k_pool, void* v_pool, int num_pages, const void* k_new, const void* v_new,
                         void* q, int num_q_heads, const int32_t* cu_seqlens_new, const int32_t* seq_lens,

@@ -258,11 +258,8 @@ __global__ void __launch_bounds__(kWarps * 32) kv_write_rope_kernel(const __grid
             if (lane == 0) report(p.status, PA_ERR_BAD_LEN);
             continue;
         }
+        // the page is looked up now and used after the query rows, which need only the position
         const int phys = __ldg(p.block_table + (size_t)b * p.max_pages + pos / p.page_size);
-        if (phys < 0 || phys >= p.num_pages) {
-            if (lane == 0) report(p.status, PA_ERR_BAD_PAGE);
-            continue;
-        }
         const int slot = pos % p.page_size;
         // cos / sin of this position's angles, one pair at a time
         float c[PPL], s[PPL];
@@ -271,6 +268,29 @@ __global__ void __launch_bounds__(kWarps * 32) kv_write_rope_kernel(const __grid
             const unsigned long long turn = (unsigned long long)pos * p.turns[lane * PPL + j];  // mod 2^64
             const float frac = (float)(unsigned)(turn >> 40) * 0x1p-24f;                     // exact
             sincospif(2.f * frac, &s[j], &c[j]);
+        }
+        if (p.q != nullptr) {
+            __nv_bfloat16* qrow = p.q + (size_t)t * p.Hq * D;
+            // eight head rows per batch of loads: one warp keeps 2 KB in flight
+            int h = 0;
+            for (; h + 8 <= p.Hq; h += 8) {
+                __nv_bfloat16* qd[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) qd[k] = qrow + (h + k) * D;
+                rope_rows<D, 8>(qrow + h * D, D, qd, p.q_norm_w, p.eps, lane, c, s);
+            }
+            for (; h + 4 <= p.Hq; h += 4) {
+                __nv_bfloat16* qd[4] = {qrow + h * D, qrow + (h + 1) * D, qrow + (h + 2) * D, qrow + (h + 3) * D};
+                rope_rows<D, 4>(qrow + h * D, D, qd, p.q_norm_w, p.eps, lane, c, s);
+            }
+            for (; h < p.Hq; ++h) {
+                __nv_bfloat16* qd[1] = {qrow + h * D};
+                rope_rows<D, 1>(qrow + h * D, D, qd, p.q_norm_w, p.eps, lane, c, s);
+            }
+        }
+        if (phys < 0 || phys >= p.num_pages) {
+            if (lane == 0) report(p.status, PA_ERR_BAD_PAGE);
+            continue;
         }
         // K heads (rotated) and V heads (copied), four at a time
         for (int g0 = 0; g0 < p.Hkv; g0 += 4) {
@@ -292,25 +312,6 @@ __global__ void __launch_bounds__(kWarps * 32) kv_write_rope_kernel(const __grid
 #pragma unroll
             for (int h = 0; h < 4; ++h)
                 if (h < nh) PairIO<D>::store(kd[h] - p.k_pool + p.v_pool, lane, v1[h], v2[h]);  // exact copy
-        }
-        if (p.q != nullptr) {
-            __nv_bfloat16* qrow = p.q + (size_t)t * p.Hq * D;
-            // eight head rows per batch of loads: one warp keeps 2 KB in flight
-            int h = 0;
-            for (; h + 8 <= p.Hq; h += 8) {
-                __nv_bfloat16* qd[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) qd[k] = qrow + (h + k) * D;
-                rope_rows<D, 8>(qrow + h * D, D, qd, p.q_norm_w, p.eps, lane, c, s);
-            }
-            for (; h + 4 <= p.Hq; h += 4) {
-                __nv_bfloat16* qd[4] = {qrow + h * D, qrow + (h + 1) * D, qrow + (h + 2) * D, qrow + (h + 3) * D};
-                rope_rows<D, 4>(qrow + h * D, D, qd, p.q_norm_w, p.eps, lane, c, s);
-            }
-            for (; h < p.Hq; ++h) {
-                __nv_bfloat16* qd[1] = {qrow + h * D};
-                rope_rows<D, 1>(qrow + h * D, D, qd, p.q_norm_w, p.eps, lane, c, s);
-            }
         }
     }
 }
