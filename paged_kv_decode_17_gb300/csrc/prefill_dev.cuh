@@ -256,6 +256,18 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// 32 lanes x 8 columns of 32-bit: thread t of the warp loads / stores its lane's 8 columns.
+__device__ __forceinline__ void ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 // max of three (one instruction on sm_100 and later)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float m;
@@ -848,13 +860,13 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                         if (!ok) break;
                         tc::fence_after_sync();
 #pragma unroll 1
-                        for (int c0 = 0; c0 < D; c0 += 32) {
-                            uint32_t o[32];
-                            tc::ld_32x32b_x32(t_o + c0, o);
+                        for (int c0 = 0; c0 < D; c0 += 8) {  // 8 columns at a time: the score row stays live
+                            uint32_t o[8];
+                            ld_32x32b_x8(t_o + c0, o);
                             tc::wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                            tc::st_32x32b_x32(t_o + c0, o);
+                            for (int i = 0; i < 8; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                            st_32x32b_x8(t_o + c0, o);
                         }
                         tc::wait_st();
                         l *= alpha;
