@@ -101,6 +101,21 @@ int encode_rows_map_noswizzle(CUtensorMap* map, const void* base, uint64_t rows,
     return encode_impl(map, base, rows, row_elems, box_cols, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+int encode_blocks_map(CUtensorMap* map, const void* base, uint64_t blocks) {
+    std::call_once(g_encode_once, load_encode);
+    if (g_encode == nullptr) return PA_ERR_CUDA;
+    // a 16-row block of 128-column bf16 rows (4 KB) in the order [row half][column block][row][column]:
+    // dimension 1 (rows) steps 256 bytes, dimension 2 (column block) 128, dimension 3 (row half) 2048
+    cuuint64_t dims[5] = {64, 8, 2, 2, blocks};
+    cuuint64_t strides[4] = {256, 128, 2048, 4096};
+    cuuint32_t box[5] = {64, 8, 2, 2, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 int encode_q_map(CUtensorMap* map, const void* q, int total_q, int Hq, int D) {
     std::call_once(g_encode_once, load_encode);
     if (g_encode == nullptr) return PA_ERR_CUDA;

@@ -38,6 +38,8 @@ int encode_rows_map_noswizzle(CUtensorMap* map, const void* base, uint64_t rows,
 
 // 3-D bf16 tensor map over q [total_q][Hq][D] with box {64, 1, 128} and
 // 128-byte swizzle: one head's 128-row tile, 64 columns at a time.
+// K or V pool at head_dim 128 as 16-row blocks: one box = one block (see pf::Cfg::BLK4).
+int encode_blocks_map(CUtensorMap* map, const void* base, uint64_t blocks);
 int encode_q_map(CUtensorMap* map, const void* q, int total_q, int Hq, int D);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

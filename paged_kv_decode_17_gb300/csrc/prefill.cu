@@ -189,8 +189,13 @@ extern "C" int attn_prefill_varlen_causal(void* out, float* lse, const void* q, 
     CUtensorMap qmap, kmap, vmap, omap;
     if (encode_q_map(&qmap, q, total_q, num_q_heads, head_dim) != PA_OK) return PA_ERR_CUDA;
     if (encode_q_map(&omap, out, total_q, num_q_heads, head_dim) != PA_OK) return PA_ERR_CUDA;
-    if (encode_rows_map(&kmap, k_pool, (uint64_t)pool_rows, head_dim, 64, 16) != PA_OK) return PA_ERR_CUDA;
-    if (encode_rows_map(&vmap, v_pool, (uint64_t)pool_rows, head_dim, 64, 16) != PA_OK) return PA_ERR_CUDA;
+    if (head_dim == 128 && !pair) {  // one TMA box per 16-key page block (pf::Cfg::BLK4)
+        if (encode_blocks_map(&kmap, k_pool, (uint64_t)pool_rows / 16) != PA_OK) return PA_ERR_CUDA;
+        if (encode_blocks_map(&vmap, v_pool, (uint64_t)pool_rows / 16) != PA_OK) return PA_ERR_CUDA;
+    } else {
+        if (encode_rows_map(&kmap, k_pool, (uint64_t)pool_rows, head_dim, 64, 16) != PA_OK) return PA_ERR_CUDA;
+        if (encode_rows_map(&vmap, v_pool, (uint64_t)pool_rows, head_dim, 64, 16) != PA_OK) return PA_ERR_CUDA;
+    }
 
     pf::Params prm;
     prm.out = static_cast<__nv_bfloat16*>(out);

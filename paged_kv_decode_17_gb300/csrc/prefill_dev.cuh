@@ -85,6 +85,11 @@ template <int D, bool PAIR = false>
 struct Cfg {
     static_assert(!PAIR || D == 128, "a CTA pair splits V into two 128-byte column blocks");
     static constexpr int KB = D / 64;               // 128-byte column blocks per row
+    // BLK4: a 16-key page block (16 rows x 256 bytes, contiguous in the pool) is one TMA box,
+    // landing as [row half][column block][8 rows][128 bytes], so a stage holds page block u at
+    // u * 4096 and every 8-row swizzle atom of one column block sits 2048 bytes after the last.
+    // Otherwise (head_dim 64, CTA pairs) a box is 16 rows of one column block, stages [kb][u].
+    static constexpr bool BLK4 = !PAIR && D == 128;
     static constexpr int NKr = PAIR ? PNK : NK;     // ring depths
     static constexpr int NVr = PAIR ? PNV : NV;
     static constexpr int NST = NKr + NVr;
@@ -245,6 +250,16 @@ __device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, Shared& 
             return false;
         }
     }
+}
+
+// One 16-key page block of a pool (5-D map: 64 columns, 8 rows, column block, row half,
+// 16-row block of the pool); the other coordinates are 0.
+__device__ __forceinline__ void tma_load_block(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int blk) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %3, %3, %3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(0), "r"(blk)
+        : "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
@@ -551,7 +566,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                     // both column blocks), V columns 64 r .. 64 r + 63 of every block.
                     int u, kb, off;
                     bool has;
-                    if (!PAIR) {
+                    if (C::BLK4) {
+                        u = lane;
+                        kb = 0;
+                        has = lane < UPT;
+                        off = u * 4096;
+                    } else if (!PAIR) {
                         u = lane / C::KB;
                         kb = lane - u * C::KB;
                         has = lane < UPT * C::KB;
@@ -582,6 +602,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                         if (mine) {
                             if (PAIR)
                                 tma_load_2d_pair(dst + off, map, map_cta(&sh.kv_full[st], 0), kb * 64, box_row);
+                            else if (C::BLK4)
+                                tma_load_block(dst + off, map, &sh.kv_full[st], box_row >> 4);
                             else
                                 tma_load_2d(dst + off, map, &sh.kv_full[st], kb * 64, box_row);
                         }
@@ -597,7 +619,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                                 mbar_arrive_expect_tx(&sh.v_tail, own_bytes);
                         }
                         __syncwarp();
-                        if (mine) tma_load_2d(dst + off, map, &sh.v_tail, kb * 64, box_row);
+                        if (mine) {
+                            if (C::BLK4)
+                                tma_load_block(dst + off, map, &sh.v_tail, box_row >> 4);
+                            else
+                                tma_load_2d(dst + off, map, &sh.v_tail, kb * 64, box_row);
+                        }
                         ++tails_armed;
                         v_open[st - NKr] = true;
                         ok = __all_sync(0xffffffffu, wait_ab(&sh.v_tail, tails & 1, sh, p));
@@ -609,8 +636,9 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                             const int cb = c / ((BN - first) * 8);
                             const int rem = c - cb * (BN - first) * 8;
                             const int r = first + rem / 8;
-                            *reinterpret_cast<uint4*>(dst + cb * C::KV_KB + r * 128 + (rem & 7) * 16) =
-                                make_uint4(0, 0, 0, 0);
+                            const int roff = C::BLK4 ? (r >> 4) * 4096 + ((r >> 3) & 1) * 2048 + cb * 1024 + (r & 7) * 128
+                                                     : cb * C::KV_KB + r * 128;
+                            *reinterpret_cast<uint4*>(dst + roff + (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
@@ -718,7 +746,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                             const uint64_t ad =
                                 tc::smem_desc_sw128(qaddr + (kk >> 2) * C::Q_KB + (kk & 3) * 32, 16, 1024);
                             const uint64_t bd =
-                                tc::smem_desc_sw128(kaddr + (kk >> 2) * C::K_KB + (kk & 3) * 32, 16, 1024);
+                                C::BLK4 ? tc::smem_desc_sw128(kaddr + (kk >> 2) * 1024 + (kk & 3) * 32, 16, 2048)
+                                        : tc::smem_desc_sw128(kaddr + (kk >> 2) * C::K_KB + (kk & 3) * 32, 16, 1024);
                             mma(t_s, ad, bd, C::IDESC_S, kk > 0);
                         }
                         commit_to(&sh.s_full[hh]);
@@ -730,7 +759,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                         for (int kk = 0; kk < BN / 16; ++kk) {
                             const uint64_t ad =
                                 tc::smem_desc_sw128(paddr + (kk >> 2) * C::P_KB + (kk & 3) * 32, 16, 1024);
-                            const uint64_t bd = tc::smem_desc_sw128(vaddr + kk * 2048, C::KV_KB, 1024);
+                            const uint64_t bd = C::BLK4 ? tc::smem_desc_sw128(vaddr + kk * 4096, 1024, 2048)
+                                                        : tc::smem_desc_sw128(vaddr + kk * 2048, C::KV_KB, 1024);
                             mma(t_o, ad, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
                         }
                         commit_to(&sh.pv_done[hh]);
