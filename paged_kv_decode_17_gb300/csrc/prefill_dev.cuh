@@ -488,6 +488,15 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
                 itm.qmin = itm.seq_len - itm.q_len + itm.t * BM;
                 itm.n_kv = (itm.qmin + itm.rows_valid - 1) / BN + 1;
             }
+            // block-table entries of four key tiles at a time, one per lane (tile t0 + lane / 8,
+            // page block lane % 8), loaded four tiles before they are used, so the table's
+            // latency hides behind the copies; the first four load while this item is published
+            const int32_t* btab = itm.end ? p.block_table : p.block_table + (size_t)itm.b * p.max_pages;
+            auto fetch4 = [&](int t0) -> int {
+                const int key0 = (t0 + (lane >> 3)) * BN + (lane & 7) * 16;
+                return (!itm.end && key0 < itm.seq_len) ? __ldg(btab + key0 / p.page_size) : -1;
+            };
+            int ent_next = fetch4(0);
             const int slot = k & 1;
             ok = __all_sync(0xffffffffu, wait_ab(&sh.item_empty[slot], ((k >> 1) & 1) ^ 1, sh, p));
             if (!ok) break;
@@ -523,29 +532,25 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
             }
             if (!ok) break;
 
-            // ---- K / V tiles.  A tile is UPT x KB boxes: 16-key page blocks x 64-column halves,
-            // box b issued by lane b.  Lane u < UPT resolves block u of a tile through the block
-            // table one tile ahead.
-            const int32_t* btab = p.block_table + (size_t)itm.b * p.max_pages;
-            auto block_row = [&](int j) -> int {  // pool row of block `lane` of tile j, -1 if none
-                int row = -1;
-                if (lane < UPT && j < itm.n_kv) {
+            // ---- K / V tiles.  A tile is UPT x KB boxes: 16-key page blocks x 64-column halves
+            // (one box per block at head_dim 128).  Lane u < UPT holds the pool row of block u.
+            int ent = -1;
+            for (int j = 0; j < itm.n_kv && ok; ++j) {
+                if ((j & 3) == 0) {
+                    ent = ent_next;
+                    ent_next = fetch4(j + 4);
+                }
+                const int phys = __shfl_sync(0xffffffffu, ent, ((j & 3) << 3) + (lane & 7));
+                int my_row = -1;  // pool row of block `lane` of tile j, -1 if none
+                if (lane < UPT) {
                     const int key0 = j * BN + lane * 16;
                     if (key0 < itm.seq_len) {
-                        const int page = key0 / p.page_size;
-                        const int phys = __ldg(btab + page);
                         if (phys < 0 || phys >= p.num_pages)
                             report(p.status, PA_ERR_BAD_PAGE);
                         else
-                            row = (phys * p.Hkv + itm.g) * p.page_size + (key0 - page * p.page_size);
+                            my_row = (phys * p.Hkv + itm.g) * p.page_size + key0 % p.page_size;
                     }
                 }
-                return row;
-            };
-            int next_row = block_row(0);
-            for (int j = 0; j < itm.n_kv && ok; ++j) {
-                const int my_row = next_row;
-                next_row = block_row(j + 1);
                 const unsigned goodmask = __ballot_sync(0xffffffffu, my_row >= 0) & ((1u << UPT) - 1);
                 const int good = __popc(goodmask);
                 const bool tail = (j + 1) * BN > itm.seq_len;
