@@ -20,10 +20,12 @@
 // * warp 8 (producer): publishes each item through a 2-slot ring in shared
 //   memory, loads the two Q tiles by TMA (3-D tensor map over [rows][Hq][D],
 //   128-byte swizzle) and gathers K and V tiles: a 128-key tile is eight
-//   16-row page blocks found through the block table (one tile ahead), each
-//   64-column half a 128-byte-swizzled TMA box.  K and V tiles have
-//   separate rings (1 and 2 stages), so the next K tile loads as soon as the
-//   current scores are computed.
+//   16-row page blocks found through the block table (entries loaded four
+//   tiles ahead), each one 128-byte-swizzled TMA box of 4 KB at head_dim 128
+//   (see Cfg::BLK4; a warp issues about one copy per 110 cycles, so fewer,
+//   larger boxes move the tile sooner).  K and V tiles have separate rings
+//   (1 and 2 stages), so the next K tile loads as soon as the current scores
+//   are computed.
 // * warps 9 / 10 (MMA, one per head): one thread issues tcgen05.mma:
 //   S_h = Q_h K^T into TMEM (fp32, 128 columns) and O_h += P_h V into TMEM
 //   (fp32, D columns); the next tile's scores are issued as soon as the
