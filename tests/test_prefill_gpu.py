@@ -46,6 +46,9 @@ CASES = [
     ("d64", [400, 129], [400, 60], 8, 2, 64, 16),
     ("page32", [500, 77], [300, 77], 8, 2, 128, 32),
     ("page64", [260, 1000], [260, 500], 4, 1, 128, 64),
+    # several 16-key blocks per page (one TMA box per block)
+    ("page128", [700, 300], [700, 130], 8, 2, 128, 128),
+    ("page256", [1100, 513], [600, 513], 4, 2, 128, 256),
     ("mixed_decode_rows", [900, 1, 77, 3000, 256], [256, 1, 1, 1, 256], 32, 8, 128, 16),
     # one-row entries (swapped operand order: group x 1 <= 8 rows) next to 2-8-row blocks (plain
     # order) and a prefill chunk in the same call

@@ -390,7 +390,8 @@ def llama8b_ragged_small(seed: int = 2, device="cpu") -> PagedCase:
 def awkward_cases(device="cpu", seed: int = 10) -> Dict[str, PagedCase]:
     """Small cases at the places fast paths skip work: one-token contexts,
     partially filled pages, contexts 127 and 4096, batch 1 and 32, extreme
-    logits, an empty sequence, GQA groups 1..8, head_dim 64 and 128."""
+    logits, an empty sequence, GQA groups 1..8, head_dim 64 and 128, pages of
+    16, 64 and 256 tokens."""
     cases = {}
     cases["one_token"] = make_paged_case("one_token", [1, 1, 1], [1, 1, 1], 8, 2, 128, seed=seed, device=device)
     cases["ctx127_b1"] = make_paged_case("ctx127_b1", [127], [1], 8, 8, 128, num_pages=20, seed=seed + 1, device=device)
@@ -406,4 +407,6 @@ def awkward_cases(device="cpu", seed: int = 10) -> Dict[str, PagedCase]:
     cases["group32_mqa"] = make_paged_case("group32_mqa", [129, 700], [1, 1], 32, 1, 64, seed=seed + 8, device=device)
     cases["page64"] = make_paged_case("page64", [100, 300], [1, 1], 8, 2, 128, page_size=64, seed=seed + 9,
                                       device=device)
+    cases["page256"] = make_paged_case("page256", [600, 257, 1], [1, 1, 1], 8, 2, 128, page_size=256,
+                                       seed=seed + 10, device=device)
     return cases
