@@ -81,7 +81,10 @@
  *
  * Supported shapes: head_dim 64 or 128; page_size a power of two from 16 to
  * 256; num_q_heads a multiple of num_kv_heads; num_q_heads / num_kv_heads
- * up to 128.
+ * up to 128.  The pools, q, out, k_new and v_new must start on a 16-byte
+ * boundary (PA_ERR_SHAPE otherwise: the kernels move 16-byte vectors, and
+ * the prefill moves whole 16-row page blocks with bulk tensor copies); a
+ * workspace must start on a 256-byte boundary (PA_ERR_WORKSPACE otherwise).
  *
  * Errors: a negative return value is a pa_status detected on the host
  * before anything is launched (nothing was enqueued).  Errors found on the
