@@ -141,6 +141,33 @@ def test_fused_path_repeated_calls_bit_identical(cuda_device):
     assert torch.equal(ob1.view(torch.int16), ob2.view(torch.int16)) and torch.equal(lb1, lb2)
 
 
+def test_fused_path_back_to_back_calls_share_a_workspace(cuda_device):
+    """32 mixed calls queued back to back on one stream (each launch may start while
+    the previous one's merge runs) with one workspace and one status word: the
+    status stays clean and the last result equals a lone call's."""
+    pa = _pa()
+    c = workloads.make_paged_case("b2b", [1500, 1, 3000, 64, 700], [400, 1, 1, 64, 129], 32, 8, 128,
+                                  seed=72).to(cuda_device)
+    ws = pa.Workspace(pa.prefill_workspace_bytes(c.batch, c.total_q, c.num_q_heads, c.num_kv_heads, c.head_dim),
+                      cuda_device)
+    status = pa.new_status(cuda_device)
+    out = torch.empty_like(c.q)
+
+    def call():
+        pa.attn_prefill_varlen_causal(c.q, c.k_pool, c.v_pool, c.block_table, c.cu_seqlens_q, c.seq_lens,
+                                      c.softmax_scale, max_q_len=c.max_q_len, max_seq_len=c.max_seq_len, out=out,
+                                      workspace=ws, status=status)
+
+    call()
+    torch.cuda.synchronize()
+    want = out.clone()
+    for _ in range(32):
+        call()
+    torch.cuda.synchronize()
+    pa.check_status(status, "back-to-back mixed calls")
+    assert torch.equal(out.view(torch.int16), want.view(torch.int16))
+
+
 def test_prefill_sharp_logits(cuda_device):
     case = workloads.make_paged_case("sharp", [700, 300], [700, 150], 8, 2, 128, k_scale=8.0, seed=60)
     _check(case, cuda_device)
