@@ -46,6 +46,9 @@ CASES = [
     ("d64", [400, 129], [400, 60], 8, 2, 64, 16),
     ("page32", [500, 77], [300, 77], 8, 2, 128, 32),
     ("page64", [260, 1000], [260, 500], 4, 1, 128, 64),
+    # the boundary between the two paths: 8 rows (split-K decode) next to 9 rows (prefill tiles),
+    # with and without cached tokens before them
+    ("q8_q9_boundary", [9, 500, 8, 300, 17], [9, 9, 8, 8, 17], 8, 2, 128, 16),
     # several 16-key blocks per page (one TMA box per block)
     ("page128", [700, 300], [700, 130], 8, 2, 128, 128),
     ("page256", [1100, 513], [600, 513], 4, 2, 128, 256),
