@@ -338,7 +338,8 @@ __device__ __forceinline__ int seq_tiles(const int32_t* cu_q, const int32_t* seq
 
 // ---------------------------------------------------------------------------------- items
 // Where the producer finds this CTA's k-th work item.  Without a counter: the static
-// round-robin walk blockIdx.x + k * gridDim.x of the sorted list.  With one: the next
+// round-robin walk blockIdx.x + k * gridDim.x of the sorted list (head slots rotated by
+// the tile index).  With one: the next
 // unclaimed item, one fetch-and-add on a 64-bit counter, so CTAs that finish earlier
 // work take more items.  The plan is then built inside the same launch: whoever builds
 // it sets the counter to (tag << 32) before it publishes plan_flag = (tag << 32) | 1,
@@ -471,7 +472,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap& qmap, const CUte
             if (!itm.end) {
                 const int per = p.Hkv * p.NPC;
                 const int ti = (int)(it / per);
-                const int rem = (int)(it - (long long)ti * per);
+                int rem = (int)(it - (long long)ti * per);
+                // the static round-robin (no counter) hands a CTA every gridDim-th item; with
+                // gridDim a multiple of per, it would always draw the same head slot, so the
+                // CTAs drawing a group's lone last head would idle at the end: rotate the slots
+                // by the tile index (a permutation within each tile)
+                if (src.counter == nullptr) rem = (rem + ti) % per;
                 itm.g = rem / p.NPC;
                 const int pair = rem - itm.g * p.NPC;  // (CTA pairs: block of 4 heads)
                 const int2 bt = __ldcg(p.tiles + ti);
