@@ -128,6 +128,9 @@ __device__ __forceinline__ void build_plan(const MixParams& mp, const int t, int
     for (int b = t; b < f.batch; b += 128) {
         int ql, sl;
         const int nt = pf::seq_tiles(f.cu_q, f.seq_lens, b, mp.cap, nullptr, ql, sl);
+        // eight slot claims in flight at a time: each is an L2 round trip, and the other
+        // CTAs wait for this list (a sequence's tiles mostly have distinct costs, so distinct counters)
+#pragma unroll 8
         for (int i = 0; i < nt; ++i) {
             const int rows = min(pf::BM, ql - i * pf::BM);
             const int cost = min(mp.max_cost, (sl - ql + i * pf::BM + rows - 1) / pf::BN + 1);
